@@ -1,0 +1,295 @@
+"""Seeded synthetic inputs for FP8 paged decode attention and cache append.
+
+This module holds no step of the method: it draws raw FP32 tensors (N(0,1)),
+sequence lengths, paged block tables and slot mappings. Quantisation to E4M3
+and everything after it is done separately by the CUDA library and by the
+CPU oracle. Both sides take their inputs from here.
+
+Workloads (sizes from the GLM-4.5 decode setting; D = 128, block_size = 128):
+  tiny     B=2,  S1=1, NQ=4,  NKV=1, kv lengths {37, 300}, 8 physical blocks
+  glm      B=16, S1=1, NQ=96, NKV=8, lengths ~ U{1..4096}, s2_tile 512
+  long     B=4,  S1=1, NQ=96, NKV=8, lengths ~ U{32768..131072}; every 64th
+           K row scaled by 8 before quantisation (outlier tokens)
+  ragged   B=256, S1=2, NQ=96, NKV=8, lengths lognormal(median 1024, sigma 1)
+           clipped to [1, 16384]
+  append   64 new tokens (one per sequence) over contexts ~ U{512..8192},
+           BNBD cache; 5% of the new slots are -1 (skipped)
+The block pool holds the needed blocks plus 10% spare; each sequence's block
+table row is a slice of a random permutation of the pool, padded with -1.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+LAYOUT_BSND = 0
+LAYOUT_BNBD = 1
+BASE_SEED = 20261202
+
+
+def _rng(seed: int, *stream) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, *stream])))
+
+
+@dataclasses.dataclass
+class DecodeCase:
+    """One paged decode workload. Raw tensors are drawn lazily and cached."""
+
+    name: str
+    B: int
+    S1: int
+    NQ: int
+    NKV: int
+    act: np.ndarray            # int32 [B] kv_act_seqs
+    max_blocks: int
+    num_blocks: int
+    block_table: np.ndarray    # int32 [B, max_blocks], -1 padded
+    seed: int
+    D: int = 128
+    BS: int = 128
+    s2_tile: int = 512
+    layout: int = LAYOUT_BSND
+    k_outlier_every: int = 0   # every n-th token row of K is scaled by k_outlier_scale
+    k_outlier_scale: float = 8.0
+
+    def __post_init__(self):
+        self._q = None
+        self._kv = None
+
+    # ---- derived integer structure ------------------------------------
+    @property
+    def group(self) -> int:
+        return self.NQ // self.NKV
+
+    @property
+    def softmax_scale(self) -> float:
+        return float(np.float32(1.0) / np.sqrt(np.float32(self.D)))
+
+    @property
+    def cu_seqlens(self) -> np.ndarray:
+        cu = np.zeros(self.B + 1, dtype=np.int64)
+        cu[1:] = np.cumsum(np.maximum(self.act, 0).astype(np.int64))
+        return cu
+
+    @property
+    def total_tokens(self) -> int:
+        return int(np.maximum(self.act, 0).astype(np.int64).sum())
+
+    @property
+    def token_batch(self) -> np.ndarray:
+        """int32 [Ttot]: the batch of each context token."""
+        return np.repeat(np.arange(self.B, dtype=np.int32),
+                         np.maximum(self.act, 0).astype(np.int64))
+
+    @property
+    def token_pos(self) -> np.ndarray:
+        """int64 [Ttot]: the position of each context token in its sequence."""
+        cu = self.cu_seqlens
+        tb = self.token_batch
+        return np.arange(self.total_tokens, dtype=np.int64) - cu[tb]
+
+    @property
+    def slots(self) -> np.ndarray:
+        """int64 [Ttot]: physical cache slot of each context token,
+        block_table[b][j // BS] * BS + j % BS."""
+        tb = self.token_batch
+        j = self.token_pos
+        return self.block_table[tb, j // self.BS].astype(np.int64) * self.BS + j % self.BS
+
+    # ---- raw FP32 tensors ------------------------------------------------
+    def q(self) -> np.ndarray:
+        """float32 [B*S1, NQ, D], N(0,1)."""
+        if self._q is None:
+            self._q = _rng(self.seed, 1).standard_normal(
+                (self.B * self.S1, self.NQ, self.D), dtype=np.float32)
+        return self._q
+
+    def kv(self):
+        """(k, v) float32 [Ttot, NKV, D], N(0,1), sequences concatenated in
+        batch order (cu_seqlens). Drawn per sequence from its own stream."""
+        if self._kv is None:
+            T = self.total_tokens
+            k = np.empty((T, self.NKV, self.D), dtype=np.float32)
+            v = np.empty((T, self.NKV, self.D), dtype=np.float32)
+            cu = self.cu_seqlens
+            for b in range(self.B):
+                n = int(cu[b + 1] - cu[b])
+                if n == 0:
+                    continue
+                r = _rng(self.seed, 2, b)
+                kb = r.standard_normal((n, self.NKV, self.D), dtype=np.float32)
+                vb = r.standard_normal((n, self.NKV, self.D), dtype=np.float32)
+                if self.k_outlier_every:
+                    kb[:: self.k_outlier_every] *= np.float32(self.k_outlier_scale)
+                k[cu[b]:cu[b + 1]] = kb
+                v[cu[b]:cu[b + 1]] = vb
+            self._kv = (k, v)
+        return self._kv
+
+    def drop(self):
+        """Forget the cached raw tensors."""
+        self._q = None
+        self._kv = None
+
+    # ---- byte accounting (valid tokens only) -----------------------------
+    def algorithmic_bytes(self) -> int:
+        """Bytes one decode step must move at minimum: K, V and k_scale of the
+        valid tokens, q and q_scale, v_scale, the BF16 output, block table and
+        lengths."""
+        B, S1, NQ, NKV, D = self.B, self.S1, self.NQ, self.NKV, self.D
+        return (self.total_tokens * NKV * (2 * D + 4) + B * S1 * NQ * (D + 4)
+                + B * NKV * D * 4 + B * S1 * NQ * D * 2 + 4 * (B * self.max_blocks + B))
+
+    def flops(self) -> int:
+        return 4 * self.D * self.total_tokens * self.S1 * self.NQ
+
+
+def _paged(name, B, S1, NQ, NKV, act, max_blocks, seed, *, num_blocks=None, spare=0.10,
+           **kw) -> DecodeCase:
+    act = np.asarray(act, dtype=np.int32)
+    BS = kw.get("BS", 128)
+    need = [int(math.ceil(int(a) / BS)) for a in act]
+    total = sum(need)
+    if num_blocks is None:
+        num_blocks = max(1, int(math.ceil(total * (1.0 + spare))))
+    assert num_blocks >= total and max(need) <= max_blocks
+    perm = _rng(seed, 0).permutation(num_blocks).astype(np.int32)
+    bt = np.full((B, max_blocks), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        bt[b, :need[b]] = perm[pos:pos + need[b]]
+        pos += need[b]
+    return DecodeCase(name=name, B=B, S1=S1, NQ=NQ, NKV=NKV, act=act, max_blocks=max_blocks,
+                      num_blocks=num_blocks, block_table=bt, seed=seed, **kw)
+
+
+def tiny(s2_tile: int = 512, layout: int = LAYOUT_BSND) -> DecodeCase:
+    """B=2, NQ=4, NKV=1, lengths {37, 300}, 8 physical blocks."""
+    return _paged("tiny", 2, 1, 4, 1, [37, 300], 4, BASE_SEED + 0, num_blocks=8,
+                  s2_tile=s2_tile, layout=layout)
+
+
+def glm(s2_tile: int = 512, layout: int = LAYOUT_BSND, seed_offset: int = 0) -> DecodeCase:
+    """GLM-4.5 decode shape: B=16, NQ=96, NKV=8, lengths ~ U{1..4096}."""
+    seed = BASE_SEED + 1 + 1000 * seed_offset
+    act = _rng(seed, 9).integers(1, 4096, size=16, endpoint=True)
+    return _paged("glm", 16, 1, 96, 8, act, 32, seed, s2_tile=s2_tile, layout=layout)
+
+
+def long_ctx(s2_tile: int = 512, layout: int = LAYOUT_BSND) -> DecodeCase:
+    """B=4, NQ=96, NKV=8, lengths ~ U{32768..131072}, K outlier rows x8."""
+    seed = BASE_SEED + 2
+    act = _rng(seed, 9).integers(32768, 131072, size=4, endpoint=True)
+    return _paged("long", 4, 1, 96, 8, act, 1024, seed, s2_tile=s2_tile, layout=layout,
+                  k_outlier_every=64)
+
+
+def ragged(s2_tile: int = 512, layout: int = LAYOUT_BSND, sigma: float = 1.0) -> DecodeCase:
+    """B=256, S1=2, NQ=96, NKV=8, lengths lognormal (median 1024), clip [1, 16384]."""
+    seed = BASE_SEED + 3
+    x = _rng(seed, 9).normal(math.log(1024.0), sigma, size=256)
+    act = np.clip(np.rint(np.exp(x)), 1, 16384).astype(np.int32)
+    return _paged("ragged", 256, 2, 96, 8, act, 128, seed, s2_tile=s2_tile, layout=layout)
+
+
+def custom(name, B, S1, NQ, NKV, act, *, max_blocks=None, seed=BASE_SEED + 7, **kw):
+    act = np.asarray(act, dtype=np.int32)
+    BS = kw.get("BS", 128)
+    if max_blocks is None:
+        max_blocks = max(1, int(math.ceil(max(int(act.max()), 1) / BS)))
+    return _paged(name, B, S1, NQ, NKV, act, max_blocks, seed, **kw)
+
+
+# The six (b, s1, s2, nq, nkv) shapes of the GLM-4.5 paged FP8 page's test
+# table (every sequence at its full s2).
+PAGE_CASES = [
+    (1, 2, 2048, 48, 8),
+    (16, 1, 8195, 12, 2),
+    (16, 1, 8192, 12, 1),
+    (16, 1, 8192, 12, 2),
+    (2, 1, 1024, 12, 1),
+    (16, 1, 256, 16, 4),
+]
+
+
+def page_case(i: int, s2_tile: int = 512) -> DecodeCase:
+    b, s1, s2, nq, nkv = PAGE_CASES[i]
+    return custom("page%d" % i, b, s1, nq, nkv, [s2] * b, seed=BASE_SEED + 100 + i,
+                  s2_tile=s2_tile)
+
+
+@dataclasses.dataclass
+class AppendCase:
+    """Append one new token per sequence, then decode over the updated cache."""
+
+    ctx: DecodeCase            # the existing contexts (BNBD cache)
+    slot_mapping: np.ndarray   # int32 [T] slot of each new token (-1 = skipped)
+    seed: int
+
+    def __post_init__(self):
+        self._new = None
+
+    @property
+    def T(self) -> int:
+        return self.ctx.B
+
+    def new_kv_f32(self):
+        """(key, value) float32 [T, NKV, D] N(0,1), rounded to BF16 values."""
+        import torch  # BF16 rounding by the library routine
+        if self._new is None:
+            r = _rng(self.seed, 3)
+            shape = (self.T, self.ctx.NKV, self.ctx.D)
+            k = torch.from_numpy(r.standard_normal(shape, dtype=np.float32))
+            v = torch.from_numpy(r.standard_normal(shape, dtype=np.float32))
+            self._new = (k.to(torch.bfloat16), v.to(torch.bfloat16))
+        k, v = self._new
+        return k.float().numpy(), v.float().numpy()
+
+    def new_kv_bf16(self):
+        """(key, value) as torch.bfloat16 CPU tensors [T, NKV, D]."""
+        self.new_kv_f32()
+        return self._new
+
+    @property
+    def token_batch(self) -> np.ndarray:
+        return np.arange(self.T, dtype=np.int32)
+
+    @property
+    def act_after(self) -> np.ndarray:
+        """kv_act_seqs after the append: +1 where the token was written."""
+        return (self.ctx.act + (self.slot_mapping >= 0)).astype(np.int32)
+
+
+def append(frac_skip: float = 0.05, B: int = 64, lo: int = 512, hi: int = 8192) -> AppendCase:
+    """64 new BF16 K/V rows into contexts ~ U{512..8192}, NQ=96, NKV=8, BNBD."""
+    seed = BASE_SEED + 4
+    r = _rng(seed, 9)
+    act = r.integers(lo, hi, size=B, endpoint=True).astype(np.int32)
+    BS = 128
+    # room for one more token in every sequence
+    max_blocks = int(math.ceil((hi + 1) / BS))
+    need = [int(math.ceil((int(a) + 1) / BS)) for a in act]
+    num_blocks = int(math.ceil(sum(need) * 1.1))
+    perm = _rng(seed, 0).permutation(num_blocks).astype(np.int32)
+    bt = np.full((B, max_blocks), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        bt[b, :need[b]] = perm[pos:pos + need[b]]
+        pos += need[b]
+    ctx = DecodeCase(name="append", B=B, S1=1, NQ=96, NKV=8, act=act, max_blocks=max_blocks,
+                     num_blocks=num_blocks, block_table=bt, seed=seed, layout=LAYOUT_BNBD)
+    slot = (bt[np.arange(B), act // BS].astype(np.int64) * BS + act % BS).astype(np.int32)
+    nskip = int(round(frac_skip * B))
+    skip = r.choice(B, size=nskip, replace=False)
+    slot[skip] = -1
+    return AppendCase(ctx=ctx, slot_mapping=slot, seed=seed)
+
+
+WORKLOADS = {
+    "tiny": tiny,
+    "glm": glm,
+    "long": long_ctx,
+    "ragged": ragged,
+}
