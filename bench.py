@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 paged decode step at the GLM-4.5 decode shape.
+
+One step = the whole hot path over one batch: append one new BF16 K/V token
+per sequence into the FP8 paged cache (quantise-on-append scatter), then
+grouped-query paged FP8 decode attention over the updated cache.
+Workload: B=16, S1=1, NQ=96, NKV=8, D=128, block_size=128, kv lengths
+~U{1..4096} (seeded), s2_tile=512, PA_BSND cache; synthetic N(0,1) data.
+
+Prints one JSON line (rank 0). Metric: achieved HBM GB/s over the step's
+algorithmic bytes (valid tokens only), plus us/step. The step is timed on the
+device with CUDA events over exactly --steps steps replayed from CUDA graphs;
+the steps rotate over enough cache copies that their KV exceeds 3x the L2.
+
+--impl reference times the CPU oracle (the plain C restatement of the
+pages) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "FP8 paged decode attn: achieved HBM GB/s (% of peak), µs/step at GLM-4.5 shape"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic of one decode launch on this workload, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
+# sources it was taken with.
+DECODE_TRAFFIC = {"sources_sha1": None, "bytes_per_launch": None}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--copies", type=int, default=0, help="cache copies to rotate (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def kernel_sources_sha1() -> str:
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "fp8_paged_kv_block_gb300", "csrc")
+    for f in ("decode.cu", "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload():
+    return workloads.glm()
+
+
+def step_bytes(case, act_after):
+    """Algorithmic bytes of one step: the decode over the updated lengths plus
+    the append (BF16 K/V in, E4M3 codes and key scale out, slot and batch
+    ids)."""
+    import dataclasses
+    dec = dataclasses.replace(case, act=act_after).algorithmic_bytes()
+    app = case.B * case.NKV * (2 * case.D * 2 + 2 * case.D + 4) + case.B * 8
+    return dec, app
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 10:
+                    rows.append(p)
+        os.unlink(self.path)
+        busy = [r for r in rows if r[9].isdigit() and int(r[9]) > 0] or rows
+        sm = [float(r[1]) for r in busy if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "samples_busy": len(busy)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline (also the reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample(case, inp, budget_s: float, per_row_token_s: float):
+    """Rows (whole (batch, kv head) units, in batch order) whose estimated
+    oracle time fits ``budget_s``; at least one row."""
+    rows, est, nbytes = [], 0.0, 0
+    G = case.group
+    for b in range(case.B):
+        a = int(case.act[b])
+        for n2 in range(case.NKV):
+            unit_rows = [b * case.NQ + n2 * G + g for g in range(G)]
+            t = per_row_token_s * a * G
+            if rows and est + t > budget_s:
+                return rows, nbytes
+            rows.extend(unit_rows)
+            est += t
+            nbytes += a * (2 * case.D + 4) + G * (case.D + 4) + case.D * 4 + G * case.D * 2
+    return rows, nbytes
+
+
+def run_oracle_rows(case, inp, rows):
+    import oracle
+    return oracle.pa_decode(inp["q8"], inp["qs"], inp["kc"], inp["ksc"], inp["vc"], inp["vs"],
+                            case.block_table, case.act, S1=case.S1, NKV=case.NKV,
+                            layout=case.layout, s2_tile=case.s2_tile,
+                            softmax_scale=case.softmax_scale, rows=np.asarray(rows))
+
+
+def calibrate_oracle(case, inp):
+    """Seconds per (row x token) of the oracle on this host."""
+    b = int(np.argmin(np.where(case.act >= 64, case.act, 1 << 30)))
+    rows = [b * case.NQ]
+    t0 = time.perf_counter()
+    run_oracle_rows(case, inp, rows)
+    return max((time.perf_counter() - t0) / max(int(case.act[b]), 1), 1e-9)
+
+
+def cpu_baseline(case, budget_s: float):
+    from tests import _helpers as H
+    inp = H.oracle_inputs(case)
+    prt = calibrate_oracle(case, inp)
+    rows, nbytes = oracle_sample(case, inp, budget_s, prt)
+    t0 = time.perf_counter()
+    run_oracle_rows(case, inp, rows)
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d of %d query rows (%d whole (batch, kv-head) units), decode only, "
+                      "single-threaded C oracle, %.1f s" % (len(rows), case.B * case.NQ,
+                                                            len(rows) // case.group, dt),
+            "seconds": dt, "sample_bytes": nbytes}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    case = workload()
+    from tests import _helpers as H
+    inp = H.oracle_inputs(case)
+    prt = calibrate_oracle(case, inp)
+    total_steps = args.steps + args.warmup
+    budget = max(150.0 / max(total_steps, 1), 1e-4)
+    rows, nbytes = oracle_sample(case, inp, budget, prt)
+    for _ in range(args.warmup):
+        run_oracle_rows(case, inp, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_rows(case, inp, rows)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = nbytes / dt / 1e9
+    full = case.algorithmic_bytes()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full / (value * 1e9) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f32",
+        "data": "synthetic",
+        "config": {"workload": "glm45_decode B=16 S1=1 NQ=96 NKV=8 D=128 bs=128 "
+                               "kv~U[1,4096] s2_tile=512 PA_BSND", "sample_rows": len(rows)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d query rows (whole units) per step, decode only; "
+                                   "ms_per_step extrapolated to the full step by bytes" % len(rows)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import torch
+    import fp8_paged_kv_block_gb300 as pa
+    from fp8_paged_kv_block_gb300 import paged
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pa.build()
+    pa.lib()
+
+    case = workload()
+    knew, vnew, slot, act_after = workloads.step_tokens(case)
+    dec_bytes, app_bytes = step_bytes(case, act_after)
+    bytes_per_step = dec_bytes + app_bytes
+
+    # ---- device inputs: queries, context cache, append inputs ----
+    q8, qs = paged.quantize_queries(torch.from_numpy(case.q()).to(dev))
+    k32, v32 = case.kv()
+    base = paged.build_cache(torch.from_numpy(k32).to(dev), torch.from_numpy(v32).to(dev),
+                             torch.from_numpy(case.cu_seqlens).to(dev),
+                             torch.from_numpy(case.slots).to(dev),
+                             torch.from_numpy(case.token_batch).to(dev), case.num_blocks,
+                             case.layout)
+    del k32, v32
+    case.drop()
+    cache_bytes = 2 * base.k_cache.numel() + 4 * base.k_scale.numel()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = args.copies or max(3, math.ceil(3 * l2 / cache_bytes))
+    caches = [base] + [paged.PagedFP8(base.k_cache.clone(), base.v_cache.clone(),
+                                      base.k_scale.clone(), base.v_scale.clone(), base.layout)
+                       for _ in range(copies - 1)]
+    bt = torch.from_numpy(case.block_table).to(dev)
+    act_d = torch.from_numpy(act_after).to(dev)
+    slot_d = torch.from_numpy(slot).to(dev)
+    tb_d = torch.arange(case.B, dtype=torch.int32, device=dev)
+    kn_d, vn_d = knew.to(dev), vnew.to(dev)
+    out = torch.empty((case.B * case.S1, case.NQ, case.D), dtype=torch.bfloat16, device=dev)
+    ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile, device=dev)
+
+    def append(c):
+        pa.cache_quant_scatter(kn_d, vn_d, c.k_cache, c.v_cache, slot_d, c.k_scale, c.v_scale,
+                               tb_d, layout=case.layout)
+
+    def attend(c):
+        pa.decode(q8, qs, c.k_cache, c.k_scale, c.v_cache, c.v_scale, bt, act_d, out,
+                  S1=case.S1, layout=case.layout, s2_tile=case.s2_tile,
+                  softmax_scale=case.softmax_scale, workspace=ws)
+
+    def step(i):
+        c = caches[i % copies]
+        append(c)
+        attend(c)
+
+    def capture(fn, n):
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(min(n, copies)):
+                fn(i)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                fn(i)
+        return g
+
+    cyc = copies * max(1, math.ceil(32 / copies))           # steps per replay
+    g_step = capture(step, cyc)
+    g_dec = capture(lambda i: attend(caches[i % copies]), cyc)
+    g_one = [capture(lambda i, r=r: step(r), 1) for r in range(copies)]
+    g_one_dec = [capture(lambda i, r=r: attend(caches[r]), 1) for r in range(copies)]
+
+    def run_steps(full_graph, singles, n):
+        for _ in range(n // cyc):
+            full_graph.replay()
+        for r in range(n % cyc):
+            singles[r % copies].replay()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def timed(full_graph, singles, n):
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run_steps(full_graph, singles, n)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    clocks = ClockSampler(local)
+    # warm-up (untimed)
+    run_steps(g_step, g_one, max(args.warmup, 3))
+    run_steps(g_dec, g_one_dec, max(args.warmup, 3))
+    torch.cuda.synchronize()
+    assert ws.error_flags() == 0, "decode kernel reported a wait timeout"
+
+    clocks.start()
+    t_start = time.perf_counter()
+    ms_total = timed(g_step, g_one, args.steps)
+    ms_dec = timed(g_dec, g_one_dec, args.steps)
+    # keep the same work running until the clock sampler has seen ~1 s of it
+    while time.perf_counter() - t_start < 1.0:
+        run_steps(g_step, g_one, cyc * 8)
+        torch.cuda.synchronize()
+
+    # ---- end to end through the public API with host buffers ----
+    h_q8 = torch.empty_like(q8, device="cpu").pin_memory()
+    h_q8.copy_(q8)
+    h_qs = qs.cpu().pin_memory()
+    h_kn = knew.pin_memory()
+    h_vn = vnew.pin_memory()
+    h_slot = torch.from_numpy(slot).pin_memory()
+    h_act = torch.from_numpy(act_after).pin_memory()
+    h_bt = torch.from_numpy(case.block_table).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q8, d_qs = torch.empty_like(q8), torch.empty_like(qs)
+    d_kn, d_vn = torch.empty_like(kn_d), torch.empty_like(vn_d)
+    d_slot, d_act, d_bt = torch.empty_like(slot_d), torch.empty_like(act_d), torch.empty_like(bt)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q8, h_qs, h_kn, h_vn, h_slot, h_act, h_bt))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step(i):
+        c = caches[i % copies]
+        for d, h in ((d_q8, h_q8), (d_qs, h_qs), (d_kn, h_kn), (d_vn, h_vn), (d_slot, h_slot),
+                     (d_act, h_act), (d_bt, h_bt)):
+            d.copy_(h, non_blocking=True)
+        pa.cache_quant_scatter(d_kn, d_vn, c.k_cache, c.v_cache, d_slot, c.k_scale, c.v_scale,
+                               tb_d, layout=case.layout)
+        pa.decode(d_q8, d_qs, c.k_cache, c.k_scale, c.v_cache, c.v_scale, d_bt, d_act, out,
+                  S1=case.S1, layout=case.layout, s2_tile=case.s2_tile,
+                  softmax_scale=case.softmax_scale, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    n_e2e = args.steps
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n_e2e):
+        e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    assert ws.error_flags() == 0, "decode kernel reported a wait timeout"
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    ms_step = ms_total / args.steps
+    ms_dec_launch = ms_dec / args.steps
+    value = world * bytes_per_step * args.steps / (ms_total * 1e-3) / 1e9
+    peak, peak_src = measured_hbm_peak()
+    achieved = dec_bytes / (ms_dec_launch * 1e-3) / 1e9
+    sha = kernel_sources_sha1()
+    traffic = (DECODE_TRAFFIC["bytes_per_launch"]
+               if DECODE_TRAFFIC["sources_sha1"] == sha else None)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(workload(), args.cpu_seconds)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "us_per_step": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3+f32", "data": "synthetic",
+            "config": {
+                "workload": "glm45_decode_step: append 1 BF16 token/seq (quantise-on-append "
+                            "scatter) + FP8 paged GQA decode; B=16 S1=1 NQ=96 NKV=8 D=128 "
+                            "block_size=128 kv~U[1,4096] s2_tile=512 PA_BSND",
+                "B": case.B, "kv_tokens": int(act_after.sum()), "bytes_per_step": bytes_per_step,
+                "decode_bytes": dec_bytes, "append_bytes": app_bytes,
+                "l2": "inputs larger than L2: %d cache copies rotated (%.0f MB > %.0f MB L2)"
+                      % (copies, copies * cache_bytes / 1e6, l2 / 1e6),
+                "timing": "CUDA graphs replayed on one stream, CUDA events over the K steps",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+            },
+            "gpu_launches": 2 * args.steps,
+            "roofline": {"bound": "hbm", "kernel": "pa_fp8_decode", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "peak_source": peak_src,
+                         "frac_of_8tbs_nominal": achieved / 8000.0,
+                         "us_per_launch": ms_dec_launch * 1e3,
+                         "algorithmic_bytes_per_launch": dec_bytes},
+            "e2e": {"value": world * bytes_per_step * n_e2e / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "us_per_step": ms_e2e / n_e2e * 1e3},
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "tokens_per_s": world * case.B * case.S1 * args.steps / (ms_total * 1e-3),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

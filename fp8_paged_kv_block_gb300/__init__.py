@@ -1,0 +1,316 @@
+"""GB300 (sm_103a) FP8 paged-KV decode attention and cache append.
+
+Thin ctypes binding over the C ABI declared in ``include/pa_fp8.h``
+(``libpa_fp8.so``). This module only marshals arguments: every step runs in
+the library's CUDA kernels. PyTorch supplies device memory and the current
+stream. There is no fallback: if the library is missing, calls raise.
+
+Functions take torch CUDA tensors and work in place (outputs are arguments):
+  decode(...)              paged FP8 decode attention -> BF16
+  cache_scatter(...)       FP8 K/V (+ key_scale) append by slot_mapping
+  cache_quant_scatter(...) BF16/FP32 K/V quantised to E4M3 on append
+  quantize_rows(...)       per-token E4M3 quantiser (Q, K)
+  value_channel_scale(...) per-channel V dequant scale
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import _build
+
+LAYOUT_BSND = 0
+LAYOUT_BNBD = 1
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+INDEX_I32 = 0
+INDEX_I64 = 1
+
+PA_OK = 0
+_STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_NULLPTR", 2: "PA_ERR_INVALID", 3: "PA_ERR_WORKSPACE",
+                 4: "PA_ERR_CUDA", 5: "PA_ERR_UNSUPPORTED"}
+
+LIB_PATH = _build.LIB_PATH
+_lock = threading.Lock()
+_lib = None
+
+
+class PaError(RuntimeError):
+    """A non-PA_OK status from the library."""
+
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (where, _STATUS_NAMES.get(status, status), detail))
+
+
+class pa_decode_config(ctypes.Structure):
+    _fields_ = [("s2_tile", ctypes.c_int), ("num_ctas", ctypes.c_int),
+                ("reserved", ctypes.c_int * 6)]
+
+
+def build(force: bool = False) -> str:
+    """Compile libpa_fp8.so (nvcc, sm_103a) if it is stale."""
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded ctypes library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libpa_fp8.so is not built (%s); run "
+                               "fp8_paged_kv_block_gb300.build() first" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+        L.pa_status_string.argtypes = [i32]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_last_error.argtypes = []
+        L.pa_last_error.restype = ctypes.c_char_p
+        L.pa_fp8_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, P,
+                                                   ctypes.POINTER(sz)]
+        L.pa_fp8_decode_workspace_size.restype = i32
+        L.pa_fp8_decode.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
+                                    i32, i32, f32, P, P, sz, P]
+        L.pa_fp8_decode.restype = i32
+        L.pa_fp8_cache_scatter.argtypes = [P, P, P, P, P, i32, P, i64, i64, P, i64, i32, i32, i32,
+                                           i64, i32, i32, P]
+        L.pa_fp8_cache_scatter.restype = i32
+        L.pa_fp8_cache_quant_scatter.argtypes = [P, P, i32, P, P, P, i32, P, P, P, i32, i64, i32,
+                                                 i32, i64, i32, i32, P]
+        L.pa_fp8_cache_quant_scatter.restype = i32
+        L.pa_fp8_quantize_rows.argtypes = [P, i32, i64, i32, P, P, P]
+        L.pa_fp8_quantize_rows.restype = i32
+        L.pa_fp8_value_channel_scale.argtypes = [P, i32, P, i32, i64, i32, i32, P, P]
+        L.pa_fp8_value_channel_scale.restype = i32
+        _lib = L
+        return L
+
+
+def _check(status: int, where: str):
+    if status != PA_OK:
+        detail = lib().pa_last_error().decode(errors="replace")
+        raise PaError(status, where, detail)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, name, dtype=None, contiguous=True):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError("%s has dtype %s, expected %s" % (name, t.dtype, dtype))
+    if contiguous and not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _fp8_types():
+    torch = _torch()
+    return (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
+
+
+def _in_dtype(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError("expected float32 or bfloat16, got %s" % t.dtype)
+
+
+# --------------------------------------------------------------------------
+# Decode attention
+# --------------------------------------------------------------------------
+
+def _config(s2_tile: int, num_ctas: int):
+    c = pa_decode_config()
+    c.s2_tile = s2_tile
+    c.num_ctas = num_ctas
+    return c
+
+
+def decode_workspace_size(B: int, S1: int, NQ: int, NKV: int, D: int = 128, *,
+                          s2_tile: int = 512, num_ctas: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    cfg = _config(s2_tile, num_ctas)
+    _check(lib().pa_fp8_decode_workspace_size(B, S1, NQ, NKV, D, ctypes.byref(cfg),
+                                              ctypes.byref(n)), "pa_fp8_decode_workspace_size")
+    return n.value
+
+
+class DecodeWorkspace:
+    """Zero-initialised device scratch for pa_fp8_decode (reusable: every call
+    leaves its counters at zero)."""
+
+    def __init__(self, B, S1, NQ, NKV, D=128, *, s2_tile=512, num_ctas=0, device=None):
+        torch = _torch()
+        self.nbytes = decode_workspace_size(B, S1, NQ, NKV, D, s2_tile=s2_tile, num_ctas=num_ctas)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+
+    def error_flags(self) -> int:
+        """Non-zero if a kernel wait gave up (bitmask of the wait sites)."""
+        return int(self.buf[:4].view(_torch().int32).item())
+
+
+def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs, out, *,
+           S1: int = 1, layout: int = LAYOUT_BSND, s2_tile: int = 512, softmax_scale=None,
+           workspace: DecodeWorkspace | None = None, num_ctas: int = 0, stream=None):
+    """Paged FP8 decode attention (in place into ``out``).
+
+    q [B*S1, NQ, D] E4M3 (uint8 or float8_e4m3fn), q_scale float32 [B*S1, NQ],
+    k_cache/v_cache E4M3 in ``layout`` ([NB, BS, NKV, D] for BSND,
+    [NB, NKV, BS, D] for BNBD), k_scale float32 (cache shape without D),
+    v_scale float32 [B, NKV, D], block_table int32 [B, max_blocks],
+    kv_act_seqs int32 [B], out bfloat16 [B*S1, NQ, D].
+    """
+    torch = _torch()
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, _fp8_types())
+    _need(q_scale, "q_scale", torch.float32)
+    _need(k_scale, "k_scale", torch.float32)
+    _need(v_scale, "v_scale", torch.float32)
+    _need(block_table, "block_table", torch.int32)
+    _need(kv_act_seqs, "kv_act_seqs", torch.int32)
+    _need(out, "out", torch.bfloat16)
+    B = kv_act_seqs.shape[0]
+    BS1, NQ, D = q.shape
+    if layout == LAYOUT_BSND:
+        NB, BS, NKV, _ = k_cache.shape
+    else:
+        NB, NKV, BS, _ = k_cache.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if workspace is None:
+        workspace = DecodeWorkspace(B, S1, NQ, NKV, D, s2_tile=s2_tile, num_ctas=num_ctas,
+                                    device=q.device)
+    cfg = _config(s2_tile, num_ctas)
+    st = lib().pa_fp8_decode(_ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
+                             _ptr(v_scale), _ptr(block_table), _ptr(kv_act_seqs), _ptr(out),
+                             B, S1, NQ, NKV, D, BS, NB, block_table.shape[1], layout,
+                             float(softmax_scale), ctypes.byref(cfg), _ptr(workspace.buf),
+                             workspace.nbytes, _stream(stream))
+    _check(st, "pa_fp8_decode")
+    return out
+
+
+# --------------------------------------------------------------------------
+# Cache append
+# --------------------------------------------------------------------------
+
+def _cache_dims(key_cache, layout):
+    if layout == LAYOUT_BNBD:
+        NB, H, BS, _ = key_cache.shape
+    else:
+        NB, BS, H, _ = key_cache.shape
+    return NB, H, BS
+
+
+def _slot_type(slot_mapping):
+    torch = _torch()
+    if slot_mapping.dtype == torch.int32:
+        return INDEX_I32
+    if slot_mapping.dtype == torch.int64:
+        return INDEX_I64
+    raise TypeError("slot_mapping must be int32 or int64")
+
+
+def cache_scatter(key, value, key_cache, value_cache, slot_mapping, key_scale, key_scale_cache,
+                  *, layout: int = LAYOUT_BNBD, stream=None):
+    """FP8 K/V + key_scale append by slot_mapping (in place). key_scale may
+    have a non-contiguous tail (any 2-D strides)."""
+    torch = _torch()
+    for t, n in ((key, "key"), (value, "value"), (key_cache, "key_cache"),
+                 (value_cache, "value_cache")):
+        _need(t, n, _fp8_types())
+    _need(slot_mapping, "slot_mapping", (torch.int32, torch.int64))
+    _need(key_scale, "key_scale", torch.float32, contiguous=False)
+    _need(key_scale_cache, "key_scale_cache", torch.float32)
+    T, H, Dk = key.shape
+    Dv = value.shape[2]
+    NB, _, BS = _cache_dims(key_cache, layout)
+    st = lib().pa_fp8_cache_scatter(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                    _ptr(slot_mapping), _slot_type(slot_mapping), _ptr(key_scale),
+                                    key_scale.stride(0), key_scale.stride(1),
+                                    _ptr(key_scale_cache), T, H, Dk, Dv, NB, BS, layout,
+                                    _stream(stream))
+    _check(st, "pa_fp8_cache_scatter")
+
+
+def cache_quant_scatter(key, value, key_cache, value_cache, slot_mapping, key_scale_cache,
+                        v_scale, token_batch, *, layout: int = LAYOUT_BNBD, stream=None):
+    """BF16/FP32 K/V quantised to E4M3 on append (in place): key per
+    (token, head) with scale amax/448 stored to key_scale_cache, value against
+    v_scale[token_batch[i]]."""
+    torch = _torch()
+    _need(key, "key", (torch.float32, torch.bfloat16))
+    _need(value, "value", (key.dtype,))
+    for t, n in ((key_cache, "key_cache"), (value_cache, "value_cache")):
+        _need(t, n, _fp8_types())
+    _need(slot_mapping, "slot_mapping", (torch.int32, torch.int64))
+    _need(key_scale_cache, "key_scale_cache", torch.float32)
+    _need(v_scale, "v_scale", torch.float32)
+    _need(token_batch, "token_batch", torch.int32)
+    T, H, D = key.shape
+    NB, _, BS = _cache_dims(key_cache, layout)
+    st = lib().pa_fp8_cache_quant_scatter(_ptr(key), _ptr(value), _in_dtype(key), _ptr(key_cache),
+                                          _ptr(value_cache), _ptr(slot_mapping),
+                                          _slot_type(slot_mapping), _ptr(key_scale_cache),
+                                          _ptr(v_scale), _ptr(token_batch), v_scale.shape[0], T, H,
+                                          D, NB, BS, layout, _stream(stream))
+    _check(st, "pa_fp8_cache_quant_scatter")
+
+
+def quantize_rows(x, codes, scale, *, stream=None):
+    """Per-row E4M3 quantiser: x [..., D] float32/bfloat16 -> codes [..., D],
+    dequant scale [...] = amax / 448."""
+    torch = _torch()
+    _need(x, "x", (torch.float32, torch.bfloat16))
+    _need(codes, "codes", _fp8_types())
+    _need(scale, "scale", torch.float32)
+    D = x.shape[-1]
+    rows = x.numel() // D
+    st = lib().pa_fp8_quantize_rows(_ptr(x), _in_dtype(x), rows, D, _ptr(codes), _ptr(scale),
+                                    _stream(stream))
+    _check(st, "pa_fp8_quantize_rows")
+
+
+def value_channel_scale(v, cu_seqlens, v_scale, *, stream=None):
+    """v [Ttot, H, D] float32/bfloat16, cu_seqlens int64 [B+1] (device) ->
+    v_scale [B, H, D] = per-channel max |v| over each sequence / 448."""
+    torch = _torch()
+    _need(v, "v", (torch.float32, torch.bfloat16))
+    _need(cu_seqlens, "cu_seqlens", torch.int64)
+    _need(v_scale, "v_scale", torch.float32)
+    T, H, D = v.shape
+    B = cu_seqlens.shape[0] - 1
+    st = lib().pa_fp8_value_channel_scale(_ptr(v), _in_dtype(v), _ptr(cu_seqlens), B, T, H, D,
+                                          _ptr(v_scale), _stream(stream))
+    _check(st, "pa_fp8_value_channel_scale")
+
+
+__all__ = [
+    "LAYOUT_BSND", "LAYOUT_BNBD", "PaError", "build", "lib", "decode", "decode_workspace_size",
+    "DecodeWorkspace", "cache_scatter", "cache_quant_scatter", "quantize_rows",
+    "value_channel_scale",
+]

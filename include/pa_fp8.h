@@ -1,0 +1,238 @@
+/*
+ * pa_fp8.h -- C ABI of the GB300 (sm_103a) FP8 paged-KV library.
+ *
+ * Two operations sit on the decode hot path:
+ *   pa_fp8_decode        grouped-query paged decode attention over an FP8
+ *                        E4M3 KV cache (split-KV flash decoding, BF16 out);
+ *   pa_fp8_cache_scatter the FP8 cache append by slot_mapping, with its
+ *                        quantise-on-append form pa_fp8_cache_quant_scatter.
+ * Two small quantisers prepare FP8 inputs the way the decode page describes
+ * (per-token Q/K, per-channel V): pa_fp8_quantize_rows and
+ * pa_fp8_value_channel_scale.
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor pointer is CUDA device memory owned by the caller (or
+ *    memory the device can address, e.g. managed memory). The library keeps
+ *    no pointer after a call returns.
+ *  - The library never allocates or frees device memory and never waits
+ *    for the device: each call validates its arguments on the host, enqueues
+ *    its kernels on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and returns. Results are ready when the stream reaches them.
+ *  - Shapes are explicit integers; tensors are dense row-major unless a
+ *    stride argument says otherwise. FP8 tensors are bytes (E4M3 codes).
+ *  - Errors: argument problems found on the host return a status without
+ *    enqueuing anything; a failed launch returns PA_ERR_CUDA.
+ *    pa_last_error() gives a one-line description of the last failure on the
+ *    calling thread. Device-side data (block ids, slots, lengths) is not
+ *    validated on the host; the kernels guard memory safety as documented
+ *    per call.
+ *
+ * Page references name the page title and section:
+ *  [PA] "PyPTO 实现 GLM-4.5 Paged Attention FP8 量化算子 ... Kernel 实战解析"
+ *  [SC] "CANN ops-transformer 中的 FP8 KV Cache 更新算子
+ *        scatter_pa_kv_cache_with_k_scale 使用指南"
+ *  [KC] "CANN ops-transformer aclnnKvCompressEpilog 算子详解"
+ */
+#ifndef PA_FP8_H
+#define PA_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_NULLPTR = 1,     /* a required pointer is NULL                      */
+    PA_ERR_INVALID = 2,     /* bad shape, size, layout, dtype or empty tensor  */
+    PA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required      */
+    PA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed     */
+    PA_ERR_UNSUPPORTED = 5  /* valid, but not built (e.g. head_size != 128)    */
+} pa_status;
+
+/* Paged cache layouts.
+ * PA_LAYOUT_BSND: [num_blocks, block_size, num_heads, head_size] -- the
+ *   "PA_BSND" layout of [PA] (Kernel 签名: k [num_blocks, block_size, NKV, D]).
+ * PA_LAYOUT_BNBD: [num_blocks, num_heads, block_size, head_size] -- the
+ *   "BNBD" cache_layout of [SC] (参数说明).
+ * Scale caches use the same shapes with head_size 1. */
+typedef enum pa_kv_layout {
+    PA_LAYOUT_BSND = 0,
+    PA_LAYOUT_BNBD = 1
+} pa_kv_layout;
+
+/* Element type of floating-point inputs to the quantisers. */
+typedef enum pa_dtype {
+    PA_DTYPE_F32 = 0,
+    PA_DTYPE_BF16 = 1
+} pa_dtype;
+
+/* Element type of slot_mapping ([SC] 参数说明: int32 or int64). */
+typedef enum pa_index_type {
+    PA_INDEX_I32 = 0,
+    PA_INDEX_I64 = 1
+} pa_index_type;
+
+/* Tuning knobs of pa_fp8_decode. Zero-initialise and set only what you
+ * need; 0 means "default". */
+typedef struct pa_decode_config {
+    int s2_tile;   /* KV tile of the online softmax and the P-quantisation
+                      group ([PA] 配置说明: s2_tile). Multiple of block_size;
+                      128, 256 or 512 are built. Default 512.                 */
+    int num_ctas;  /* persistent grid size. Default: SM count x resident
+                      CTAs per SM.                                            */
+    int reserved[6];
+} pa_decode_config;
+
+/* Text of a status code (static storage). */
+PA_API const char* pa_status_string(pa_status status);
+
+/* One-line description of the last non-PA_OK status returned on the calling
+ * thread (static thread-local storage; "" if none). */
+PA_API const char* pa_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Paged FP8 decode attention ([PA] 计算流程 steps 1-10; signature from
+ * [PA] Kernel 签名与源码对应关系).
+ *
+ * For every batch b, query row s < S1 and query head h (kv head
+ * n2 = h / (NQ / NKV), grouped-query attention), over the kv_act_seqs[b]
+ * tokens of sequence b, walked in s2_tile-sized tiles:
+ *   S_j  = ((Q_fp8 . K_fp8,j) * q_scale) * k_scale_j * softmax_scale
+ *   M    = running max, P_j = exp(S_j - M),
+ *   Sum  = Sum * exp(M_old - M) + sum_j P_j                (FP32 state)
+ *   P_fp8 = E4M3(P * 448 / max_j P_j) per row and tile, P_scale = max P / 448
+ *   O    = O * exp(M_old - M) + ((P_fp8 . V_fp8) * P_scale) * v_scale
+ *   out  = BF16(O / Sum)
+ * The tiles of one sequence may be processed by several CTAs (split-KV) and
+ * merged with a log-sum-exp combine; splits fall on s2_tile boundaries so
+ * the P-quantisation groups are those of the sequential walk.
+ *
+ * Arguments (device pointers; shapes in elements):
+ *   q            E4M3 [B*S1, NQ, D], row (b*S1 + s)*NQ + h.
+ *   q_scale      float [B*S1, NQ] dequant scale per query token and head.
+ *   k_cache      E4M3 paged cache in `layout`, num_blocks blocks of
+ *                block_size tokens, NKV heads of D bytes.
+ *   k_scale      float, the k_cache shape with D = 1 (per token and head).
+ *   v_cache      E4M3, same shape as k_cache.
+ *   v_scale      float [B, NKV, D] per-channel dequant scale.
+ *   block_table  int32 [B, max_blocks_per_seq]; entry i of row b is the
+ *                physical block of tokens [i*block_size, (i+1)*block_size).
+ *                -1 (and any id outside [0, num_blocks)) is read as block 0
+ *                ([PA] 注意事项); entries past the sequence end are not read.
+ *   kv_act_seqs  int32 [B] sequence lengths. Values above
+ *                max_blocks_per_seq*block_size are clamped to it; values
+ *                <= 0 give an all-zero output row.
+ *   out          BF16 [B*S1, NQ, D].
+ *   D, block_size  128 and 128 are built; anything else is
+ *                PA_ERR_UNSUPPORTED. NQ must be a multiple of NKV.
+ *   softmax_scale  usually 1/sqrt(D).
+ *   cfg          optional (NULL = defaults).
+ *   workspace    device scratch of at least pa_fp8_decode_workspace_size()
+ *                bytes, 256-byte aligned. Its first bytes are per-sequence
+ *                counters that must be zero before the FIRST call that uses
+ *                this workspace (e.g. cudaMemset once after allocation);
+ *                every call leaves them zero again. Calls that share a
+ *                workspace must not overlap in time (same stream is fine).
+ * Alignment: q, k_cache, v_cache, v_scale and out 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+PA_API pa_status pa_fp8_decode_workspace_size(int B, int S1, int NQ, int NKV, int D,
+                                       const pa_decode_config* cfg, size_t* bytes);
+
+PA_API pa_status pa_fp8_decode(const void* q, const float* q_scale,
+                        const void* k_cache, const float* k_scale,
+                        const void* v_cache, const float* v_scale,
+                        const int32_t* block_table, const int32_t* kv_act_seqs,
+                        void* out,
+                        int B, int S1, int NQ, int NKV, int D, int block_size,
+                        int64_t num_blocks, int max_blocks_per_seq, int layout,
+                        float softmax_scale, const pa_decode_config* cfg,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 cache append scatter ([SC] 功能说明与计算公式, 参数说明, 约束说明).
+ * In place. For token i < num_tokens and head j < num_head, with
+ * s = slot_mapping[i]:
+ *   if s < 0 or s >= num_blocks*block_size: skip ([SC] Kernel 实现, 边界防御)
+ *   blk = s / block_size, off = s % block_size
+ *   key_cache[blk][j][off][:]   = key[i][j][:]          (BNBD indexing)
+ *   value_cache[blk][j][off][:] = value[i][j][:]
+ *   key_scale_cache[blk][j][off][0] = key_scale[i][j]
+ * key, value     FP8 bytes [num_tokens, num_head, k_head_size / v_head_size]
+ *                (E4M3 or E5M2: bytes are copied unchanged).
+ * key_cache, value_cache  FP8 bytes in `layout`.
+ * slot_mapping   int32 or int64 [num_tokens] (slot_type). Slots should be
+ *                unique; with duplicates which write wins is undefined.
+ * key_scale      float, element (i, j) at key_scale[i*ks_stride0 +
+ *                j*ks_stride1] (the tail may be non-contiguous).
+ * key_scale_cache float, the cache shape with head size 1 (contiguous).
+ * num_tokens, num_head, head sizes > 0 (empty tensors are PA_ERR_INVALID).
+ * ------------------------------------------------------------------------ */
+PA_API pa_status pa_fp8_cache_scatter(const void* key, const void* value,
+                               void* key_cache, void* value_cache,
+                               const void* slot_mapping, int slot_type,
+                               const float* key_scale, int64_t ks_stride0,
+                               int64_t ks_stride1, float* key_scale_cache,
+                               int64_t num_tokens, int num_head, int k_head_size,
+                               int v_head_size, int64_t num_blocks, int block_size,
+                               int layout, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Quantise-on-append scatter: like pa_fp8_cache_scatter, but key and value
+ * arrive in FP32 or BF16 (in_dtype) and are encoded on the way in.
+ *   key:   per (token, head) dequant scale ks = max_d |k| / 448 (FP32 IEEE
+ *          division), codes E4M3(k / ks) round-to-nearest-even, saturating;
+ *          ks is stored to key_scale_cache ([KC] 计算公式 场景 1 applied to
+ *          the whole head; the per-token-head key_scale of [SC]).
+ *   value: codes E4M3(v / v_scale[token_batch[i]][j][d]) against the
+ *          sequence's per-channel scale (saturating). A zero scale gives
+ *          code 0, as does an all-zero key row (ks = 0).
+ * v_scale      float [num_batches, num_head, head_size].
+ * token_batch  int32 [num_tokens], the sequence of each new token, in
+ *              [0, num_batches).
+ * ------------------------------------------------------------------------ */
+PA_API pa_status pa_fp8_cache_quant_scatter(const void* key, const void* value, int in_dtype,
+                                     void* key_cache, void* value_cache,
+                                     const void* slot_mapping, int slot_type,
+                                     float* key_scale_cache, const float* v_scale,
+                                     const int32_t* token_batch, int num_batches,
+                                     int64_t num_tokens, int num_head, int head_size,
+                                     int64_t num_blocks, int block_size, int layout,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * Per-token quantiser ([PA] 量化策略: Query/Key per-token): each row of D
+ * values gets dequant scale s = max|x| / 448 and codes E4M3(x / s)
+ * (round-to-nearest-even, saturating; an all-zero row gives s = 0, codes 0).
+ * x      FP32 or BF16 [rows, D];  codes  E4M3 [rows, D];  scale float [rows].
+ * ------------------------------------------------------------------------ */
+PA_API pa_status pa_fp8_quantize_rows(const void* x, int in_dtype, int64_t rows, int D,
+                               void* codes, float* scale, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Per-channel value scale ([PA] 量化策略: Value per-channel, maximum over
+ * the sequence): v_scale[b][h][d] = max over the tokens of sequence b of
+ * |v[t][h][d]|, divided by 448.
+ * v           FP32 or BF16 [total_tokens, H, D], sequences concatenated.
+ * cu_seqlens  int64 [B + 1] device array of token offsets (non-decreasing,
+ *             cu_seqlens[0] = 0, cu_seqlens[B] = total_tokens).
+ * v_scale     float [B, H, D] (written; also used as scratch).
+ * ------------------------------------------------------------------------ */
+PA_API pa_status pa_fp8_value_channel_scale(const void* v, int in_dtype,
+                                     const int64_t* cu_seqlens, int B,
+                                     int64_t total_tokens, int H, int D,
+                                     float* v_scale, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_FP8_H */

@@ -1,0 +1,116 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it builds, loads,
+exports every function declared in include/pa_fp8.h, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa_fp8.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import fp8_paged_kv_block_gb300 as pa
+    pa.build()
+    return pa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for need in ("pa_fp8_decode", "pa_fp8_decode_workspace_size", "pa_fp8_cache_scatter",
+                 "pa_fp8_cache_quant_scatter", "pa_fp8_quantize_rows",
+                 "pa_fp8_value_channel_scale", "pa_status_string", "pa_last_error"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import fp8_paged_kv_block_gb300 as pa
+    out = subprocess.run(["nm", "-D", "--defined-only", pa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(L, name)
+
+
+def test_header_compiles_as_c():
+    src = '#include "pa_fp8.h"\nint main(void){ pa_decode_config c = {0}; (void)c; return 0; }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                        "-x", "c", "-", "-o", os.devnull], input=src, text=True,
+                       capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert L.pa_status_string(code)
+    assert b"PA_ERR_WORKSPACE" in L.pa_status_string(3)
+
+
+def test_scatter_rejects_bad_arguments_without_launching(L):
+    P = ctypes.c_void_p
+    fake = P(256)  # never dereferenced: validation fails first
+    st = L.pa_fp8_cache_scatter(None, fake, fake, fake, fake, 0, fake, 1, 1, fake, 4, 8, 128, 128,
+                                2, 16, 1, None)
+    assert st == 1 and b"NULL" in L.pa_last_error()
+    st = L.pa_fp8_cache_scatter(fake, fake, fake, fake, fake, 0, fake, 1, 1, fake, 0, 8, 128, 128,
+                                2, 16, 1, None)
+    assert st == 2
+    st = L.pa_fp8_cache_scatter(fake, fake, fake, fake, fake, 0, fake, 1, 1, fake, 4, 8, 128, 128,
+                                2, 16, 7, None)
+    assert st == 2 and b"layout" in L.pa_last_error()
+    st = L.pa_fp8_cache_scatter(fake, fake, fake, fake, fake, 3, fake, 1, 1, fake, 4, 8, 128, 128,
+                                2, 16, 1, None)
+    assert st == 2
+
+
+def test_decode_rejects_bad_arguments_without_launching(L):
+    import fp8_paged_kv_block_gb300 as pa
+    n = ctypes.c_size_t(0)
+    assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 64, None, ctypes.byref(n)) == 5
+    assert b"head size" in L.pa_last_error()
+    assert L.pa_fp8_decode_workspace_size(16, 1, 96, 7, 128, None, ctypes.byref(n)) == 2
+    assert L.pa_fp8_decode_workspace_size(0, 1, 96, 8, 128, None, ctypes.byref(n)) == 2
+    cfg = pa.pa_decode_config()
+    cfg.s2_tile = 100
+    assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 128, ctypes.byref(cfg),
+                                          ctypes.byref(n)) == 2
+    cfg.s2_tile = 1024
+    assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 128, ctypes.byref(cfg),
+                                          ctypes.byref(n)) == 5
+    P = ctypes.c_void_p
+    fake = P(256)
+    st = L.pa_fp8_decode(fake, fake, None, fake, fake, fake, fake, fake, fake, 16, 1, 96, 8, 128,
+                         128, 10, 4, 0, ctypes.c_float(0.088), None, fake, 1 << 20, None)
+    assert st == 1
+
+
+def test_quantizers_reject_bad_arguments(L):
+    P = ctypes.c_void_p
+    fake = P(256)
+    assert L.pa_fp8_quantize_rows(fake, 0, 10, 6, fake, fake, None) == 5
+    assert L.pa_fp8_quantize_rows(fake, 9, 10, 128, fake, fake, None) == 2
+    assert L.pa_fp8_quantize_rows(None, 0, 10, 128, fake, fake, None) == 1
+    assert L.pa_fp8_value_channel_scale(fake, 0, fake, 0, 10, 8, 128, fake, None) == 2
+    assert L.pa_fp8_cache_quant_scatter(fake, fake, 0, fake, fake, fake, 0, fake, fake, fake, 1,
+                                        4, 8, 126, 2, 16, 1, None) == 5
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The package must not import, load or call the oracle."""
+    pkg = os.path.join(ROOT, "fp8_paged_kv_block_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text and "pa_oracle" not in text, f

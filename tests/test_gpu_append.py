@@ -1,0 +1,163 @@
+"""GPU parity of the FP8 cache append: pass-through scatter and
+quantise-on-append, bit-exact against the oracle, then decode attention over
+the updated cache (the append + attend step)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests import _helpers as H
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    import fp8_paged_kv_block_gb300 as pa
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pa.lib()
+    return torch
+
+
+def test_scatter_worked_example(torch_cuda):
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    d = json.load(open(os.path.join(GOLDEN, "scatter_worked_example.json")))
+    T, Hh, Dk, Dv = d["num_tokens"], d["num_head"], d["k_head_size"], d["v_head_size"]
+    NB, BS = d["num_blocks"], d["block_size"]
+    rng = np.random.default_rng(41)
+    key = rng.integers(1, 255, (T, Hh, Dk), dtype=np.uint8)
+    val = rng.integers(1, 255, (T, Hh, Dv), dtype=np.uint8)
+    ks = rng.standard_normal((T, Hh)).astype(np.float32)
+    kc = torch.zeros((NB, Hh, BS, Dk), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros((NB, Hh, BS, Dv), dtype=torch.uint8, device="cuda")
+    ksc = torch.zeros((NB, Hh, BS, 1), dtype=torch.float32, device="cuda")
+    pa.cache_scatter(torch.from_numpy(key).cuda(), torch.from_numpy(val).cuda(), kc, vc,
+                     torch.tensor(d["slot_mapping"], dtype=torch.int32, device="cuda"),
+                     torch.from_numpy(ks).cuda(), ksc, layout=pa.LAYOUT_BNBD)
+    kc, vc, ksc = kc.cpu().numpy(), vc.cpu().numpy(), ksc.cpu().numpy()
+    written = np.zeros((NB, BS), bool)
+    for i, (blk, off) in enumerate(d["expected_block_offset"]):
+        assert np.array_equal(kc[blk, :, off], key[i])
+        assert np.array_equal(vc[blk, :, off], val[i])
+        assert np.array_equal(ksc[blk, :, off, 0], ks[i])
+        written[blk, off] = True
+    assert not kc.transpose(0, 2, 1, 3)[~written].any()
+    assert not vc.transpose(0, 2, 1, 3)[~written].any()
+
+
+@pytest.mark.parametrize("layout", [workloads.LAYOUT_BSND, workloads.LAYOUT_BNBD])
+@pytest.mark.parametrize("slot_dtype", ["int32", "int64"])
+@pytest.mark.parametrize("dims", [(128, 128), (64, 32), (24, 40)])
+def test_scatter_bitexact(torch_cuda, layout, slot_dtype, dims):
+    """Random slots (unique) with invalid ones mixed in, non-contiguous
+    key_scale, pre-filled caches: bytes equal the oracle's."""
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    Dk, Dv = dims
+    rng = np.random.default_rng(42 + Dk + layout)
+    T, Hh, NB, BS = 300, 4, 9, 128
+    key = rng.integers(0, 256, (T, Hh, Dk), dtype=np.uint8)
+    val = rng.integers(0, 256, (T, Hh, Dv), dtype=np.uint8)
+    ks_full = rng.standard_normal((T, 3 * Hh)).astype(np.float32)
+    slots = rng.choice(NB * BS, T, replace=False).astype(np.int64)
+    slots[::17] = -1
+    slots[5] = NB * BS
+    slots[6] = -7
+    shape_k = (NB, Hh, BS, Dk) if layout == workloads.LAYOUT_BNBD else (NB, BS, Hh, Dk)
+    shape_v = shape_k[:3] + (Dv,)
+    kc0 = rng.integers(0, 256, shape_k, dtype=np.uint8)
+    vc0 = rng.integers(0, 256, shape_v, dtype=np.uint8)
+    ksc0 = rng.standard_normal(shape_k[:3] + (1,)).astype(np.float32)
+    kc, vc, ksc = kc0.copy(), vc0.copy(), ksc0.copy()
+    oracle.cache_scatter(key, val, kc, vc, slots, ks_full[:, ::3], ksc, layout=layout)
+    gk = torch.from_numpy(kc0).cuda()
+    gv = torch.from_numpy(vc0).cuda()
+    gs = torch.from_numpy(ksc0).cuda()
+    ks_dev = torch.from_numpy(ks_full).cuda()[:, ::3]
+    pa.cache_scatter(torch.from_numpy(key).cuda(), torch.from_numpy(val).cuda(), gk, gv,
+                     torch.from_numpy(slots.astype(slot_dtype)).cuda(), ks_dev, gs, layout=layout)
+    assert np.array_equal(gk.cpu().numpy(), kc)
+    assert np.array_equal(gv.cpu().numpy(), vc)
+    assert np.array_equal(gs.cpu().numpy(), ksc)
+
+
+def _append_context():
+    ap = workloads.append()
+    return ap, ap.ctx
+
+
+def test_append_quant_scatter_bitexact_and_attend(torch_cuda):
+    """The append + attend step: 64 BF16 K/V rows quantised per token-head
+    (key_scale = amax/448) and scattered (5% slots -1) into a BNBD cache over
+    contexts of 512-8192 tokens, then GQA decode over the updated cache."""
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    ap, ctx = _append_context()
+    rng = np.random.default_rng(43)
+    bsel = np.sort(rng.choice(ctx.B, 12, replace=False))
+    # context caches, both paths (the oracle fills the sampled sequences)
+    inp = H.oracle_inputs(ctx, batches=bsel)
+    dev = H.device_inputs(ctx)
+    H.check_cache_bitexact(ctx, dev, inp)
+    # new tokens
+    k_new, v_new = ap.new_kv_f32()
+    kb, vb = ap.new_kv_bf16()
+    slot = ap.slot_mapping
+    c = dev["cache"]
+    pa.cache_quant_scatter(kb.cuda(), vb.cuda(), c.k_cache, c.v_cache,
+                           torch.from_numpy(slot).cuda(), c.k_scale, c.v_scale,
+                           torch.from_numpy(ap.token_batch).cuda(), layout=ctx.layout)
+    # oracle append for every new token (its cache holds only the sampled
+    # sequences' contexts; the appended rows are compared for all tokens)
+    kc, vc, ksc = inp["kc"], inp["vc"], inp["ksc"]
+    vs_all = c.v_scale.cpu().numpy()          # compared bit-exact below for bsel
+    for b in inp["batches"]:
+        assert np.array_equal(vs_all[b], inp["vs"][b])
+    vs_or = inp["vs"].copy()
+    # sequences outside bsel: the oracle computes their channel scales itself
+    k32, v32 = ctx.kv()
+    cu = ctx.cu_seqlens
+    for b in range(ctx.B):
+        if b not in set(bsel.tolist()):
+            vs_or[b] = oracle.value_channel_scale(v32[cu[b]:cu[b + 1]],
+                                                  np.array([0, cu[b + 1] - cu[b]]), 1)[0]
+    assert np.array_equal(vs_all, vs_or)
+    oracle.cache_quant_scatter(k_new, v_new, kc, vc, slot.astype(np.int64), ksc, vs_or,
+                               ap.token_batch, layout=ctx.layout)
+    gk, gv, gs = c.k_cache.cpu().numpy(), c.v_cache.cpu().numpy(), c.k_scale.cpu().numpy()
+    BS = ctx.BS
+    for i, s in enumerate(slot):
+        if s < 0:
+            continue
+        blk, off = s // BS, s % BS
+        assert np.array_equal(gk[blk, :, off], kc[blk, :, off]), i
+        assert np.array_equal(gv[blk, :, off], vc[blk, :, off]), i
+        assert np.array_equal(gs[blk, :, off], ksc[blk, :, off]), i
+    # skipped tokens left their slots untouched (still zero)
+    for b in np.nonzero(slot < 0)[0]:
+        a = int(ctx.act[b])
+        s = int(ctx.block_table[b, a // BS]) * BS + a % BS
+        assert not gk[s // BS, :, s % BS].any() and not gv[s // BS, :, s % BS].any()
+    # attend over the updated cache
+    act_after = ap.act_after
+    import dataclasses
+    ctx2 = dataclasses.replace(ctx, act=act_after)
+    out = torch.empty((ctx.B, ctx.NQ, ctx.D), dtype=torch.bfloat16, device="cuda")
+    ws = pa.DecodeWorkspace(ctx.B, 1, ctx.NQ, ctx.NKV)
+    pa.decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale,
+              dev["block_table"], torch.from_numpy(act_after).cuda(), out, S1=1,
+              layout=ctx.layout, workspace=ws)
+    rows = np.sort(np.concatenate([b * ctx.NQ + rng.choice(ctx.NQ, 6, replace=False)
+                                   for b in bsel]))
+    ref = oracle.pa_decode(inp["q8"], inp["qs"], kc, ksc, vc, vs_or, ctx.block_table, act_after,
+                           S1=1, NKV=ctx.NKV, layout=ctx.layout, s2_tile=512,
+                           softmax_scale=ctx.softmax_scale, rows=rows)
+    H.compare_bf16(H.to_u16(out), ref, rows=rows)
+    assert ws.error_flags() == 0

@@ -1,0 +1,182 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs. FP8 codes, scales and scattered bytes bit-exact; BF16
+attention output within max-abs 3e-2 / mean-abs 2e-3."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests import _helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    import fp8_paged_kv_block_gb300 as pa
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pa.lib()
+    return torch
+
+
+def _run_case(case, *, rows=None, batches=None, num_ctas=0, check_cache=True):
+    inp = H.oracle_inputs(case, batches=batches)
+    dev = H.device_inputs(case)
+    if check_cache:
+        H.check_cache_bitexact(case, dev, inp)
+    import fp8_paged_kv_block_gb300 as pa
+    ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile,
+                            num_ctas=num_ctas)
+    out = H.gpu_decode(case, dev, num_ctas=num_ctas, workspace=ws)
+    ref = H.oracle_decode(case, inp, rows=rows)
+    stats = H.compare_bf16(H.to_u16(out), ref, rows=rows)
+    assert ws.error_flags() == 0
+    return stats, out, dev, ws
+
+
+# ---------------------------------------------------------------------------
+# Quantisers and cache construction: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_quantize_rows_bitexact(torch_cuda, dtype):
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((777, 128)) * np.exp2(rng.uniform(-20, 20, (777, 1)))).astype(np.float32)
+    x[5] = 0.0
+    x[6, :] = -3.0
+    xt = torch.from_numpy(x).to(getattr(torch, dtype))
+    xf = xt.float().numpy()
+    codes = torch.empty((777, 128), dtype=torch.uint8, device="cuda")
+    scale = torch.empty(777, dtype=torch.float32, device="cuda")
+    pa.quantize_rows(xt.cuda(), codes, scale)
+    rc, rs = oracle.quant_rows(xf)
+    assert np.array_equal(scale.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_value_channel_scale_bitexact(torch_cuda):
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    rng = np.random.default_rng(22)
+    lens = np.array([3, 0, 200, 64, 1, 0, 129])
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    v = rng.standard_normal((int(cu[-1]), 8, 128)).astype(np.float32)
+    vs = torch.empty((len(lens), 8, 128), dtype=torch.float32, device="cuda")
+    pa.value_channel_scale(torch.from_numpy(v).cuda(), torch.from_numpy(cu).cuda(), vs)
+    ref = oracle.value_channel_scale(v, cu, len(lens))
+    assert np.array_equal(vs.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("layout", [workloads.LAYOUT_BSND, workloads.LAYOUT_BNBD])
+def test_cache_build_bitexact(torch_cuda, layout):
+    case = workloads.custom("build", 3, 1, 8, 2, [1, 300, 517], layout=layout)
+    inp = H.oracle_inputs(case)
+    dev = H.device_inputs(case)
+    H.check_cache_bitexact(case, dev, inp)
+    assert np.array_equal(dev["q8"].cpu().numpy(), inp["q8"])
+    assert np.array_equal(dev["qs"].cpu().numpy(), inp["qs"])
+
+
+# ---------------------------------------------------------------------------
+# Decode parity
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("s2_tile", [128, 256, 512])
+@pytest.mark.parametrize("layout", [workloads.LAYOUT_BSND, workloads.LAYOUT_BNBD])
+def test_decode_tiny(torch_cuda, s2_tile, layout):
+    _run_case(workloads.tiny(s2_tile=s2_tile, layout=layout))
+
+
+@pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 40, 152, 600])
+def test_decode_split_combine(torch_cuda, num_ctas):
+    """Several units, lengths on and off tile/block boundaries, one CTA up to
+    far more CTAs than tiles (every unit split and merged)."""
+    case = small_case()
+    _run_case(case, num_ctas=num_ctas)
+
+
+def small_case():
+    return workloads.custom("smallgqa", 5, 1, 24, 2, [1, 127, 128, 513, 1300], s2_tile=512)
+
+
+@pytest.mark.parametrize("acts", [[1], [31, 32, 33], [511, 512, 513], [1024, 1025, 2047]])
+def test_decode_boundaries(torch_cuda, acts):
+    case = workloads.custom("bnd", len(acts), 1, 12, 1, acts, s2_tile=512)
+    _run_case(case, num_ctas=5)
+
+
+def test_decode_zero_length(torch_cuda):
+    case = workloads.custom("zero", 4, 1, 8, 2, [0, 200, 0, 5])
+    stats, out, _, _ = _run_case(case, num_ctas=3)
+    o = out.float().cpu().numpy()
+    assert not o[0].any() and not o[2].any()
+
+
+def test_decode_s1_two_rows_per_head(torch_cuda):
+    """S1=2 with group 12: 24 query rows per kv head (two m16 tiles)."""
+    case = workloads.custom("s1two", 3, 2, 24, 2, [100, 700, 1500], s2_tile=512)
+    _run_case(case, num_ctas=4)
+
+
+def test_decode_large_group(torch_cuda):
+    """64 query rows per kv head: two 32-row chunks per (batch, kv head)."""
+    case = workloads.custom("biggroup", 2, 1, 64, 1, [300, 900], s2_tile=256)
+    _run_case(case, num_ctas=5)
+
+
+@pytest.mark.parametrize("i", range(len(workloads.PAGE_CASES)))
+def test_decode_page_cases(torch_cuda, i):
+    """The six (b, s1, s2, nq, nkv) shapes of the GLM-4.5 paged FP8 page's
+    test table, every sequence at its full s2."""
+    case = workloads.page_case(i)
+    rows = None
+    if case.B * case.S1 * case.NQ * int(case.act.max()) > 4_000_000:
+        rng = np.random.default_rng(i)
+        rows = np.sort(rng.choice(case.B * case.S1 * case.NQ, 48, replace=False))
+    _run_case(case, rows=rows)
+
+
+def test_decode_workspace_reuse_and_determinism(torch_cuda):
+    case = workloads.custom("reuse", 5, 1, 24, 2, [1, 127, 128, 513, 1300])
+    stats, out1, dev, ws = _run_case(case, num_ctas=7)
+    out2 = H.gpu_decode(case, dev, num_ctas=7, workspace=ws)
+    assert np.array_equal(H.to_u16(out1), H.to_u16(out2))
+    counters = ws.buf[256:256 + 4 * case.B * case.NKV].view(torch_cuda.int32).cpu().numpy()
+    assert not counters.any()
+    assert ws.error_flags() == 0
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads in the benchmark's launch configuration (default grid)
+# ---------------------------------------------------------------------------
+
+def test_decode_glm_full(torch_cuda):
+    """GLM-4.5 decode shape, every output row against the oracle."""
+    stats, *_ = _run_case(workloads.glm())
+    print("glm", stats)
+
+
+def test_decode_long_context_sampled(torch_cuda):
+    case = workloads.long_ctx()
+    rng = np.random.default_rng(31)
+    rows = np.sort(rng.choice(case.B * case.NQ, 24, replace=False))
+    batches = np.unique(rows // case.NQ)
+    stats, *_ = _run_case(case, rows=rows, batches=batches)
+    print("long", stats)
+
+
+def test_decode_ragged_sampled(torch_cuda):
+    case = workloads.ragged()
+    rng = np.random.default_rng(32)
+    # the longest, the shortest and random sequences
+    order = np.argsort(case.act)
+    bsel = np.unique(np.concatenate([order[:3], order[-3:], rng.choice(case.B, 10, replace=False)]))
+    rows = np.sort(np.concatenate([
+        (b * case.S1 + s) * case.NQ + rng.choice(case.NQ, 4, replace=False)
+        for b in bsel for s in range(case.S1)]))
+    stats, *_ = _run_case(case, rows=rows, batches=bsel)
+    print("ragged", stats)

@@ -147,10 +147,12 @@ class DecodeCase:
 
 
 def _paged(name, B, S1, NQ, NKV, act, max_blocks, seed, *, num_blocks=None, spare=0.10,
-           **kw) -> DecodeCase:
+           room=0, **kw) -> DecodeCase:
+    """Block pool and tables for sequences of lengths ``act`` with space for
+    ``room`` more tokens each."""
     act = np.asarray(act, dtype=np.int32)
     BS = kw.get("BS", 128)
-    need = [int(math.ceil(int(a) / BS)) for a in act]
+    need = [int(math.ceil((int(a) + room) / BS)) for a in act]
     total = sum(need)
     if num_blocks is None:
         num_blocks = max(1, int(math.ceil(total * (1.0 + spare))))
@@ -175,15 +177,15 @@ def glm(s2_tile: int = 512, layout: int = LAYOUT_BSND, seed_offset: int = 0) -> 
     """GLM-4.5 decode shape: B=16, NQ=96, NKV=8, lengths ~ U{1..4096}."""
     seed = BASE_SEED + 1 + 1000 * seed_offset
     act = _rng(seed, 9).integers(1, 4096, size=16, endpoint=True)
-    return _paged("glm", 16, 1, 96, 8, act, 32, seed, s2_tile=s2_tile, layout=layout)
+    return _paged("glm", 16, 1, 96, 8, act, 33, seed, s2_tile=s2_tile, layout=layout, room=1)
 
 
 def long_ctx(s2_tile: int = 512, layout: int = LAYOUT_BSND) -> DecodeCase:
     """B=4, NQ=96, NKV=8, lengths ~ U{32768..131072}, K outlier rows x8."""
     seed = BASE_SEED + 2
     act = _rng(seed, 9).integers(32768, 131072, size=4, endpoint=True)
-    return _paged("long", 4, 1, 96, 8, act, 1024, seed, s2_tile=s2_tile, layout=layout,
-                  k_outlier_every=64)
+    return _paged("long", 4, 1, 96, 8, act, 1025, seed, s2_tile=s2_tile, layout=layout,
+                  k_outlier_every=64, room=1)
 
 
 def ragged(s2_tile: int = 512, layout: int = LAYOUT_BSND, sigma: float = 1.0) -> DecodeCase:
@@ -191,7 +193,8 @@ def ragged(s2_tile: int = 512, layout: int = LAYOUT_BSND, sigma: float = 1.0) ->
     seed = BASE_SEED + 3
     x = _rng(seed, 9).normal(math.log(1024.0), sigma, size=256)
     act = np.clip(np.rint(np.exp(x)), 1, 16384).astype(np.int32)
-    return _paged("ragged", 256, 2, 96, 8, act, 128, seed, s2_tile=s2_tile, layout=layout)
+    return _paged("ragged", 256, 2, 96, 8, act, 129, seed, s2_tile=s2_tile, layout=layout,
+                  room=1)
 
 
 def custom(name, B, S1, NQ, NKV, act, *, max_blocks=None, seed=BASE_SEED + 7, **kw):
@@ -218,6 +221,25 @@ def page_case(i: int, s2_tile: int = 512) -> DecodeCase:
     b, s1, s2, nq, nkv = PAGE_CASES[i]
     return custom("page%d" % i, b, s1, nq, nkv, [s2] * b, seed=BASE_SEED + 100 + i,
                   s2_tile=s2_tile)
+
+
+def step_tokens(case: DecodeCase, seed_offset: int = 0):
+    """One new token per sequence for a decode step: (key, value) BF16 torch
+    CPU tensors [B, NKV, D] drawn N(0,1), the int32 slot of position
+    kv_act_seqs[b] in each sequence's block table (-1 where the table has no
+    room), and the lengths after the append."""
+    import torch  # BF16 rounding by the library routine
+    r = _rng(case.seed, 4, seed_offset)
+    shape = (case.B, case.NKV, case.D)
+    k = torch.from_numpy(r.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(r.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
+    a = case.act.astype(np.int64)
+    bi = a // case.BS
+    ok = bi < case.max_blocks
+    blk = np.where(ok, case.block_table[np.arange(case.B), np.minimum(bi, case.max_blocks - 1)], -1)
+    slot = np.where(blk >= 0, blk.astype(np.int64) * case.BS + a % case.BS, -1).astype(np.int32)
+    act_after = (case.act + (slot >= 0)).astype(np.int32)
+    return k, v, slot, act_after
 
 
 @dataclasses.dataclass
