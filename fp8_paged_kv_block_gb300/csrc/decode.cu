@@ -904,3 +904,76 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     if (pl.S2T == 256) return launch<2, 256>(tk, tv, prm, s);
     return launch<2, 512>(tk, tv, prm, s);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of pa_fp8_decode: the same kernel, with its scratch
+// (split partials, per-sequence counters, error flag) in a fixed array that
+// is part of the library's device image instead of a caller workspace.
+// ---------------------------------------------------------------------------
+namespace pa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(PA_FP8_DECODE_NOALLOC_MAX_SCRATCH);
+
+// One array per device that loads the library, alive until process exit.
+__device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+// Device address of g_decode_scratch on the current device. The host-side
+// name is only a stand-in for the symbol, so the address is looked up once
+// per device (with that device current) and cached.
+pa_status decode_scratch_address(void** out)
+{
+    static std::mutex mu;
+    static void* cache[64] = {nullptr};
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode_noalloc: cudaGetDevice: %s",
+               cudaGetErrorString(e));
+    PA_REQUIRE(dev >= 0 && dev < 64, PA_ERR_UNSUPPORTED, "pa_fp8_decode_noalloc: device %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        PA_REQUIRE(e == cudaSuccess && p != nullptr, PA_ERR_CUDA,
+                   "pa_fp8_decode_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        cache[dev] = p;
+    }
+    *out = cache[dev];
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_fp8_decode_noalloc(const void* q, const float* q_scale, const void* k_cache,
+                                           const float* k_scale, const void* v_cache,
+                                           const float* v_scale, const int32_t* block_table,
+                                           const int32_t* kv_act_seqs, void* out, int B, int S1,
+                                           int NQ, int NKV, int D, int block_size,
+                                           int64_t num_blocks, int max_blocks_per_seq, int layout,
+                                           float softmax_scale, const pa_decode_config* cfg,
+                                           void* stream)
+{
+    PA_REQUIRE(q && q_scale && k_cache && k_scale && v_cache && v_scale && block_table &&
+                   kv_act_seqs && out,
+               PA_ERR_NULLPTR, "pa_fp8_decode_noalloc: NULL tensor pointer");
+    Plan pl;
+    pa_status st = make_plan(B, S1, NQ, NKV, D, cfg, &pl);
+    if (st != PA_OK) return st;
+    PA_REQUIRE(pl.total <= kStaticScratchBytes, PA_ERR_WORKSPACE,
+               "pa_fp8_decode_noalloc: this shape needs %zu bytes of scratch, more than the "
+               "built-in %zu; use pa_fp8_decode with a caller workspace",
+               pl.total, kStaticScratchBytes);
+    void* ws = nullptr;
+    st = decode_scratch_address(&ws);
+    if (st != PA_OK) return st;
+    // The array keeps the previous call's contents: the error flag and the
+    // per-sequence counters must start at zero.
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeader + pl.counters_bytes, s);
+    PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode_noalloc: clearing scratch: %s",
+               cudaGetErrorString(e));
+    return pa_fp8_decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs,
+                         out, B, S1, NQ, NKV, D, block_size, num_blocks, max_blocks_per_seq, layout,
+                         softmax_scale, cfg, ws, kStaticScratchBytes, stream);
+}

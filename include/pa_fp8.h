@@ -158,6 +158,43 @@ PA_API pa_status pa_fp8_decode(const void* q, const float* q_scale,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_fp8_decode_noalloc: the same decode as pa_fp8_decode for callers that
+ * cannot allocate device memory. The pages have no counterpart to it; it
+ * exists for callers that are handed tensor pointers and a stream but own no
+ * allocator -- for example a plugin inside another framework's runtime, or
+ * a serving loop whose device memory is planned up front and which must not
+ * call cudaMalloc in the middle of a step (cudaMalloc can synchronise the
+ * device and can fail under memory pressure).
+ *
+ * It takes the arguments of pa_fp8_decode except the workspace. Its scratch
+ * is a fixed array of PA_FP8_DECODE_NOALLOC_MAX_SCRATCH bytes compiled into
+ * the library; every GPU that loads the library holds that array until the
+ * process exits. Shapes whose pa_fp8_decode_workspace_size() exceeds it are
+ * rejected with PA_ERR_WORKSPACE (nothing is enqueued).
+ *  - No cudaMalloc, cudaFree or allocating library routine is called.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Each call clears the scratch's flag and counter words with
+ *    cudaMemsetAsync on `stream`, then launches the decode kernel.
+ *  - All calls on a device share the one array: calls whose execution
+ *    overlaps on the GPU (different streams without ordering) race and give
+ *    wrong results. Calls ordered on one stream are safe.
+ * ------------------------------------------------------------------------ */
+#define PA_FP8_DECODE_NOALLOC_MAX_SCRATCH (16u << 20)
+
+PA_API pa_status pa_fp8_decode_noalloc(const void* q, const float* q_scale,
+                                       const void* k_cache, const float* k_scale,
+                                       const void* v_cache, const float* v_scale,
+                                       const int32_t* block_table,
+                                       const int32_t* kv_act_seqs, void* out,
+                                       int B, int S1, int NQ, int NKV, int D,
+                                       int block_size, int64_t num_blocks,
+                                       int max_blocks_per_seq, int layout,
+                                       float softmax_scale, const pa_decode_config* cfg,
+                                       void* stream);
+
+/* ------------------------------------------------------------------------
  * FP8 cache append scatter ([SC] 功能说明与计算公式, 参数说明, 约束说明).
  * In place. For token i < num_tokens and head j < num_head, with
  * s = slot_mapping[i]:
