@@ -105,7 +105,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    uint32_t ns = 16;
     for (uint32_t it = 1;; ++it) {
+        // back off so that waiting warps leave issue slots to working ones
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0) {
             if (*abort) return false;
@@ -152,6 +156,29 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
+// 2-D TMA tile load without an L2 policy.
+__device__ __forceinline__ void tma_load_2d_nohint(void* dst, const void* tmap, int x, int y,
+                                                   uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
+// of 16), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {
     uint64_t p;
@@ -181,11 +208,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "r"(addr));
 }
 
-// D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col)
+// D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col). Registers only,
+// so not volatile: the compiler may schedule it after later (volatile)
+// shared-memory loads, which is what hides their latency.
 __device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1)
 {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
