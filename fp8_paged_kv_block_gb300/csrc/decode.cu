@@ -505,27 +505,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kbase = smem_u32(sm.ring[ks_slot]);
                 const float* ksm = sm.kscale[ks_slot];
                 const bool full = wtok0 + TPW <= valid;
+                // key scales first (their latency overlaps the MMAs)
+                float kv0[NT8], kv1[NT8];
 #pragma unroll
                 for (int j = 0; j < NT8; ++j) {
-                    uint32_t bb[8];
+                    const int trow = wrow0 + 8 * j + 2 * tq;
+                    kv0[j] = ksm[trow * ks_st + ks_off];
+                    kv1[j] = ksm[(trow + 1) * ks_st + ks_off];
+                }
+                // K fragments double-buffered one n8 tile ahead of the MMAs
+                uint32_t bb[2][8];
+                auto load_k = [&](int j, uint32_t (&dst)[8]) {
                     const int row = wrow0 + 8 * j + (lane & 7);
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         const int chunk = hf * 4 + (lane >> 3);
-                        ldsm_x4(kbase + row * 128 + ((chunk ^ (row & 7)) << 4), bb[4 * hf],
-                                bb[4 * hf + 1], bb[4 * hf + 2], bb[4 * hf + 3]);
+                        ldsm_x4(kbase + row * 128 + ((chunk ^ (row & 7)) << 4), dst[4 * hf], dst[4 * hf + 1],
+                                dst[4 * hf + 2], dst[4 * hf + 3]);
                     }
+                };
+                load_k(0, bb[0]);
+#pragma unroll
+                for (int j = 0; j < NT8; ++j) {
+                    if (j + 1 < NT8) load_k(j + 1, bb[(j + 1) & 1]);
                     float c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma_e4m3(c4, qa[kk], bb[2 * kk], bb[2 * kk + 1]);
+                    for (int kk = 0; kk < 4; ++kk) mma_e4m3(c4, qa[kk], bb[j & 1][2 * kk], bb[j & 1][2 * kk + 1]);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[j][e] = c4[e];
                 }
 #pragma unroll
                 for (int j = 0; j < NT8; ++j) {
-                    const int trow = wrow0 + 8 * j + 2 * tq;
-                    const float k0 = ksm[trow * ks_st + ks_off];
-                    const float k1 = ksm[(trow + 1) * ks_st + ks_off];
+                    const float k0 = kv0[j];
+                    const float k1 = kv1[j];
                     const int tk = wtok0 + 8 * j + 2 * tq;
                     const bool v0 = full || tk < valid, v1 = full || tk + 1 < valid;
 #pragma unroll
@@ -658,10 +670,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t m1 = (tk + 8 < lim ? 0x0000FFFFu : 0u) | (tk + 9 < lim ? 0xFFFF0000u : 0u);
                     const uint32_t m2 = (tk + 16 < lim ? 0x0000FFFFu : 0u) | (tk + 17 < lim ? 0xFFFF0000u : 0u);
                     const uint32_t m3 = (tk + 24 < lim ? 0x0000FFFFu : 0u) | (tk + 25 < lim ? 0xFFFF0000u : 0u);
+                    // all four channel chunks of this k-step in flight at once
+                    uint32_t rv[4][4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        ldsm_x4_t(vbase + row * 128 + (((4 * dh + c) ^ (row & 7)) << 4), rv[c][0], rv[c][1],
+                                  rv[c][2], rv[c][3]);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        uint32_t r0, r1, r2, r3;
-                        ldsm_x4_t(vbase + row * 128 + (((4 * dh + c) ^ (row & 7)) << 4), r0, r1, r2, r3);
+                        uint32_t r0 = rv[c][0], r1 = rv[c][1], r2 = rv[c][2], r3 = rv[c][3];
                         if (lim < 32) {  // zero V bytes of tokens past the sequence end
                             r0 &= m0;
                             r1 &= m1;
