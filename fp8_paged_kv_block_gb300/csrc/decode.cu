@@ -12,25 +12,35 @@
 //    rows are all S1 x group query rows that share kv head n2, so each K/V
 //    byte is read once for all of them. The unit's KV is walked in s2 tiles.
 //  * Persistent grid, one CTA per SM. The flattened (unit, tile) sequence is
-//    cut into contiguous per-CTA ranges balanced by token count (plus a fixed
-//    per-tile cost); ranges start and end on tile boundaries so the
-//    P-quantisation groups are those of the sequential walk. A unit split
+//    cut into contiguous per-CTA ranges balanced by token count (plus fixed
+//    per-unit and per-tile costs); ranges start and end on tile boundaries so
+//    the P-quantisation groups are those of the sequential walk. A unit split
 //    across CTAs is merged by whichever CTA finishes its part last
 //    (log-sum-exp combine through the workspace; no waiting on other CTAs).
-//  * One thread of warp 8 is the producer. Per 128-token block it issues one
-//    2-D TMA load (128 rows x 128 bytes, 128-byte swizzle) of K or V into a
-//    shared-memory ring, plus one TMA of the block's key scales with K; the
-//    unit's Q rows arrive by 1-D bulk copies. Block ids are loaded one tile
-//    ahead, so no global load sits between two copies.
-//  * Warps 0-7 consume. MM1: warp w takes s2_tile/8 tokens, FP8 mma.sync
-//    m16n8k32 with Q as A (rows padded to 16/32) and K rows (ldmatrix) as B.
-//    Row maxima meet in shared memory; P = exp2(S*log2e - M), its sum, and the
-//    E4M3 quantisation (cvt.rn.satfinite) stay in registers, written once to
-//    shared memory already in mma A-fragment order. MM2: warp w owns 16 of
-//    the 128 output channels over the whole tile; V comes in through
-//    ldmatrix.trans + byte permutes so no transpose pass is needed.
-//  * Masked tokens (beyond kv_act_seqs) get S = -inf, P = 0, and their V
-//    bytes are zeroed in registers (a stale E4M3 NaN code times 0 is NaN).
+//  * Warp 8 (one thread) is the producer: per 128-token block one 2-D TMA
+//    load (128 rows x 128 bytes, 128-byte swizzle) of K or V into a
+//    shared-memory ring, plus the block's key scales with K; per unit the Q
+//    rows, q_scale and v_scale. Block ids are loaded one tile ahead.
+//  * Warp 9 owns the tensor memory and issues the tensor-core MMAs
+//    (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32, M = 128) from one thread:
+//      MM1  S^T[token][row]   = K_blk (K-major, the ring slot as loaded)
+//                               x Q^T (K-major, 128-byte swizzled rows)
+//      MM2  O^T[chan][row]    = V_blk^T (MN-major: the same ring slot)
+//                               x P8^T (MN-major, written by the consumers)
+//    S^T lives in tensor memory, double-buffered across tiles; O^T of one
+//    tile is a fresh tensor-memory accumulator.
+//  * Warps 0-7 consume: tcgen05.ld of S^T (a lane = a token, a column = a
+//    query row), scaling by q_scale * k_scale, masking past kv_act_seqs, the
+//    tile's row maxima (butterfly over lanes, then over warps through shared
+//    memory), P = 2^(x - tile max), the row sums, E4M3 P8 = 448 * P written
+//    as the MM2 operand, then the tile's O^T folded into registers with the
+//    running-max rescale. Quantising against the tile's own maximum gives the
+//    same codes as quantising exp(S - running max) against its tile maximum
+//    (the ratio cancels the running max); the running max only weights whole
+//    tiles.
+//  * Masked tokens get S = -inf (selected, never multiplied) and P = 0; the
+//    V rows of a partial last block are zeroed in shared memory before MM2
+//    (a stale E4M3 NaN code times 0 is NaN).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -45,7 +55,12 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBS = 128;
 constexpr int kNCW = 8;                      // consumer warps
-constexpr int kThreads = (kNCW + 1) * 32;    // + one producer warp
+constexpr int kKProducerWarp = kNCW;        // K blocks, key scales, per-unit header
+constexpr int kVProducerWarp = kNCW + 1;    // V blocks
+constexpr int kMmaWarp = kNCW + 2;          // tensor memory owner; issues MM1
+constexpr int kMma2Warp = kNCW + 3;         // issues MM2
+constexpr int kThreads = (kNCW + 4) * 32;
+constexpr int kKSlots = 4;                   // K ring; the V ring takes the other slots
 constexpr int kSlotBytes = kBS * kD;         // one 128-token block of one head
 constexpr int kKsFloats = 512;               // key-scale area per ring slot
 constexpr int kMaxB = 1024;
@@ -63,37 +78,73 @@ enum : int {
     KS_WHOLE = 2     // BSND, NKV <= 3: the block's whole [128][NKV] region
 };
 
-template <int MT, int S2T>
-struct DecodeCfg {
-    static constexpr int NSLOT = (MT == 2 && S2T == 512) ? 9 : 10;
-};
+__host__ __device__ constexpr uint32_t tmem_cols(int need)
+{
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(need)) c <<= 1;
+    return c;
+}
 
-template <int MT, int S2T>
-struct __align__(1024) DecodeSmem {
-    static constexpr int NSLOT = DecodeCfg<MT, S2T>::NSLOT;
-    alignas(1024) uint8_t ring[NSLOT][kSlotBytes];
-    alignas(1024) float kscale[NSLOT][kKsFloats];
-    // P8 A-fragments (two-row-tile path only)
-    alignas(128) uint32_t pfrag[MT == 1 ? 1 : 2][MT == 1 ? 1 : S2T / 32][MT][32][4];
-    // P8 swap between paired warps / cross-warp output sum (one-row-tile path)
-    alignas(128) float obuf[MT == 1 ? kNCW * 512 : 4];
-    alignas(128) uint8_t q[2][32][kD];
-    alignas(128) float vsc[2][kD];
-    float red_max[2][kNCW][32];
-    float red_l[kNCW][32];
-    float rrow[32];
-    float lrow[32];
-    float mrow[32];
-    int scan[kThreads];
+// S^T buffers in tensor memory (MM1 may run that many tiles ahead of the
+// consumers): as many as fit next to O^T in the 512 columns, at most 4.
+__host__ __device__ constexpr int s_buffers(int sc, int nr)
+{
+    return (4 * sc + nr <= 512) ? 4 : ((3 * sc + nr <= 512) ? 3 : 2);
+}
+
+// NR: padded query rows per unit (16 or 32, the MMA N); S2T: s2 tile; NS:
+// ring slots (as many as fit): slots 0 .. kKSlots-1 hold K blocks, the rest
+// V blocks, each ring with its own producer.
+template <int NR, int S2T, int NS>
+struct __align__(1024) DecodeSmemT {
+    static constexpr int NSLOT = NS;
+    alignas(1024) uint8_t ring[NS][kSlotBytes];
+    // Q rows: bulk-copied as plain rows, then swizzled in place into the
+    // 128-byte-swizzled K-major operand layout
+    alignas(1024) uint8_t qb[2][NR][kD];
+    // P8^T, MN-major without swizzle: token t, row r at
+    // (t / 8) * 8 * NR + (r / 16) * 128 + (t % 8) * 16 + r % 16
+    alignas(1024) uint8_t pbuf[S2T * NR];
+    // key scales of one tile's blocks, double-buffered by tile parity
+    alignas(128) float ksb[2][S2T / kBS][kKsFloats];
+    alignas(16) float vsc[2][kD];
+    alignas(16) float qs[2][32];
+    float red[2][kNCW][32];     // per-warp row maxima, double-buffered by tile
+    float redl[kNCW][32];       // per-warp row sums at unit end
+    alignas(16) float wst[kNCW][4][32];   // per-warp copies of row values
+    int scan[kThreads / 32];
     int bpre[kMaxB + 1];
     int slen[kMaxB];
-    uint64_t full_bar[NSLOT];
-    uint64_t empty_bar[NSLOT];
+    uint64_t full_bar[NS];
+    uint64_t empty_bar[NS];
     uint64_t hdr_full[2];
     uint64_t hdr_empty[2];
+    uint64_t ks_full[2];
+    uint64_t ks_empty[2];
+    uint64_t s_full[4];
+    uint64_t s_empty[4];
+    uint64_t p_full;
+    uint64_t o_full;
+    uint64_t done_bar;
+    uint32_t tmem;
+    int k_tiles;                // tiles whose K blocks the K producer has requested
     int flag;
     int abort;
 };
+
+constexpr size_t kSmemOptIn = 232448;   // per-block opt-in maximum (the +1024 is alignment slack)
+
+template <int NR, int S2T>
+constexpr int pick_slots()
+{
+    return sizeof(DecodeSmemT<NR, S2T, 12>) + 1024 <= kSmemOptIn   ? 12
+           : sizeof(DecodeSmemT<NR, S2T, 11>) + 1024 <= kSmemOptIn ? 11
+           : sizeof(DecodeSmemT<NR, S2T, 10>) + 1024 <= kSmemOptIn ? 10
+                                                                    : 9;
+}
+
+template <int NR, int S2T>
+using DecodeSmem = DecodeSmemT<NR, S2T, pick_slots<NR, S2T>()>;
 
 struct DecodeParams {
     const uint8_t* q;
@@ -206,21 +257,77 @@ __device__ __forceinline__ void zero_rows(const DecodeParams& p, int b, int tid,
     for (int64_t k = tid; k < n16; k += nthreads) dst[k] = make_uint4(0, 0, 0, 0);
 }
 
-template <int MT, int S2T>
+// Butterfly reduction over the 32 lanes of a warp of N per-lane values (one
+// per query row): on return lane L holds the reduction of row
+// (N == 16 ? L / 2 : L) over all lanes. `a` is clobbered.
+template <int N, bool kMax>
+__device__ __forceinline__ float lane_reduce(float (&a)[N], int lane)
+{
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        const int h = N >> (s + 1);
+        if (h == 0) break;
+        const int o = 16 >> s;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float keep = up ? a[i + h] : a[i];
+            const float send = up ? a[i] : a[i + h];
+            const float got = __shfl_xor_sync(0xffffffffu, send, o);
+            a[i] = kMax ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    float v = a[0];
+    if (N == 16) {
+        const float got = __shfl_xor_sync(0xffffffffu, v, 1);
+        v = kMax ? fmaxf(v, got) : v + got;
+    }
+    return v;
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v)
+{
+    if constexpr (N == 8) {
+        tmem_ld8(taddr, v);
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 16) tmem_ld16(taddr + c, v + c);
+    }
+}
+
+template <int NSLOT>
+__device__ __forceinline__ int ring_slot(int slot, uint32_t ph, int j, uint32_t* par)
+{
+    int s = slot + j;
+    *par = ph;
+    if (s >= NSLOT) {
+        s -= NSLOT;
+        *par ^= 1u;
+    }
+    return s;
+}
+
+template <int NR, int S2T>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmKS, const DecodeParams p)
 {
-    constexpr int NSLOT = DecodeCfg<MT, S2T>::NSLOT;
-    constexpr int RCH = MT * 16;      // rows per unit chunk (padded)
-    constexpr int NBT = S2T / kBS;    // blocks per tile
-    constexpr int TPW = S2T / kNCW;   // MM1 tokens per warp
-    constexpr int NT8 = TPW / 8;      // n8 tiles per warp
+    constexpr int NBT = S2T / kBS;               // 128-token blocks (MMA M-blocks) per tile
+    constexpr int MBW = NBT >= 2 ? NBT / 2 : 1;  // blocks per consumer warp
+    constexpr int SC = NBT * NR;                 // tensor-memory columns of one S^T buffer
+    constexpr int NSB = s_buffers(SC, NR);       // S^T buffers
+    constexpr int OCOL = NSB * SC;               // first column of O^T
+    constexpr uint32_t TCOLS = tmem_cols(NSB * SC + NR);
+    constexpr int HR = NR / 2;                   // O^T columns (query rows) per consumer warp
     constexpr int TC = S2T + kC0;
+    constexpr int NSLOT = DecodeSmem<NR, S2T>::NSLOT;
+    constexpr int NK = kKSlots, NV = NSLOT - kKSlots;
+    static_assert(NV >= NBT, "the V ring must hold one tile");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    auto& sm = *reinterpret_cast<DecodeSmem<MT, S2T>*>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
+    auto& sm = *reinterpret_cast<DecodeSmem<NR, S2T>*>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int W = p.NKV * p.NRC;
@@ -228,20 +335,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < NSLOT; ++i) {
             mbar_init(&sm.full_bar[i], 1);
-            mbar_init(&sm.empty_bar[i], kNCW);
+            mbar_init(&sm.empty_bar[i], 1);          // the MMAs reading the slot completed
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.hdr_full[i], 1);
-            mbar_init(&sm.hdr_empty[i], kNCW);
+            mbar_init(&sm.hdr_full[i], 2);           // byte-counted copies + the q_scale cp.async
+            mbar_init(&sm.hdr_empty[i], 1 + kNCW);   // last MM1 of the unit + every consumer warp
+            mbar_init(&sm.ks_full[i], 1);
+            mbar_init(&sm.ks_empty[i], kNCW);
         }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.s_empty[i], kNCW);
+        }
+        mbar_init(&sm.p_full, kNCW);
+        mbar_init(&sm.o_full, 1);
+        mbar_init(&sm.done_bar, 2);                  // one commit from each MMA-issuing warp
         sm.abort = 0;
+        sm.k_tiles = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // Rows of a query chunk shorter than 32 are never copied in: start from
-    // zeros (later such rows hold earlier finite Q codes, and their q_scale
-    // is taken as 0).
-    for (int k = tid; k < 2 * 32 * kD / 16; k += kThreads)
-        reinterpret_cast<uint4*>(&sm.q[0][0][0])[k] = make_uint4(0, 0, 0, 0);
+    // warm L2 with the block table; the producer reads it once its range is known
+    {
+        const int64_t bt_bytes = static_cast<int64_t>(p.B) * p.max_blocks * 4;
+        if (static_cast<int64_t>(tid) * 128 < bt_bytes)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(p.block_table) +
+                                                          static_cast<size_t>(tid) * 128));
+    }
 
     // ---- per-batch lengths and cost prefix: cost(b) = kCU + len_b + tiles_b * kC0 --
     {
@@ -301,568 +420,313 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Pos end = find_pos<S2T>(sm.slen, sm.bpre, p.B,
                                   (static_cast<int64_t>(cta + 1) * Ctot + grid - 1) / grid, Ctot, W);
 
-    if (warp == kNCW) {
-        // =============================== producer ===============================
+    // tensor memory: allocated by the MMA warp, address published in shared memory
+    if (warp == kMmaWarp) tmem_alloc(&sm.tmem, TCOLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+
+    if (warp == kKProducerWarp || warp == kVProducerWarp) {
+        // ============================== producers ==============================
+        // The K producer fills the K ring (plus key scales and the per-unit
+        // header), the V producer the V ring; each runs ahead of the MMAs as
+        // far as its own ring allows, so V tiles waiting for their P never
+        // hold back the next tile's K.
         if (lane != 0) return;
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmK) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmV) : "memory");
-        if (p.ks_mode == KS_QUAD) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmKS) : "memory");
+        const bool isK = warp == kKProducerWarp;
+        const CUtensorMap* tm = isK ? &tmK : &tmV;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
+        if (isK && p.ks_mode == KS_QUAD) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmKS) : "memory");
         const uint64_t pol = l2_evict_first_policy();
         const int ks_bytes = p.ks_mode == KS_CONTIG ? kBS * 4
                                                     : (p.ks_mode == KS_QUAD ? kBS * 16 : kBS * 4 * p.NKV);
+        const int base = isK ? 0 : NK, nring = isK ? NK : NV;
         int slot = 0;
         uint32_t ph = 0;
-        int hcount = 0;
+        int hcount = 0, fills = 0, tcount = 0;
         bool first = true;
-        // block ids of the current and the next tile (loaded one tile ahead)
-        int cid[NBT], nid[NBT];
-#pragma unroll
-        for (int j = 0; j < NBT; ++j) nid[j] = 0;
+        // block ids, loaded two tiles ahead of their use
+        int id0[NBT], id1[NBT], id2[NBT];
         auto load_ids = [&](const Pos& x, int (&ids)[NBT]) {
+            if (pos_eq(x, end)) return;
             const int nbx = min(NBT, (sm.slen[x.b] - x.t * S2T + kBS - 1) / kBS);
             const int* row = p.block_table + static_cast<int64_t>(x.b) * p.max_blocks + x.t * NBT;
 #pragma unroll
             for (int j = 0; j < NBT; ++j) ids[j] = j < nbx ? __ldg(row + j) : 0;
         };
-        load_ids(start, cid);
+#pragma unroll
+        for (int j = 0; j < NBT; ++j) id0[j] = id1[j] = id2[j] = 0;
+        Pos x1 = start;
+        load_ids(start, id0);
+        if (!pos_eq(start, end)) {
+            x1 = pos_next<S2T>(sm.slen, sm.bpre, p.B, start, W);
+            load_ids(x1, id1);
+        }
         for (Pos x = start; !pos_eq(x, end);) {
-            const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
-            if (!pos_eq(nx, end)) load_ids(nx, nid);
+            const Pos nx = x1;
+            if (!pos_eq(nx, end)) {
+                x1 = pos_next<S2T>(sm.slen, sm.bpre, p.B, nx, W);
+                load_ids(x1, id2);
+            }
             const int b = x.b, n2 = x.i / p.NRC, rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
             const int len = sm.slen[b];
-            if (first || t == 0) {
-                // this unit's Q rows: one bulk copy per run of consecutive rows
+            if (isK && (first || t == 0)) {
+                // the unit's Q rows (one bulk copy per run of consecutive rows),
+                // its q_scale values and its v_scale row
                 const int hs = hcount & 1;
                 mbar_wait(&sm.hdr_empty[hs], ((hcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort);
-                const int r0 = rc * RCH, r1 = min(p.R, r0 + RCH);
+                const int r0 = rc * NR, r1 = min(p.R, r0 + NR);
                 mbar_arrive_expect_tx(&sm.hdr_full[hs], static_cast<uint32_t>((r1 - r0) * kD + kD * 4));
                 bulk_load_1d(&sm.vsc[hs][0], p.v_scale + (static_cast<int64_t>(b) * p.NKV + n2) * kD,
                              kD * 4, &sm.hdr_full[hs]);
                 for (int r = r0; r < r1;) {
                     const int s = r / p.G, g0 = r - s * p.G;
                     const int n = min(p.G - g0, r1 - r);
-                    bulk_load_1d(&sm.q[hs][r - r0][0], p.q + q_row(p, b, n2, r) * kD,
-                                 static_cast<uint32_t>(n * kD), &sm.hdr_full[hs]);
+                    const int64_t row = q_row(p, b, n2, r);
+                    bulk_load_1d(&sm.qb[hs][r - r0][0], p.q + row * kD, static_cast<uint32_t>(n * kD),
+                                 &sm.hdr_full[hs]);
+                    for (int k = 0; k < n; ++k) cp_async4(&sm.qs[hs][r - r0 + k], p.q_scale + row + k, 4);
                     r += n;
                 }
+                cp_async_arrive_noinc(&sm.hdr_full[hs]);
                 ++hcount;
-                first = false;
             }
+            first = false;
             const int nb = min(NBT, (len - t * S2T + kBS - 1) / kBS);
-            for (int kind = 0; kind < 2; ++kind) {
-#pragma unroll
-                for (int j = 0; j < NBT; ++j) {
-                    if (j >= nb) break;
-                    mbar_wait(&sm.empty_bar[slot], ph ^ 1, p.err, 4, &sm.abort);
-                    int blk = cid[j];
-                    if (blk < 0 || blk >= p.num_blocks) blk = 0;
-                    int x0, y0;
-                    if (p.layout == PA_LAYOUT_BSND) {
-                        x0 = n2 * kD;
-                        y0 = blk * kBS;
-                    } else {
-                        x0 = 0;
-                        y0 = (blk * p.NKV + n2) * kBS;
-                    }
-                    if (kind == 0) {
-                        mbar_arrive_expect_tx(&sm.full_bar[slot], kSlotBytes + ks_bytes);
-                        tma_load_2d(sm.ring[slot], &tmK, x0, y0, &sm.full_bar[slot], pol);
-                        if (p.ks_mode == KS_CONTIG)
-                            bulk_load_1d(sm.kscale[slot],
-                                         p.k_scale + (static_cast<int64_t>(blk) * p.NKV + n2) * kBS,
-                                         kBS * 4, &sm.full_bar[slot]);
-                        else if (p.ks_mode == KS_QUAD)
-                            tma_load_2d_nohint(sm.kscale[slot], &tmKS, n2 & ~3, blk * kBS,
-                                               &sm.full_bar[slot]);
-                        else
-                            bulk_load_1d(sm.kscale[slot],
-                                         p.k_scale + static_cast<int64_t>(blk) * kBS * p.NKV,
-                                         static_cast<uint32_t>(ks_bytes), &sm.full_bar[slot]);
-                    } else {
-                        mbar_arrive_expect_tx(&sm.full_bar[slot], kSlotBytes);
-                        tma_load_2d(sm.ring[slot], &tmV, x0, y0, &sm.full_bar[slot], pol);
-                    }
-                    if (++slot == NSLOT) {
-                        slot = 0;
-                        ph ^= 1;
+            // V blocks of a tile are requested only after its K blocks: K is
+            // needed first (MM1, softmax), V only once P is known
+            if (!isK) {
+                const volatile int* kt = &sm.k_tiles;
+                if (*kt <= tcount) {
+                    const uint64_t t0 = globaltimer_ns();
+                    volatile int* ab = &sm.abort;
+                    while (*kt <= tcount) {
+                        __nanosleep(64);
+                        if (*ab) break;
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            *ab = 1;
+                            atomicOr(p.err, 2048);
+                            break;
+                        }
                     }
                 }
             }
+            // this tile's key scales go to their own buffer (tile parity kb)
+            const int kb = tcount & 1;
+            if (isK) {
+                mbar_wait(&sm.ks_empty[kb], ((tcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort);
+                mbar_arrive_expect_tx(&sm.ks_full[kb], static_cast<uint32_t>(nb * ks_bytes));
+            }
 #pragma unroll
-            for (int j = 0; j < NBT; ++j) cid[j] = nid[j];
+            for (int j = 0; j < NBT; ++j) {
+                if (j >= nb) break;
+                const int sl = base + slot;
+                mbar_wait(&sm.empty_bar[sl], ph ^ 1, p.err, 4, &sm.abort);
+                int blk = id0[j];
+                if (blk < 0 || blk >= p.num_blocks) blk = 0;
+                int x0, y0;
+                if (p.layout == PA_LAYOUT_BSND) {
+                    x0 = n2 * kD;
+                    y0 = blk * kBS;
+                } else {
+                    x0 = 0;
+                    y0 = (blk * p.NKV + n2) * kBS;
+                }
+                mbar_arrive_expect_tx(&sm.full_bar[sl], kSlotBytes);
+                tma_load_2d(sm.ring[sl], tm, x0, y0, &sm.full_bar[sl], pol);
+                if (isK) {
+                    float* kdst = sm.ksb[kb][j];
+                    if (p.ks_mode == KS_CONTIG)
+                        bulk_load_1d(kdst, p.k_scale + (static_cast<int64_t>(blk) * p.NKV + n2) * kBS, kBS * 4,
+                                     &sm.ks_full[kb]);
+                    else if (p.ks_mode == KS_QUAD)
+                        tma_load_2d_nohint(kdst, &tmKS, n2 & ~3, blk * kBS, &sm.ks_full[kb]);
+                    else
+                        bulk_load_1d(kdst, p.k_scale + static_cast<int64_t>(blk) * kBS * p.NKV,
+                                     static_cast<uint32_t>(ks_bytes), &sm.ks_full[kb]);
+                }
+                ++fills;
+                if (++slot == nring) {
+                    slot = 0;
+                    ph ^= 1;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NBT; ++j) {
+                id0[j] = id1[j];
+                id1[j] = id2[j];
+            }
+            if (isK) {
+                __threadfence_block();
+                *reinterpret_cast<volatile int*>(&sm.k_tiles) = tcount + 1;
+            }
+            ++tcount;
             x = nx;
+        }
+        // every copy issued here lands before the CTA may exit
+        for (int s = 0; s < nring; ++s) {
+            const int n = fills / nring + (s < fills % nring ? 1 : 0);
+            if (n > 0) mbar_wait_drain(&sm.full_bar[base + s], static_cast<uint32_t>(n - 1) & 1u, p.err, 1024);
+        }
+        if (isK) {
+            for (int h = 0; h < 2; ++h) {
+                const int n = tcount / 2 + (h < tcount % 2 ? 1 : 0);
+                if (n > 0) mbar_wait_drain(&sm.ks_full[h], static_cast<uint32_t>(n - 1) & 1u, p.err, 1024);
+            }
+            for (int h = 0; h < 2; ++h) {
+                const int n = hcount / 2 + (h < hcount % 2 ? 1 : 0);
+                if (n > 0) mbar_wait_drain(&sm.hdr_full[h], static_cast<uint32_t>(n - 1) & 1u, p.err, 1024);
+            }
+        }
+        return;
+    }
+
+    if (warp == kMmaWarp || warp == kMma2Warp) {
+        // ============================ tensor-core issue ============================
+        // Warp kMmaWarp issues MM1 as soon as a K block lands (up to NSB tiles
+        // ahead of the consumers); warp kMma2Warp issues MM2 once a tile's P8
+        // and V blocks are in. Each commits its own MMAs.
+        constexpr uint32_t kIdescS = idesc_e4m3(128, NR, 0, 0);   // K-major K and Q
+        constexpr uint32_t kIdescO = idesc_e4m3(128, NR, 1, 1);   // MN-major V^T and P8^T
+        const bool mm1 = warp == kMmaWarp;
+        int slot = 0;
+        uint32_t ph = 0;
+        int hcount = 0, tcount = 0, hs = 0;
+        bool first = true;
+        for (Pos x = start; !pos_eq(x, end);) {
+            const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
+            const int rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
+            const int len = sm.slen[x.b];
+            const int valid = min(S2T, len - t * S2T);
+            const int nb = (valid + kBS - 1) / kBS;
+            if (mm1) {
+                if (first || t == 0) {
+                    hs = hcount & 1;
+                    mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
+                    // Q rows into the 128-byte-swizzled K-major layout (16-byte
+                    // chunk c of row r goes to position c ^ (r % 8)); rows past
+                    // the chunk's end become zeros
+                    if (lane < NR) {
+                        const int nrows = min(p.R - rc * NR, NR);
+                        uint4* row = reinterpret_cast<uint4*>(&sm.qb[hs][lane][0]);
+                        uint4 v[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) v[c] = lane < nrows ? row[c] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) row[c ^ (lane & 7)] = v[c];
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    ++hcount;
+                }
+                const int sb = tcount % NSB;
+                if (lane == 0) {
+                    // MM1: S^T[token][row] for each block of the tile
+                    mbar_wait(&sm.s_empty[sb], ((tcount / NSB) & 1) ^ 1, p.err, 64, &sm.abort);
+                    tc_fence_after();
+                    const uint64_t qd = smem_desc(smem_u32(&sm.qb[hs][0][0]), 16, 1024, kSmem128BSwizzle);
+                    for (int j = 0; j < nb; ++j) {
+                        uint32_t par;
+                        const int s = ring_slot<NK>(slot, ph, j, &par);
+                        mbar_wait(&sm.full_bar[s], par, p.err, 16, &sm.abort);
+                        tc_fence_after();
+                        const uint64_t kd = smem_desc(smem_u32(sm.ring[s]), 16, 1024, kSmem128BSwizzle);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)   // 32 bytes of head dim per MMA
+                            umma_e4m3(tmem + sb * SC + j * NR, kd + 2 * kk, qd + 2 * kk, kIdescS, kk);
+                        umma_commit(&sm.empty_bar[s]);
+                    }
+                    umma_commit(&sm.s_full[sb]);
+                    if (t == tiles_of<S2T>(len) - 1 || pos_eq(nx, end)) umma_commit(&sm.hdr_empty[hs]);
+                }
+                __syncwarp();
+                slot += nb;
+                if (slot >= NK) {
+                    slot -= NK;
+                    ph ^= 1;
+                }
+            } else {
+                if (lane == 0) {
+                    // MM2: O^T[chan][row] = V^T . P8^T over the tile's tokens
+                    mbar_wait(&sm.p_full, tcount & 1, p.err, 128, &sm.abort);
+                    tc_fence_after();
+                    const uint64_t pd = smem_desc(smem_u32(sm.pbuf), 8 * NR, 128, kSmemNoSwizzle);
+                    for (int j = 0; j < nb; ++j) {
+                        uint32_t par;
+                        const int s = NK + ring_slot<NV>(slot, ph, j, &par);
+                        mbar_wait(&sm.full_bar[s], par, p.err, 32, &sm.abort);
+                        tc_fence_after();
+                        const uint64_t vd = smem_desc(smem_u32(sm.ring[s]), 1024, 1024, kSmem128BSwizzle);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)   // 32 tokens per MMA
+                            umma_e4m3(tmem + OCOL, vd + 256 * kk,
+                                      pd + static_cast<uint64_t>(((j * kBS + 32 * kk) * NR) >> 4), kIdescO,
+                                      (j | kk) != 0);
+                        umma_commit(&sm.empty_bar[s]);
+                    }
+                    umma_commit(&sm.o_full);
+                }
+                __syncwarp();
+                slot += nb;
+                if (slot >= NV) {
+                    slot -= NV;
+                    ph ^= 1;
+                }
+            }
+            first = false;
+            ++tcount;
+            x = nx;
+        }
+        // all MMAs complete before the tensor memory is released
+        if (lane == 0) {
+            umma_commit(&sm.done_bar);
+            mbar_wait_drain(&sm.done_bar, 0, p.err, 1024);
+        }
+        __syncwarp();
+        named_bar_sync(2, (kNCW + 2) * 32);
+        if (mm1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, TCOLS);
         }
         return;
     }
 
     // ================================ consumers ================================
-    const int g = lane >> 2, tq = lane & 3;
+    // Warp w reads tensor-memory lanes 32 (w % 4) .. +31: tokens of its blocks
+    // (S^T) and channels (O^T). Warps 0-3 take the first half of the tile's
+    // blocks and O^T rows 0 .. NR/2-1, warps 4-7 the rest.
+    const int q4 = warp & 3, hh = warp >> 2;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    const int rho = NR == 16 ? (lane >> 1) : lane;   // query row whose reductions this lane holds
+    const bool rep = NR == 32 || (lane & 1) == 0;    // lane that publishes row rho
 
     // sequences of length 0 produce zero rows (no tile ever covers them)
     for (int b = cta; b < p.B; b += p.grid)
         if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
 
-    if constexpr (MT == 1) {
-        // ------------------------------------------------------------------
-        // One row tile (<= 16 query rows per kv head). Warps form 4 token
-        // groups x 2 channel halves: warp w runs MM1 on its own s2_tile/8
-        // tokens, keeps its P8 in registers in mma A-fragment order, swaps
-        // it with its partner warp (w ^ 1) through shared memory, and runs
-        // MM2 over the pair's tokens for 64 of the 128 channels. Per tile the
-        // only CTA-wide exchange is the row maximum. The accumulator holds
-        // O*448 / r, where r (per row) is the P-quantisation reference (max P
-        // of the last tile that contributed); a new tile rescales it by
-        // f = r * alpha / a (alpha = exp(M_old - M_new), a = max P of the
-        // tile). The four token groups' partial outputs are summed once per
-        // unit in shared memory.
-        // ------------------------------------------------------------------
-        constexpr int GT = 2 * TPW;           // tokens per group (pair of warps)
-        constexpr int KSG = GT / 32;          // MM2 k-steps per group: 4 / 2 / 1
-        constexpr int HU = TPW / 16;          // 16-token half k-steps per warp: 4 / 2 / 1
-        constexpr float kMinA = 5.421010862427522e-20f;  // 2^-64
-        const int tg = warp >> 1, dh = warp & 1;
-        uint32_t* xbuf = reinterpret_cast<uint32_t*>(&sm.obuf[0]);   // [warp][lane][2*HU]
-        int ks_st = 1, ks_off = 0;
-        int slot = 0;
-        uint32_t ph = 0;
-        int hcount = 0, tcount = 0, hs = 0;
-        bool first = true;
-        uint32_t qa[4][4];
-        float qsc[2], M[2], Lp[2], rsc[2];
-        float Oh[4][2][4];
-
-        for (Pos x = start; !pos_eq(x, end);) {
-            const int b = x.b, n2 = x.i / p.NRC, rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
-            const int len = sm.slen[b];
-            const int T = tiles_of<S2T>(len);
-
-            if (first || t == 0) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = rc * RCH + g + 8 * h;
-                    qsc[h] = r < p.R ? __ldg(p.q_scale + q_row(p, b, n2, r)) * p.sscale : 0.f;
-                }
-                if (p.ks_mode == KS_CONTIG) {
-                    ks_st = 1;
-                    ks_off = 0;
-                } else if (p.ks_mode == KS_QUAD) {
-                    ks_st = 4;
-                    ks_off = n2 & 3;
-                } else {
-                    ks_st = p.NKV;
-                    ks_off = n2;
-                }
-                hs = hcount & 1;
-                mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint8_t* r0 = &sm.q[hs][g][kk * 32 + 4 * tq];
-                    const uint8_t* r8 = &sm.q[hs][g + 8][kk * 32 + 4 * tq];
-                    qa[kk][0] = *reinterpret_cast<const uint32_t*>(r0);
-                    qa[kk][1] = *reinterpret_cast<const uint32_t*>(r8);
-                    qa[kk][2] = *reinterpret_cast<const uint32_t*>(r0 + 16);
-                    qa[kk][3] = *reinterpret_cast<const uint32_t*>(r8 + 16);
-                }
-                ++hcount;
-                first = false;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    M[h] = -INFINITY;
-                    Lp[h] = 0.f;
-                    rsc[h] = 1.f;
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) Oh[c][e][i] = 0.f;
-            }
-
-            // ------------------------------ one s2 tile ------------------------------
-            const int valid = min(S2T, len - t * S2T);
-            const int nb = (valid + kBS - 1) / kBS;
-            const int buf = tcount & 1;
-            const int wtok0 = warp * TPW;
-            const int wblk = wtok0 / kBS;
-            const int wrow0 = wtok0 - wblk * kBS;
-            const int gtok0 = tg * GT;
-            const int gblk = gtok0 / kBS;
-            const int grow0 = gtok0 - gblk * kBS;
-            const bool active = wtok0 < valid;
-            const bool gactive = gtok0 < valid;
-
-            float s[NT8][4];
-            float rmax[2] = {-INFINITY, -INFINITY};
-            if (active) {
-                int ks_slot = slot + wblk;
-                uint32_t ks_par = ph;
-                if (ks_slot >= NSLOT) {
-                    ks_slot -= NSLOT;
-                    ks_par ^= 1;
-                }
-                mbar_wait(&sm.full_bar[ks_slot], ks_par, p.err, 16, &sm.abort);
-                const uint32_t kbase = smem_u32(sm.ring[ks_slot]);
-                const float* ksm = sm.kscale[ks_slot];
-                const bool full = wtok0 + TPW <= valid;
-                // key scales first (their latency overlaps the MMAs)
-                float kv0[NT8], kv1[NT8];
-#pragma unroll
-                for (int j = 0; j < NT8; ++j) {
-                    const int trow = wrow0 + 8 * j + 2 * tq;
-                    kv0[j] = ksm[trow * ks_st + ks_off];
-                    kv1[j] = ksm[(trow + 1) * ks_st + ks_off];
-                }
-                // K fragments double-buffered one n8 tile ahead of the MMAs
-                uint32_t bb[2][8];
-                auto load_k = [&](int j, uint32_t (&dst)[8]) {
-                    const int row = wrow0 + 8 * j + (lane & 7);
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int chunk = hf * 4 + (lane >> 3);
-                        ldsm_x4(kbase + row * 128 + ((chunk ^ (row & 7)) << 4), dst[4 * hf], dst[4 * hf + 1],
-                                dst[4 * hf + 2], dst[4 * hf + 3]);
-                    }
-                };
-                load_k(0, bb[0]);
-#pragma unroll
-                for (int j = 0; j < NT8; ++j) {
-                    if (j + 1 < NT8) load_k(j + 1, bb[(j + 1) & 1]);
-                    float c4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma_e4m3(c4, qa[kk], bb[j & 1][2 * kk], bb[j & 1][2 * kk + 1]);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[j][e] = c4[e];
-                }
-#pragma unroll
-                for (int j = 0; j < NT8; ++j) {
-                    const float k0 = kv0[j];
-                    const float k1 = kv1[j];
-                    const int tk = wtok0 + 8 * j + 2 * tq;
-                    const bool v0 = full || tk < valid, v1 = full || tk + 1 < valid;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float x0 = v0 ? (s[j][2 * h] * qsc[h]) * k0 : -INFINITY;
-                        const float x1 = v1 ? (s[j][2 * h + 1] * qsc[h]) * k1 : -INFINITY;
-                        s[j][2 * h] = x0;
-                        s[j][2 * h + 1] = x1;
-                        rmax[h] = fmaxf(rmax[h], fmaxf(x0, x1));
-                    }
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float v = rmax[h];
-                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-                if (tq == 0) sm.red_max[buf][warp][g + 8 * h] = v;
-            }
-            __syncwarp();
-            if (lane == 0)
-                for (int j = 0; j < nb; ++j) {
-                    int sl = slot + j;
-                    if (sl >= NSLOT) sl -= NSLOT;
-                    mbar_arrive(&sm.empty_bar[sl]);
-                }
-            named_bar_sync(1, kNCW * 32);
-
-            // tile max -> running max, P quantisation scale, accumulator rescale
-            float Mn[2], alpha[2], qs[2], f[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int rr = g + 8 * h;
-                float m = sm.red_max[buf][0][rr];
-#pragma unroll
-                for (int w = 1; w < kNCW; ++w) m = fmaxf(m, sm.red_max[buf][w][rr]);
-                const float mn = fmaxf(M[h], m);
-                Mn[h] = mn;
-                alpha[h] = ex2(M[h] - mn);
-                const float a = ex2(m - mn);  // max_j P_j of this tile
-                const bool use = a >= kMinA;
-                qs[h] = use ? __fdividef(448.0f, a) : 0.f;
-                f[h] = use ? __fdividef(rsc[h] * alpha[h], a) : 1.f;
-                rsc[h] = use ? a : rsc[h] * alpha[h];
-                M[h] = mn;
-            }
-
-            // P, its sum, and this warp's P8 as 16-token half k-steps
-            // (own[u][0]: row g, own[u][1]: row g+8; tokens 16u .. 16u+15)
-            uint32_t own[HU][2];
-            if (active) {
-                float lsum[2] = {0.f, 0.f};
-#pragma unroll
-                for (int j = 0; j < NT8; ++j)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = e >> 1;
-                        const float pv = ex2(s[j][e] - Mn[h]);
-                        lsum[h] += pv;
-                        s[j][e] = pv * qs[h];
-                    }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) Lp[h] = Lp[h] * alpha[h] + lsum[h];
-#pragma unroll
-                for (int u = 0; u < HU; ++u) {
-                    own[u][0] = e4m3x4(s[2 * u][0], s[2 * u][1], s[2 * u + 1][0], s[2 * u + 1][1]);
-                    own[u][1] = e4m3x4(s[2 * u][2], s[2 * u][3], s[2 * u + 1][2], s[2 * u + 1][3]);
-                }
-            } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) Lp[h] = Lp[h] * alpha[h];
-#pragma unroll
-                for (int u = 0; u < HU; ++u) own[u][0] = own[u][1] = 0u;
-            }
-            // swap P8 with the partner warp of the token group
-            {
-                uint32_t* mine = xbuf + (warp * 32 + lane) * (2 * HU);
-#pragma unroll
-                for (int u = 0; u < HU; ++u)
-                    *reinterpret_cast<uint2*>(mine + 2 * u) = make_uint2(own[u][0], own[u][1]);
-            }
-            named_bar_sync(2 + tg, 64);
-            uint32_t par[HU][2];
-            {
-                const uint32_t* theirs = xbuf + (((warp ^ 1) * 32) + lane) * (2 * HU);
-#pragma unroll
-                for (int u = 0; u < HU; ++u) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(theirs + 2 * u);
-                    par[u][0] = v.x;
-                    par[u][1] = v.y;
-                }
-            }
-            // A fragments of the group's k-steps: half k-steps 0..HU-1 belong
-            // to warp 2tg, HU..2HU-1 to warp 2tg+1
-            uint32_t pa[KSG][4];
-#pragma unroll
-            for (int kk = 0; kk < KSG; ++kk)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int uu = 2 * kk + hh;
-                    const int owner = uu / HU, loc = uu - owner * HU;
-                    const bool mineu = owner == dh;
-                    pa[kk][2 * hh] = mineu ? own[loc][0] : par[loc][0];
-                    pa[kk][2 * hh + 1] = mineu ? own[loc][1] : par[loc][1];
-                }
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) Oh[c][e][i] *= f[i >> 1];
-
-            if (gactive) {
-                int vs_slot = slot + nb + gblk;
-                uint32_t vs_par = ph;
-                if (vs_slot >= NSLOT) {
-                    vs_slot -= NSLOT;
-                    vs_par ^= 1;
-                }
-                mbar_wait(&sm.full_bar[vs_slot], vs_par, p.err, 32, &sm.abort);
-                const uint32_t vbase = smem_u32(sm.ring[vs_slot]);
-#pragma unroll
-                for (int kk = 0; kk < KSG; ++kk) {
-                    const int tb = gtok0 + 32 * kk;
-                    if (tb >= valid) break;
-                    const int lim = valid - tb;
-                    const int row = grow0 + 32 * kk + lane;
-                    const int tk = 2 * tq;
-                    const uint32_t m0 = (tk < lim ? 0x0000FFFFu : 0u) | (tk + 1 < lim ? 0xFFFF0000u : 0u);
-                    const uint32_t m1 = (tk + 8 < lim ? 0x0000FFFFu : 0u) | (tk + 9 < lim ? 0xFFFF0000u : 0u);
-                    const uint32_t m2 = (tk + 16 < lim ? 0x0000FFFFu : 0u) | (tk + 17 < lim ? 0xFFFF0000u : 0u);
-                    const uint32_t m3 = (tk + 24 < lim ? 0x0000FFFFu : 0u) | (tk + 25 < lim ? 0xFFFF0000u : 0u);
-                    // all four channel chunks of this k-step in flight at once
-                    uint32_t rv[4][4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        ldsm_x4_t(vbase + row * 128 + (((4 * dh + c) ^ (row & 7)) << 4), rv[c][0], rv[c][1],
-                                  rv[c][2], rv[c][3]);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r0 = rv[c][0], r1 = rv[c][1], r2 = rv[c][2], r3 = rv[c][3];
-                        if (lim < 32) {  // zero V bytes of tokens past the sequence end
-                            r0 &= m0;
-                            r1 &= m1;
-                            r2 &= m2;
-                            r3 &= m3;
-                        }
-                        const uint32_t b0e0 = prmt(r0, r1, 0x6420), b1e0 = prmt(r2, r3, 0x6420);
-                        const uint32_t b0e1 = prmt(r0, r1, 0x7531), b1e1 = prmt(r2, r3, 0x7531);
-                        mma_e4m3(Oh[c][0], pa[kk], b0e0, b1e0);
-                        mma_e4m3(Oh[c][1], pa[kk], b0e1, b1e1);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0)
-                for (int j = 0; j < nb; ++j) {
-                    int sl = slot + nb + j;
-                    if (sl >= NSLOT) sl -= NSLOT;
-                    mbar_arrive(&sm.empty_bar[sl]);
-                }
-            slot += 2 * nb;
-            if (slot >= NSLOT) {
-                slot -= NSLOT;
-                ph ^= 1;
-            }
-            ++tcount;
-
-            const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
-            if (t == T - 1 || pos_eq(nx, end)) {
-                // ------------------------------ unit end ------------------------------
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float l = Lp[h];
-                    l += __shfl_xor_sync(0xffffffffu, l, 1);
-                    l += __shfl_xor_sync(0xffffffffu, l, 2);
-                    if (tq == 0) sm.red_l[warp][g + 8 * h] = l;
-                }
-                named_bar_sync(1, kNCW * 32);  // every warp is past its MM2 (xbuf free)
-                if (warp == 0 && tq == 0) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float l = 0.f;
-#pragma unroll
-                        for (int w = 0; w < kNCW; ++w) l += sm.red_l[w][g + 8 * h];
-                        sm.lrow[g + 8 * h] = l;
-                        sm.rrow[g + 8 * h] = rsc[h];
-                        sm.mrow[g + 8 * h] = M[h];
-                    }
-                }
-                const int64_t u = static_cast<int64_t>(b) * W + x.i;
-                const int64_t cost = sm.bpre[b + 1] - sm.bpre[b];
-                const int64_t pu = static_cast<int64_t>(sm.bpre[b]) * W + static_cast<int64_t>(x.i) * cost;
-                const int cf = cta_of(pu + kCU, Ctot, grid);
-                const int cl = cta_of(pu + kCU + static_cast<int64_t>(T - 1) * TC, Ctot, grid);
-                float* part = p.part + (u + cta) * kPartFloats;
-                // Sum of the 4 token groups, rows 0-7 then 8-15. Accumulator
-                // (c, e, i) of lane (g, tq) is channel 64dh + 16c + 4tq + e +
-                // 2(i & 1) of row g + 8(i >> 1); it is stored in fragment order.
-#pragma unroll
-                for (int ih = 0; ih < 2; ++ih) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e)
-#pragma unroll
-                            for (int il = 0; il < 2; ++il)
-                                sm.obuf[warp * 512 + ((c * 2 + e) * 2 + il) * 32 + lane] = Oh[c][e][2 * ih + il];
-                    named_bar_sync(1, kNCW * 32);
-                    const int orow = 8 * ih + (tid >> 5);
-                    const int d0 = (tid & 31) * 4;
-                    const float rr = sm.rrow[orow] * (1.0f / 448.0f);
-                    float ov[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int col = d0 + k;
-                        const int dhh = col >> 6, cc = (col >> 4) & 3, r16 = col & 15;
-                        const int src = ((cc * 2 + (r16 & 1)) * 2 + ((r16 >> 1) & 1)) * 32 + (orow & 7) * 4 + (r16 >> 2);
-                        float acc = 0.f;
-#pragma unroll
-                        for (int gq = 0; gq < 4; ++gq) acc += sm.obuf[(2 * gq + dhh) * 512 + src];
-                        ov[k] = acc * rr * sm.vsc[hs][col];
-                    }
-                    named_bar_sync(1, kNCW * 32);  // obuf free for the next round / unit
-                    const int r = rc * RCH + orow;
-                    if (cf == cl) {
-                        if (r < p.R) {
-                            const float L = sm.lrow[orow];
-                            uint2 o;
-                            o.x = pack_bf16x2(__fdiv_rn(ov[0], L), __fdiv_rn(ov[1], L));
-                            o.y = pack_bf16x2(__fdiv_rn(ov[2], L), __fdiv_rn(ov[3], L));
-                            *reinterpret_cast<uint2*>(p.out + q_row(p, b, n2, r) * kD + d0) = o;
-                        }
-                    } else {
-                        *reinterpret_cast<float4*>(part + orow * kD + d0) = make_float4(ov[0], ov[1], ov[2], ov[3]);
-                        if ((tid & 31) == 0) {
-                            part[32 * kD + orow] = sm.mrow[orow];
-                            part[32 * kD + 32 + orow] = sm.lrow[orow];
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.hdr_empty[hs]);
-                if (cf != cl) {
-                    __threadfence();
-                    named_bar_sync(1, kNCW * 32);
-                    if (tid == 0) {
-                        const int old = atomicAdd(p.counters + u, 1);
-                        const int last = (old == cl - cf);
-                        if (last) p.counters[u] = 0;
-                        sm.flag = last;
-                    }
-                    named_bar_sync(1, kNCW * 32);
-                    if (sm.flag) {
-                        __threadfence();
-                        const int n = cl - cf + 1;
-                        const int orow = tid >> 4, d0 = (tid & 15) * 8;
-                        const int r = rc * RCH + orow;
-                        if (r < p.R) {
-                            float mx = -INFINITY;
-                            for (int k = 0; k < n; ++k)
-                                mx = fmaxf(mx, __ldcg(p.part + (u + cf + k) * kPartFloats + 32 * kD + orow));
-                            float ls = 0.f;
-                            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            for (int k = 0; k < n; ++k) {
-                                const float* pp = p.part + (u + cf + k) * kPartFloats;
-                                const float sc = ex2(__ldcg(pp + 32 * kD + orow) - mx);
-                                ls += __ldcg(pp + 32 * kD + 32 + orow) * sc;
-                                const float4 o4a = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0));
-                                const float4 o4b = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0 + 4));
-                                acc[0] += o4a.x * sc;
-                                acc[1] += o4a.y * sc;
-                                acc[2] += o4a.z * sc;
-                                acc[3] += o4a.w * sc;
-                                acc[4] += o4b.x * sc;
-                                acc[5] += o4b.y * sc;
-                                acc[6] += o4b.z * sc;
-                                acc[7] += o4b.w * sc;
-                            }
-                            uint4 o;
-                            o.x = pack_bf16x2(__fdiv_rn(acc[0], ls), __fdiv_rn(acc[1], ls));
-                            o.y = pack_bf16x2(__fdiv_rn(acc[2], ls), __fdiv_rn(acc[3], ls));
-                            o.z = pack_bf16x2(__fdiv_rn(acc[4], ls), __fdiv_rn(acc[5], ls));
-                            o.w = pack_bf16x2(__fdiv_rn(acc[6], ls), __fdiv_rn(acc[7], ls));
-                            *reinterpret_cast<uint4*>(p.out + q_row(p, b, n2, r) * kD + d0) = o;
-                        }
-                    }
-                }
-            }
-            x = nx;
-        }
-        return;
-    }
-
-
-    // key scale of row r of this CTA's head inside a slot: kscale[r*ks_st + ks_off]
     int ks_st = 1, ks_off = 0;
-
-    int slot = 0;
-    uint32_t ph = 0;
-    int hcount = 0, tcount = 0;
+    int vslot = 0;
+    uint32_t vph = 0;
+    int hcount = 0, tcount = 0, hs = 0, nrows = 0;
     bool first = true;
-
-    uint32_t qa[MT][4][4];
-    float qsc[MT][2];
-    float4 vsc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float M[MT][2], Lp[MT][2], O[MT][2][4];
+    float Lp[NR];               // this thread's share of the row sums (running-max units)
+    float Oa[HR];               // O^T[32 q4 + lane][hh * HR + k], times 448
+    float Mref = -INFINITY;     // running max of row rho (scaled log2 units)
+#pragma unroll
+    for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
+#pragma unroll
+    for (int k = 0; k < HR; ++k) Oa[k] = 0.f;
 
     for (Pos x = start; !pos_eq(x, end);) {
+        const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
         const int b = x.b, n2 = x.i / p.NRC, rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
         const int len = sm.slen[b];
         const int T = tiles_of<S2T>(len);
 
         if (first || t == 0) {
-            // per-unit scales: loads issued here, first used after MM1 / MM2
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = rc * RCH + mt * 16 + g + 8 * h;
-                    qsc[mt][h] = r < p.R ? __ldg(p.q_scale + q_row(p, b, n2, r)) * p.sscale : 0.f;
-                }
-            vsc = __ldg(reinterpret_cast<const float4*>(p.v_scale +
-                                                        (static_cast<int64_t>(b) * p.NKV + n2) * kD +
-                                                        16 * warp + 4 * tq));
+            hs = hcount & 1;
+            mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
             if (p.ks_mode == KS_CONTIG) {
                 ks_st = 1;
                 ks_off = 0;
@@ -873,285 +737,180 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ks_st = p.NKV;
                 ks_off = n2;
             }
-            const int hs = hcount & 1;
-            mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
+            nrows = min(p.R - rc * NR, NR);
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
+            for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint8_t* r0 = &sm.q[hs][mt * 16 + g][kk * 32 + 4 * tq];
-                    const uint8_t* r8 = &sm.q[hs][mt * 16 + g + 8][kk * 32 + 4 * tq];
-                    qa[mt][kk][0] = *reinterpret_cast<const uint32_t*>(r0);
-                    qa[mt][kk][1] = *reinterpret_cast<const uint32_t*>(r8);
-                    qa[mt][kk][2] = *reinterpret_cast<const uint32_t*>(r0 + 16);
-                    qa[mt][kk][3] = *reinterpret_cast<const uint32_t*>(r8 + 16);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.hdr_empty[hs]);
+            for (int k = 0; k < HR; ++k) Oa[k] = 0.f;
+            Mref = -INFINITY;
             ++hcount;
             first = false;
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    M[mt][h] = -INFINITY;
-                    Lp[mt][h] = 0.f;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) O[mt][h][c] = 0.f;
-                }
         }
 
-        // --------------------------------- one s2 tile ---------------------------------
-        const int tok0 = t * S2T;
-        const int valid = min(S2T, len - tok0);
+        const int valid = min(S2T, len - t * S2T);
         const int nb = (valid + kBS - 1) / kBS;
-        const int buf = tcount & 1;
-        const int wtok0 = warp * TPW;
-        const int wblk = wtok0 / kBS;
-        const int wrow0 = wtok0 - wblk * kBS;
+        const int sb = tcount % NSB;
 
-        float s[MT][NT8][4];
-        float rmax[MT][2];
+        // ---- S^T of this warp's blocks and their key scales ----
+        mbar_wait(&sm.s_full[sb], (tcount / NSB) & 1, p.err, 256, &sm.abort);
+        tc_fence_after();
+        float sv[MBW][NR];
+        float ksv[MBW];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) rmax[mt][0] = rmax[mt][1] = -INFINITY;
-
-        if (wtok0 < valid) {
-            int ks_slot = slot + wblk;
-            uint32_t ks_par = ph;
-            if (ks_slot >= NSLOT) {
-                ks_slot -= NSLOT;
-                ks_par ^= 1;
-            }
-            mbar_wait(&sm.full_bar[ks_slot], ks_par, p.err, 16, &sm.abort);
-            const uint32_t kbase = smem_u32(sm.ring[ks_slot]);
-            const float* ksm = sm.kscale[ks_slot];
-            const bool full = wtok0 + TPW <= valid;
-#pragma unroll
-            for (int j = 0; j < NT8; ++j) {
-                uint32_t bb[8];
-                const int row = wrow0 + 8 * j + (lane & 7);
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int chunk = hf * 4 + (lane >> 3);
-                    ldsm_x4(kbase + row * 128 + ((chunk ^ (row & 7)) << 4), bb[4 * hf], bb[4 * hf + 1],
-                            bb[4 * hf + 2], bb[4 * hf + 3]);
-                }
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma_e4m3(c, qa[mt][kk], bb[2 * kk], bb[2 * kk + 1]);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[mt][j][e] = c[e];
-                }
-            }
-            // dequant (q_scale * softmax_scale * log2e, and k_scale), mask, row max
-#pragma unroll
-            for (int j = 0; j < NT8; ++j) {
-                const int trow = wrow0 + 8 * j + 2 * tq;
-                const float k0 = ksm[trow * ks_st + ks_off];
-                const float k1 = ksm[(trow + 1) * ks_st + ks_off];
-                const int tk = wtok0 + 8 * j + 2 * tq;
-                const bool v0 = full || tk < valid, v1 = full || tk + 1 < valid;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float x0 = v0 ? (s[mt][j][2 * h] * qsc[mt][h]) * k0 : -INFINITY;
-                        const float x1 = v1 ? (s[mt][j][2 * h + 1] * qsc[mt][h]) * k1 : -INFINITY;
-                        s[mt][j][2 * h] = x0;
-                        s[mt][j][2 * h + 1] = x1;
-                        rmax[mt][h] = fmaxf(rmax[mt][h], fmaxf(x0, x1));
-                    }
-            }
+        for (int jj = 0; jj < MBW; ++jj) {
+            const int mb = hh * MBW + jj;
+            ksv[jj] = 0.f;
+            if (mb < nb) tmem_ld_cols<NR>(tl + sb * SC + mb * NR, sv[jj]);
         }
+        const int kb = tcount & 1;
+        mbar_wait(&sm.ks_full[kb], (tcount >> 1) & 1, p.err, 16, &sm.abort);
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float v = rmax[mt][h];
-                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-                if (tq == 0) sm.red_max[0][warp][mt * 16 + g + 8 * h] = v;
-            }
+        for (int jj = 0; jj < MBW; ++jj) {
+            const int mb = hh * MBW + jj;
+            if (mb < nb) ksv[jj] = sm.ksb[kb][mb][(32 * q4 + lane) * ks_st + ks_off];
+        }
+        tmem_wait_ld();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0)
-            for (int j = 0; j < nb; ++j) {
-                int sl = slot + j;
-                if (sl >= NSLOT) sl -= NSLOT;
-                mbar_arrive(&sm.empty_bar[sl]);
-            }
-        named_bar_sync(1, kNCW * 32);
-
-        // tile row max -> running max, rescale factor, P quantisation scale
-        float Mn[MT][2], alpha[MT][2], qs[MT][2], ps[MT][2];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int rr = mt * 16 + g + 8 * h;
-                float m = sm.red_max[0][0][rr];
-#pragma unroll
-                for (int w = 1; w < kNCW; ++w) m = fmaxf(m, sm.red_max[0][w][rr]);
-                const float mn = fmaxf(M[mt][h], m);
-                Mn[mt][h] = mn;
-                alpha[mt][h] = ex2(M[mt][h] - mn);
-                const float a = ex2(m - mn);  // max_j P_j of this tile
-                qs[mt][h] = a > 0.f ? __fdividef(448.0f, a) : 0.f;
-                ps[mt][h] = a * (1.0f / 448.0f);
-            }
-
-        if (wtok0 < valid) {
-            float lsum[MT][2];
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) lsum[mt][0] = lsum[mt][1] = 0.f;
-#pragma unroll
-            for (int j = 0; j < NT8; ++j)
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = e >> 1;
-                        const float pv = ex2(s[mt][j][e] - Mn[mt][h]);
-                        lsum[mt][h] += pv;
-                        s[mt][j][e] = pv * qs[mt][h];
-                    }
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) Lp[mt][h] = Lp[mt][h] * alpha[mt][h] + lsum[mt][h];
-        } else {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) Lp[mt][h] = Lp[mt][h] * alpha[mt][h];
+        if (lane == 0) {
+            mbar_arrive(&sm.s_empty[sb]);
+            mbar_arrive(&sm.ks_empty[kb]);
         }
-        // P8 into shared memory in mma A-fragment order. Tokens 8j..8j+15 of the
-        // warp (n8 tiles j, j+1) fill half of one 32-token k-step.
+
+        // ---- scores x = S * q_scale * scale * log2(e) * k_scale; tile row maxima ----
+        float qsc[NR];
 #pragma unroll
-        for (int jp = 0; jp < NT8 / 2; ++jp) {
-            const int j = 2 * jp;
-            const int tb = wtok0 + 8 * j;
-            const int ksi = tb >> 5, half = (tb >> 4) & 1;
+        for (int r = 0; r < NR; ++r) qsc[r] = r < nrows ? sm.qs[hs][r] * p.sscale : 0.f;
+        float mloc[NR];
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                uint2 wv = make_uint2(0u, 0u);
-                if (wtok0 < valid) {
-                    wv.x = e4m3x4(s[mt][j][0], s[mt][j][1], s[mt][j + 1][0], s[mt][j + 1][1]);
-                    wv.y = e4m3x4(s[mt][j][2], s[mt][j][3], s[mt][j + 1][2], s[mt][j + 1][3]);
+        for (int r = 0; r < NR; ++r) mloc[r] = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < MBW; ++jj) {
+            const int mb = hh * MBW + jj;
+            if (mb < nb) {
+                const bool ok = mb * kBS + 32 * q4 + lane < valid;
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    const float xv = ok ? (sv[jj][r] * qsc[r]) * ksv[jj] : -INFINITY;
+                    sv[jj][r] = xv;
+                    mloc[r] = fmaxf(mloc[r], xv);
                 }
-                *reinterpret_cast<uint2*>(&sm.pfrag[buf][ksi][mt][lane][2 * half]) = wv;
             }
         }
+        const float wmax = lane_reduce<NR, true>(mloc, lane);
+        const int rb = tcount & 1;
+        if (rep) sm.red[rb][warp][rho] = wmax;
         named_bar_sync(1, kNCW * 32);
-
-        // MM2 over the tile's valid k-steps for this warp's 16 channels; two
-        // accumulator sets (even / odd k-step) halve the dependent mma chain.
-        float ot[MT][2][2][4];
+        float mt = sm.red[rb][0][rho];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int a2 = 0; a2 < 2; ++a2)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) ot[mt][e][a2][c] = 0.f;
+        for (int w = 1; w < kNCW; ++w) mt = fmaxf(mt, sm.red[rb][w][rho]);
         {
-            const int nks = (valid + 31) >> 5;
-#pragma unroll
-            for (int bi = 0; bi < NBT; ++bi) {
-                if (bi >= nb) break;
-                int vs_slot = slot + nb + bi;
-                uint32_t vs_par = ph;
-                if (vs_slot >= NSLOT) {
-                    vs_slot -= NSLOT;
-                    vs_par ^= 1;
-                }
-                mbar_wait(&sm.full_bar[vs_slot], vs_par, p.err, 32, &sm.abort);
-                const uint32_t vbase = smem_u32(sm.ring[vs_slot]);
-#pragma unroll
-                for (int kb = 0; kb < 4; ++kb) {
-                    const int ksi = bi * 4 + kb;
-                    if (ksi >= nks) break;
-                    const int row = (kb << 5) + lane;
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_t(vbase + row * 128 + ((warp ^ (row & 7)) << 4), r0, r1, r2, r3);
-                    const int lim = valid - (ksi << 5);
-                    if (lim < 32) {  // zero V bytes of tokens past the sequence end
-                        const int tk = 2 * tq;
-                        r0 &= (tk < lim ? 0x0000FFFFu : 0u) | (tk + 1 < lim ? 0xFFFF0000u : 0u);
-                        r1 &= (tk + 8 < lim ? 0x0000FFFFu : 0u) | (tk + 9 < lim ? 0xFFFF0000u : 0u);
-                        r2 &= (tk + 16 < lim ? 0x0000FFFFu : 0u) | (tk + 17 < lim ? 0xFFFF0000u : 0u);
-                        r3 &= (tk + 24 < lim ? 0x0000FFFFu : 0u) | (tk + 25 < lim ? 0xFFFF0000u : 0u);
-                    }
-                    const uint32_t b0e0 = prmt(r0, r1, 0x6420), b1e0 = prmt(r2, r3, 0x6420);
-                    const uint32_t b0e1 = prmt(r0, r1, 0x7531), b1e1 = prmt(r2, r3, 0x7531);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        const uint4 af = *reinterpret_cast<const uint4*>(&sm.pfrag[buf][ksi][mt][lane][0]);
-                        const uint32_t a[4] = {af.x, af.y, af.z, af.w};
-                        mma_e4m3(ot[mt][0][kb & 1], a, b0e0, b1e0);
-                        mma_e4m3(ot[mt][1][kb & 1], a, b0e1, b1e1);
-                    }
-                }
+            const float Mn = fmaxf(Mref, mt);
+            const float c1 = ex2(Mref - Mn), c2 = ex2(mt - Mn);
+            Mref = Mn;
+            if (rep) {
+                sm.wst[warp][0][rho] = mt;
+                sm.wst[warp][1][rho] = c1;
+                sm.wst[warp][2][rho] = c2;
             }
         }
         __syncwarp();
-        if (lane == 0)
-            for (int j = 0; j < nb; ++j) {
-                int sl = slot + nb + j;
-                if (sl >= NSLOT) sl -= NSLOT;
-                mbar_arrive(&sm.empty_bar[sl]);
-            }
-        // O = O * alpha + (O_t * P_scale) * v_scale. Channel of (e, c):
-        // 16*warp + 4*tq + e + 2*(c & 1).
+
+        // ---- P = 2^(x - tile max), row sums, P8 = E4M3(448 P) as the MM2 operand ----
+        float ls[NR];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+        for (int r = 0; r < NR; ++r) ls[r] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
+        for (int jj = 0; jj < MBW; ++jj) {
+            const int mb = hh * MBW + jj;
+            if (mb < nb) {
+                const int tok = mb * kBS + 32 * q4 + lane;
+                uint32_t pk[NR / 4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int h = c >> 1;
-                    const float vs = (c & 1) ? (e ? vsc.w : vsc.z) : (e ? vsc.y : vsc.x);
-                    const float o_t = ot[mt][e][0][c] + ot[mt][e][1][c];
-                    O[mt][e][c] = O[mt][e][c] * alpha[mt][h] + (o_t * ps[mt][h]) * vs;
+                for (int r4 = 0; r4 < NR / 4; ++r4) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(&sm.wst[warp][0][4 * r4]);
+                    const float e0 = ex2(sv[jj][4 * r4 + 0] - m4.x);
+                    const float e1 = ex2(sv[jj][4 * r4 + 1] - m4.y);
+                    const float e2 = ex2(sv[jj][4 * r4 + 2] - m4.z);
+                    const float e3 = ex2(sv[jj][4 * r4 + 3] - m4.w);
+                    ls[4 * r4 + 0] += e0;
+                    ls[4 * r4 + 1] += e1;
+                    ls[4 * r4 + 2] += e2;
+                    ls[4 * r4 + 3] += e3;
+                    pk[r4] = e4m3x4(448.f * e0, 448.f * e1, 448.f * e2, 448.f * e3);
                 }
+                uint8_t* dst = sm.pbuf + (tok >> 3) * (8 * NR) + (tok & 7) * 16;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            M[mt][0] = Mn[mt][0];
-            M[mt][1] = Mn[mt][1];
+                for (int a = 0; a < NR / 16; ++a)
+                    *reinterpret_cast<uint4*>(dst + a * 128) =
+                        make_uint4(pk[4 * a], pk[4 * a + 1], pk[4 * a + 2], pk[4 * a + 3]);
+            }
         }
-        slot += 2 * nb;
-        if (slot >= NSLOT) {
-            slot -= NSLOT;
-            ph ^= 1;
+        // V rows past the sequence end read as zeros (P is 0 there, and a stale
+        // NaN code times 0 would still be NaN)
+        {
+            const int tail = valid - (nb - 1) * kBS;
+            if (tail < kBS) {
+                uint32_t par;
+                const int s = NK + ring_slot<NV>(vslot, vph, nb - 1, &par);
+                mbar_wait(&sm.full_bar[s], par, p.err, 32, &sm.abort);
+                uint4* vr = reinterpret_cast<uint4*>(sm.ring[s]);
+                for (int k = tail * 8 + tid; k < kBS * 8; k += kNCW * 32) vr[k] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full);
+
+        // ---- running sums, then this tile's O^T folded into the accumulator ----
+        float c1v[NR], c2v[NR];
+#pragma unroll
+        for (int r4 = 0; r4 < NR / 4; ++r4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&sm.wst[warp][1][4 * r4]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&sm.wst[warp][2][4 * r4]);
+            c1v[4 * r4 + 0] = a4.x;
+            c1v[4 * r4 + 1] = a4.y;
+            c1v[4 * r4 + 2] = a4.z;
+            c1v[4 * r4 + 3] = a4.w;
+            c2v[4 * r4 + 0] = b4.x;
+            c2v[4 * r4 + 1] = b4.y;
+            c2v[4 * r4 + 2] = b4.z;
+            c2v[4 * r4 + 3] = b4.w;
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) Lp[r] = Lp[r] * c1v[r] + ls[r] * c2v[r];
+        mbar_wait(&sm.o_full, tcount & 1, p.err, 512, &sm.abort);
+        tc_fence_after();
+        {
+            float ot[HR];
+            tmem_ld_cols<HR>(tl + OCOL + hh * HR, ot);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < HR; ++k) Oa[k] = Oa[k] * c1v[hh * HR + k] + ot[k] * c2v[hh * HR + k];
+        }
+        vslot += nb;
+        if (vslot >= NV) {
+            vslot -= NV;
+            vph ^= 1;
         }
         ++tcount;
 
-        const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
         if (t == T - 1 || pos_eq(nx, end)) {
             // ------------------------------ unit end ------------------------------
+            float lsum[NR];
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float l = Lp[mt][h];
-                    l += __shfl_xor_sync(0xffffffffu, l, 1);
-                    l += __shfl_xor_sync(0xffffffffu, l, 2);
-                    if (tq == 0) sm.red_l[warp][mt * 16 + g + 8 * h] = l;
-                }
+            for (int r = 0; r < NR; ++r) lsum[r] = Lp[r];
+            const float wl = lane_reduce<NR, false>(lsum, lane);
+            if (rep) sm.redl[warp][rho] = wl;
             named_bar_sync(1, kNCW * 32);
-            float Lr[MT][2];
+            float L = 0.f;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float l = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kNCW; ++w) l += sm.red_l[w][mt * 16 + g + 8 * h];
-                    Lr[mt][h] = l;
-                }
+            for (int w = 0; w < kNCW; ++w) L += sm.redl[w][rho];
+            if (rep) sm.wst[warp][3][rho] = L;
+            __syncwarp();
+            const int ch = 32 * q4 + lane;
+            const float vs = sm.vsc[hs][ch] * (1.0f / 448.0f);
             const int64_t u = static_cast<int64_t>(b) * W + x.i;
             const int64_t cost = sm.bpre[b + 1] - sm.bpre[b];
             const int64_t pu = static_cast<int64_t>(sm.bpre[b]) * W + static_cast<int64_t>(x.i) * cost;
@@ -1159,32 +918,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int cl = cta_of(pu + kCU + static_cast<int64_t>(T - 1) * TC, Ctot, grid);
             if (cf == cl) {
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int r = rc * RCH + mt * 16 + g + 8 * h;
-                        if (r >= p.R) continue;
-                        const float L = Lr[mt][h];
-                        uint2 o;
-                        o.x = pack_bf16x2(__fdiv_rn(O[mt][0][2 * h], L), __fdiv_rn(O[mt][1][2 * h], L));
-                        o.y = pack_bf16x2(__fdiv_rn(O[mt][0][2 * h + 1], L), __fdiv_rn(O[mt][1][2 * h + 1], L));
-                        *reinterpret_cast<uint2*>(p.out + q_row(p, b, n2, r) * kD + 16 * warp + 4 * tq) = o;
-                    }
+                for (int k = 0; k < HR; ++k) {
+                    const int rr = hh * HR + k;
+                    if (rr < nrows)
+                        p.out[q_row(p, b, n2, rc * NR + rr) * kD + ch] =
+                            __float2bfloat16_rn(__fdiv_rn(Oa[k] * vs, sm.wst[warp][3][rr]));
+                }
             } else {
                 float* part = p.part + (u + cta) * kPartFloats;
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int rr = mt * 16 + g + 8 * h;
-                        *reinterpret_cast<float4*>(part + rr * kD + 16 * warp + 4 * tq) =
-                            make_float4(O[mt][0][2 * h], O[mt][1][2 * h], O[mt][0][2 * h + 1],
-                                        O[mt][1][2 * h + 1]);
-                        if (warp == 0 && tq == 0) {
-                            part[32 * kD + rr] = M[mt][h];
-                            part[32 * kD + 32 + rr] = Lr[mt][h];
-                        }
-                    }
+                for (int k = 0; k < HR; ++k) part[(hh * HR + k) * kD + ch] = Oa[k] * vs;
+                if (warp == 0 && rep) {
+                    part[32 * kD + rho] = Mref;
+                    part[32 * kD + 32 + rho] = L;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.hdr_empty[hs]);
+            if (cf != cl) {
                 __threadfence();
                 named_bar_sync(1, kNCW * 32);
                 if (tid == 0) {
@@ -1197,34 +948,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (sm.flag) {
                     __threadfence();
                     const int n = cl - cf + 1;
-                    for (int item = tid; item < RCH * 32; item += kNCW * 32) {
-                        const int rr = item >> 5, cg = item & 31, r = rc * RCH + rr;
-                        if (r >= p.R) continue;
+                    for (int item = tid; item < NR * 16; item += kNCW * 32) {
+                        const int orow = item >> 4, d0 = (item & 15) * 8;
+                        const int r = rc * NR + orow;
+                        if (orow >= nrows) continue;
                         float mx = -INFINITY;
                         for (int k = 0; k < n; ++k)
-                            mx = fmaxf(mx, __ldcg(p.part + (u + cf + k) * kPartFloats + 32 * kD + rr));
-                        float ls = 0.f;
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                            mx = fmaxf(mx, __ldcg(p.part + (u + cf + k) * kPartFloats + 32 * kD + orow));
+                        float lsm = 0.f;
+                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                         for (int k = 0; k < n; ++k) {
                             const float* pp = p.part + (u + cf + k) * kPartFloats;
-                            const float sc = ex2(__ldcg(pp + 32 * kD + rr) - mx);
-                            ls += __ldcg(pp + 32 * kD + 32 + rr) * sc;
-                            const float4 o4 = __ldcg(reinterpret_cast<const float4*>(pp + rr * kD + 4 * cg));
-                            acc.x += o4.x * sc;
-                            acc.y += o4.y * sc;
-                            acc.z += o4.z * sc;
-                            acc.w += o4.w * sc;
+                            const float sc = ex2(__ldcg(pp + 32 * kD + orow) - mx);
+                            lsm += __ldcg(pp + 32 * kD + 32 + orow) * sc;
+                            const float4 o4a = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0));
+                            const float4 o4b = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0 + 4));
+                            acc[0] += o4a.x * sc;
+                            acc[1] += o4a.y * sc;
+                            acc[2] += o4a.z * sc;
+                            acc[3] += o4a.w * sc;
+                            acc[4] += o4b.x * sc;
+                            acc[5] += o4b.y * sc;
+                            acc[6] += o4b.z * sc;
+                            acc[7] += o4b.w * sc;
                         }
-                        uint2 o;
-                        o.x = pack_bf16x2(__fdiv_rn(acc.x, ls), __fdiv_rn(acc.y, ls));
-                        o.y = pack_bf16x2(__fdiv_rn(acc.z, ls), __fdiv_rn(acc.w, ls));
-                        *reinterpret_cast<uint2*>(p.out + q_row(p, b, n2, r) * kD + 4 * cg) = o;
+                        uint4 o;
+                        o.x = pack_bf16x2(__fdiv_rn(acc[0], lsm), __fdiv_rn(acc[1], lsm));
+                        o.y = pack_bf16x2(__fdiv_rn(acc[2], lsm), __fdiv_rn(acc[3], lsm));
+                        o.z = pack_bf16x2(__fdiv_rn(acc[4], lsm), __fdiv_rn(acc[5], lsm));
+                        o.w = pack_bf16x2(__fdiv_rn(acc[6], lsm), __fdiv_rn(acc[7], lsm));
+                        *reinterpret_cast<uint4*>(p.out + q_row(p, b, n2, r) * kD + d0) = o;
                     }
                 }
             }
         }
         x = nx;
     }
+    tc_fence_before();
+    named_bar_sync(2, (kNCW + 2) * 32);
 }
 
 // ---------------------------------------------------------------------------
@@ -1281,7 +1042,7 @@ pa_status make_kscale_map(CUtensorMap* map, const float* base, int NKV, uint64_t
 }
 
 struct Plan {
-    int S2T, MT, RCH, NRC, R, G, grid;
+    int S2T, NR, NRC, R, G, grid;
     int64_t U;
     size_t counters_bytes, part_bytes, total;
 };
@@ -1302,9 +1063,8 @@ pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_confi
                "pa_fp8_decode: s2_tile %d (128, 256 and 512 are built)", pl->S2T);
     pl->G = NQ / NKV;
     pl->R = S1 * pl->G;
-    pl->MT = pl->R <= 16 ? 1 : 2;
-    pl->RCH = pl->MT * 16;
-    pl->NRC = (pl->R + pl->RCH - 1) / pl->RCH;
+    pl->NR = pl->R <= 16 ? 16 : 32;
+    pl->NRC = (pl->R + pl->NR - 1) / pl->NR;
     pl->U = static_cast<int64_t>(B) * NKV * pl->NRC;
     int grid = (cfg && cfg->num_ctas > 0) ? cfg->num_ctas : device_sm_count();
     PA_REQUIRE(grid > 0, PA_ERR_CUDA, "pa_fp8_decode: cannot query the device");
@@ -1315,42 +1075,40 @@ pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_confi
     return PA_OK;
 }
 
-template <int MT, int S2T>
+template <int NR, int S2T>
 pa_status launch(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tks,
                  const DecodeParams& prm, cudaStream_t st)
 {
-    const size_t smem = sizeof(DecodeSmem<MT, S2T>) + 1024;
+    const size_t smem = sizeof(DecodeSmem<NR, S2T>) + 1024;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&] {
-        attr = cudaFuncSetAttribute(decode_kernel<MT, S2T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr = cudaFuncSetAttribute(decode_kernel<NR, S2T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem));
     });
     PA_REQUIRE(attr == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode: smem attribute: %s", cudaGetErrorString(attr));
-    decode_kernel<MT, S2T><<<prm.grid, kThreads, smem, st>>>(tk, tv, tks, prm);
+    decode_kernel<NR, S2T><<<prm.grid, kThreads, smem, st>>>(tk, tv, tks, prm);
     return check_launch("pa_fp8_decode");
 }
 
 // Bulk-copy / TMA destinations must be 16-byte aligned (128 for the tensor
-// loads of key scales, 1024 for the 128-byte-swizzled K/V tiles).
-template <int MT, int S2T>
+// loads of key scales); the 128-byte-swizzled K/V tiles and the Q operand sit
+// on 1024-byte boundaries (the swizzle atom the MMA descriptors assume).
+template <int NR, int S2T>
 struct SmemLayoutChecks {
-    using S = DecodeSmem<MT, S2T>;
+    using S = DecodeSmem<NR, S2T>;
     static_assert(offsetof(S, ring) % 1024 == 0, "ring alignment");
-    static_assert(offsetof(S, kscale) % 128 == 0, "kscale alignment");
-    static_assert(offsetof(S, q) % 16 == 0, "q alignment");
+    static_assert(offsetof(S, qb) % 1024 == 0, "Q operand alignment");
+    static_assert(offsetof(S, pbuf) % 128 == 0, "P operand alignment");
+    static_assert(offsetof(S, ksb) % 128 == 0, "key-scale buffer alignment");
     static_assert(offsetof(S, vsc) % 16 == 0, "vsc alignment");
-    static_assert(offsetof(S, pfrag) % 16 == 0, "pfrag alignment");
-    static_assert(offsetof(S, obuf) % 16 == 0, "obuf alignment");
+    static_assert(offsetof(S, wst) % 16 == 0, "wst alignment");
     static_assert(sizeof(S) + 1024 <= 232448, "decode shared memory over budget");
     static constexpr bool ok = true;
 };
-static_assert(SmemLayoutChecks<1, 128>::ok && SmemLayoutChecks<1, 256>::ok && SmemLayoutChecks<1, 512>::ok &&
-                  SmemLayoutChecks<2, 128>::ok && SmemLayoutChecks<2, 256>::ok && SmemLayoutChecks<2, 512>::ok,
+static_assert(SmemLayoutChecks<16, 128>::ok && SmemLayoutChecks<16, 256>::ok && SmemLayoutChecks<16, 512>::ok &&
+                  SmemLayoutChecks<32, 128>::ok && SmemLayoutChecks<32, 256>::ok && SmemLayoutChecks<32, 512>::ok,
               "shared memory layout");
-static_assert(sizeof(DecodeSmem<2, 512>) + 1024 <= 232448, "decode shared memory over budget");
-static_assert(sizeof(DecodeSmem<1, 512>) + 1024 <= 232448, "decode shared memory over budget");
-static_assert(sizeof(DecodeSmem<2, 256>) + 1024 <= 232448, "decode shared memory over budget");
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -1451,14 +1209,14 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     prm.sscale = softmax_scale * 1.4426950408889634f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pl.MT == 1) {
-        if (pl.S2T == 128) return launch<1, 128>(tk, tv, tks, prm, s);
-        if (pl.S2T == 256) return launch<1, 256>(tk, tv, tks, prm, s);
-        return launch<1, 512>(tk, tv, tks, prm, s);
+    if (pl.NR == 16) {
+        if (pl.S2T == 128) return launch<16, 128>(tk, tv, tks, prm, s);
+        if (pl.S2T == 256) return launch<16, 256>(tk, tv, tks, prm, s);
+        return launch<16, 512>(tk, tv, tks, prm, s);
     }
-    if (pl.S2T == 128) return launch<2, 128>(tk, tv, tks, prm, s);
-    if (pl.S2T == 256) return launch<2, 256>(tk, tv, tks, prm, s);
-    return launch<2, 512>(tk, tv, tks, prm, s);
+    if (pl.S2T == 128) return launch<32, 128>(tk, tv, tks, prm, s);
+    if (pl.S2T == 256) return launch<32, 256>(tk, tv, tks, prm, s);
+    return launch<32, 512>(tk, tv, tks, prm, s);
 }
 
 // ---------------------------------------------------------------------------
