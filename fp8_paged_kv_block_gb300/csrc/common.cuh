@@ -105,13 +105,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t ns = 16;
     for (uint32_t it = 1;; ++it) {
-        // back off so that waiting warps leave issue slots to working ones
-        __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
+        // try_wait itself suspends the thread for a while; a short sleep only
+        // after many fruitless polls keeps long waits off the issue slots
+        // without delaying the wake-up of short ones
+        if (it > 64) __nanosleep(32);
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
+        if ((it & 63u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 *abort = 1;
