@@ -58,9 +58,8 @@ constexpr int kNCW = 8;                      // consumer warps
 constexpr int kKProducerWarp = kNCW;        // K blocks, key scales, per-unit header
 constexpr int kVProducerWarp = kNCW + 1;    // V blocks
 constexpr int kMmaWarp = kNCW + 2;          // tensor memory owner; issues MM1
-constexpr int kMma2Warp = kNCW + 3;         // issues MM2
-constexpr int kThreads = (kNCW + 4) * 32;
-constexpr int kKSlots = 4;                   // K ring; the V ring takes the other slots
+constexpr int kThreads = (kNCW + 3) * 32;
+constexpr int kKSlots = 5;                   // K ring; the V ring takes the other slots
 constexpr int kSlotBytes = kBS * kD;         // one 128-token block of one head
 constexpr int kKsFloats = 512;               // key-scale area per ring slot
 constexpr int kMaxB = 1024;
@@ -123,7 +122,6 @@ struct __align__(1024) DecodeSmemT {
     uint64_t ks_empty[2];
     uint64_t s_full[4];
     uint64_t s_empty[4];
-    uint64_t p_full;
     uint64_t o_full;
     uint64_t done_bar;
     uint32_t tmem;
@@ -335,7 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < NSLOT; ++i) {
             mbar_init(&sm.full_bar[i], 1);
-            mbar_init(&sm.empty_bar[i], 1);          // the MMAs reading the slot completed
+            // the MMAs reading the slot completed: K blocks are read by the MM1
+            // thread, V blocks by one MMA of each of the 4 consumer warps that
+            // hold the block's tokens
+            mbar_init(&sm.empty_bar[i], i < NK ? 1 : 4);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.hdr_full[i], 2);           // byte-counted copies + the q_scale cp.async
@@ -347,9 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.s_empty[i], kNCW);
         }
-        mbar_init(&sm.p_full, kNCW);
-        mbar_init(&sm.o_full, 1);
-        mbar_init(&sm.done_bar, 2);                  // one commit from each MMA-issuing warp
+        mbar_init(&sm.o_full, kNCW);                 // every consumer warp's MM2 share
+        mbar_init(&sm.done_bar, 1);
         sm.abort = 0;
         sm.k_tiles = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -582,14 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    if (warp == kMmaWarp || warp == kMma2Warp) {
-        // ============================ tensor-core issue ============================
-        // Warp kMmaWarp issues MM1 as soon as a K block lands (up to NSB tiles
-        // ahead of the consumers); warp kMma2Warp issues MM2 once a tile's P8
-        // and V blocks are in. Each commits its own MMAs.
+    if (warp == kMmaWarp) {
+        // ============================== MM1 issue ==============================
+        // One thread issues MM1 as soon as a K block lands (up to NSB tiles
+        // ahead of the consumers). MM2 is issued by the consumer warps.
         constexpr uint32_t kIdescS = idesc_e4m3(128, NR, 0, 0);   // K-major K and Q
-        constexpr uint32_t kIdescO = idesc_e4m3(128, NR, 1, 1);   // MN-major V^T and P8^T
-        const bool mm1 = warp == kMmaWarp;
+        constexpr bool mm1 = true;
         int slot = 0;
         uint32_t ph = 0;
         int hcount = 0, tcount = 0, hs = 0;
@@ -646,33 +644,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     slot -= NK;
                     ph ^= 1;
                 }
-            } else {
-                if (lane == 0) {
-                    // MM2: O^T[chan][row] = V^T . P8^T over the tile's tokens
-                    mbar_wait(&sm.p_full, tcount & 1, p.err, 128, &sm.abort);
-                    tc_fence_after();
-                    const uint64_t pd = smem_desc(smem_u32(sm.pbuf), 8 * NR, 128, kSmemNoSwizzle);
-                    for (int j = 0; j < nb; ++j) {
-                        uint32_t par;
-                        const int s = NK + ring_slot<NV>(slot, ph, j, &par);
-                        mbar_wait(&sm.full_bar[s], par, p.err, 32, &sm.abort);
-                        tc_fence_after();
-                        const uint64_t vd = smem_desc(smem_u32(sm.ring[s]), 1024, 1024, kSmem128BSwizzle);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)   // 32 tokens per MMA
-                            umma_e4m3(tmem + OCOL, vd + 256 * kk,
-                                      pd + static_cast<uint64_t>(((j * kBS + 32 * kk) * NR) >> 4), kIdescO,
-                                      (j | kk) != 0);
-                        umma_commit(&sm.empty_bar[s]);
-                    }
-                    umma_commit(&sm.o_full);
-                }
-                __syncwarp();
-                slot += nb;
-                if (slot >= NV) {
-                    slot -= NV;
-                    ph ^= 1;
-                }
             }
             first = false;
             ++tcount;
@@ -684,11 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_drain(&sm.done_bar, 0, p.err, 1024);
         }
         __syncwarp();
-        named_bar_sync(2, (kNCW + 2) * 32);
-        if (mm1) {
-            tc_fence_after();
-            tmem_dealloc(tmem, TCOLS);
-        }
+        named_bar_sync(2, (kNCW + 1) * 32);
+        tc_fence_after();
+        tmem_dealloc(tmem, TCOLS);
         return;
     }
 
@@ -717,6 +686,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
 #pragma unroll
     for (int k = 0; k < HR; ++k) Oa[k] = 0.f;
+    {
+        // O^T starts at zero: every MM2 MMA accumulates
+        const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < HR; c += 8) tmem_st8(tl + OCOL + hh * HR + c, zero8);
+        tmem_wait_st();
+        tc_fence_before();
+    }
 
     for (Pos x = start; !pos_eq(x, end);) {
         const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
@@ -846,22 +823,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(pk[4 * a], pk[4 * a + 1], pk[4 * a + 2], pk[4 * a + 3]);
             }
         }
-        // V rows past the sequence end read as zeros (P is 0 there, and a stale
-        // NaN code times 0 would still be NaN)
+        // ---- this warp's share of MM2: the k-step of its 32 tokens in each of
+        // its blocks, O^T[chan][row] += V^T[chan][tok] . P8^T[tok][row] (O^T
+        // was zeroed when the previous tile was folded). V rows of tokens
+        // past the sequence end are zeroed first: P is 0 there, and a stale
+        // NaN code times 0 would still be NaN. ----
         {
-            const int tail = valid - (nb - 1) * kBS;
-            if (tail < kBS) {
-                uint32_t par;
-                const int s = NK + ring_slot<NV>(vslot, vph, nb - 1, &par);
-                mbar_wait(&sm.full_bar[s], par, p.err, 32, &sm.abort);
-                uint4* vr = reinterpret_cast<uint4*>(sm.ring[s]);
-                for (int k = tail * 8 + tid; k < kBS * 8; k += kNCW * 32) vr[k] = make_uint4(0, 0, 0, 0);
+            constexpr uint32_t kIdescO = idesc_e4m3(128, NR, 1, 1);   // MN-major V^T and P8^T
+            int vsl[MBW];
+            uint32_t vpar[MBW];
+#pragma unroll
+            for (int jj = 0; jj < MBW; ++jj) {
+                const int mb = hh * MBW + jj;
+                vsl[jj] = NK + ring_slot<NV>(vslot, vph, mb, &vpar[jj]);
+                if (mb < nb && (mb + 1) * kBS > valid) {
+                    mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort);
+                    const int row = 32 * q4 + lane;
+                    if (mb * kBS + row >= valid) {
+                        uint4* vr = reinterpret_cast<uint4*>(sm.ring[vsl[jj]] + row * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const uint64_t pd = smem_desc(smem_u32(sm.pbuf), 8 * NR, 128, kSmemNoSwizzle);
+                bool any = false;
+#pragma unroll
+                for (int jj = 0; jj < MBW; ++jj) {
+                    const int mb = hh * MBW + jj;
+                    if (mb < nb) {
+                        mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort);
+                        tc_fence_after();
+                        const uint64_t vd = smem_desc(smem_u32(sm.ring[vsl[jj]]), 1024, 1024, kSmem128BSwizzle);
+                        umma_e4m3(tmem + OCOL, vd + 256 * q4,
+                                  pd + static_cast<uint64_t>(((mb * kBS + 32 * q4) * NR) >> 4), kIdescO, 1);
+                        umma_commit(&sm.empty_bar[vsl[jj]]);
+                        any = true;
+                    }
+                }
+                if (any)
+                    umma_commit(&sm.o_full);
+                else
+                    mbar_arrive(&sm.o_full);
+            }
+            __syncwarp();
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full);
 
         // ---- running sums, then this tile's O^T folded into the accumulator ----
         float c1v[NR], c2v[NR];
@@ -888,6 +897,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < HR; ++k) Oa[k] = Oa[k] * c1v[hh * HR + k] + ot[k] * c2v[hh * HR + k];
+            // zero this warp's part of O^T for the next tile's MMAs (which come
+            // after the next tile's row-maximum barrier)
+            const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < HR; c += 8) tmem_st8(tl + OCOL + hh * HR + c, zero8);
+            tmem_wait_st();
+            tc_fence_before();
         }
         vslot += nb;
         if (vslot >= NV) {
@@ -985,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         x = nx;
     }
     tc_fence_before();
-    named_bar_sync(2, (kNCW + 2) * 32);
+    named_bar_sync(2, (kNCW + 1) * 32);
 }
 
 // ---------------------------------------------------------------------------
