@@ -91,6 +91,10 @@ __host__ __device__ constexpr int s_buffers(int sc, int nr)
     return (4 * sc + nr <= 512) ? 4 : ((3 * sc + nr <= 512) ? 3 : 2);
 }
 
+struct Pos {
+    int b, i, t;
+};
+
 // NR: padded query rows per unit (16 or 32, the MMA N); S2T: s2 tile; NS:
 // ring slots (as many as fit): slots 0 .. kKSlots-1 hold K blocks, the rest
 // V blocks, each ring with its own producer.
@@ -125,6 +129,7 @@ struct __align__(1024) DecodeSmemT {
     uint64_t o_full;
     uint64_t done_bar;
     uint32_t tmem;
+    Pos range[2];               // this CTA's first tile and the tile after its last
     int k_tiles;                // tiles whose K blocks the K producer has requested
     int flag;
     int abort;
@@ -160,9 +165,6 @@ struct DecodeParams {
     float sscale;  // softmax_scale * log2(e)
 };
 
-struct Pos {
-    int b, i, t;
-};
 
 __device__ __forceinline__ bool pos_eq(const Pos& a, const Pos& b)
 {
@@ -415,10 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
         return;
     }
-    const Pos start = find_pos<S2T>(sm.slen, sm.bpre, p.B,
-                                    (static_cast<int64_t>(cta) * Ctot + grid - 1) / grid, Ctot, W);
-    const Pos end = find_pos<S2T>(sm.slen, sm.bpre, p.B,
-                                  (static_cast<int64_t>(cta + 1) * Ctot + grid - 1) / grid, Ctot, W);
+    // this CTA's range: two lanes of the K producer warp find its ends (the
+    // other warps get them through shared memory with the barrier below)
+    if (warp == kKProducerWarp && lane < 2)
+        sm.range[lane] = find_pos<S2T>(sm.slen, sm.bpre, p.B,
+                                       (static_cast<int64_t>(cta + lane) * Ctot + grid - 1) / grid, Ctot, W);
 
     // tensor memory: allocated by the MMA warp, address published in shared memory
     if (warp == kMmaWarp) tmem_alloc(&sm.tmem, TCOLS);
@@ -426,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem;
+    const Pos start = sm.range[0];
+    const Pos end = sm.range[1];
 
     if (warp == kKProducerWarp || warp == kVProducerWarp) {
         // ============================== producers ==============================
@@ -471,28 +476,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int b = x.b, n2 = x.i / p.NRC, rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
             const int len = sm.slen[b];
-            if (isK && (first || t == 0)) {
-                // the unit's Q rows (one bulk copy per run of consecutive rows),
-                // its q_scale values and its v_scale row
-                const int hs = hcount & 1;
-                mbar_wait(&sm.hdr_empty[hs], ((hcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort);
-                const int r0 = rc * NR, r1 = min(p.R, r0 + NR);
-                mbar_arrive_expect_tx(&sm.hdr_full[hs], static_cast<uint32_t>((r1 - r0) * kD + kD * 4));
-                bulk_load_1d(&sm.vsc[hs][0], p.v_scale + (static_cast<int64_t>(b) * p.NKV + n2) * kD,
-                             kD * 4, &sm.hdr_full[hs]);
-                for (int r = r0; r < r1;) {
-                    const int s = r / p.G, g0 = r - s * p.G;
-                    const int n = min(p.G - g0, r1 - r);
-                    const int64_t row = q_row(p, b, n2, r);
-                    bulk_load_1d(&sm.qb[hs][r - r0][0], p.q + row * kD, static_cast<uint32_t>(n * kD),
-                                 &sm.hdr_full[hs]);
-                    for (int k = 0; k < n; ++k) cp_async4(&sm.qs[hs][r - r0 + k], p.q_scale + row + k, 4);
-                    r += n;
-                }
-                cp_async_arrive_noinc(&sm.hdr_full[hs]);
-                ++hcount;
-            }
-            first = false;
             const int nb = min(NBT, (len - t * S2T + kBS - 1) / kBS);
             // V blocks of a tile are requested only after its K blocks: K is
             // needed first (MM1, softmax), V only once P is known
@@ -561,6 +544,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence_block();
                 *reinterpret_cast<volatile int*>(&sm.k_tiles) = tcount + 1;
             }
+            // the unit's header after its first K blocks (K is the long pole; MM1
+            // needs both)
+            if (isK && (first || t == 0)) {
+                // the unit's Q rows (one bulk copy per run of consecutive rows),
+                // its q_scale values and its v_scale row
+                const int hs = hcount & 1;
+                mbar_wait(&sm.hdr_empty[hs], ((hcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort);
+                const int r0 = rc * NR, r1 = min(p.R, r0 + NR);
+                mbar_arrive_expect_tx(&sm.hdr_full[hs], static_cast<uint32_t>((r1 - r0) * kD + kD * 4));
+                bulk_load_1d(&sm.vsc[hs][0], p.v_scale + (static_cast<int64_t>(b) * p.NKV + n2) * kD,
+                             kD * 4, &sm.hdr_full[hs]);
+                for (int r = r0; r < r1;) {
+                    const int s = r / p.G, g0 = r - s * p.G;
+                    const int n = min(p.G - g0, r1 - r);
+                    const int64_t row = q_row(p, b, n2, r);
+                    bulk_load_1d(&sm.qb[hs][r - r0][0], p.q + row * kD, static_cast<uint32_t>(n * kD),
+                                 &sm.hdr_full[hs]);
+                    for (int k = 0; k < n; ++k) cp_async4(&sm.qs[hs][r - r0 + k], p.q_scale + row + k, 4);
+                    r += n;
+                }
+                cp_async_arrive_noinc(&sm.hdr_full[hs]);
+                ++hcount;
+            }
+            first = false;
             ++tcount;
             x = nx;
         }
