@@ -107,7 +107,8 @@ struct __align__(1024) DecodeSmemT {
     alignas(1024) uint8_t qb[2][NR][kD];
     // P8^T, MN-major without swizzle: token t, row r at
     // (t / 8) * 8 * NR + (r / 16) * 128 + (t % 8) * 16 + r % 16
-    alignas(1024) uint8_t pbuf[S2T * NR];
+    // (also the BF16 staging of a unit's output rows, NR x 128 x 2 bytes)
+    alignas(1024) uint8_t pbuf[S2T * NR > NR * kD * 2 ? S2T * NR : NR * kD * 2];
     // key scales of one tile's blocks, double-buffered by tile parity
     alignas(128) float ksb[2][S2T / kBS][kKsFloats];
     alignas(16) float vsc[2][kD];
@@ -130,6 +131,8 @@ struct __align__(1024) DecodeSmemT {
     uint64_t done_bar;
     uint32_t tmem;
     Pos range[2];               // this CTA's first tile and the tile after its last
+    int owner[2];               // first CTA of the range's first unit, last CTA of its last unit
+    alignas(16) int64_t orow[2][32];   // output row of each query row of the unit (by unit parity)
     int k_tiles;                // tiles whose K blocks the K producer has requested
     int flag;
     int abort;
@@ -419,9 +422,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // this CTA's range: two lanes of the K producer warp find its ends (the
     // other warps get them through shared memory with the barrier below)
-    if (warp == kKProducerWarp && lane < 2)
-        sm.range[lane] = find_pos<S2T>(sm.slen, sm.bpre, p.B,
-                                       (static_cast<int64_t>(cta + lane) * Ctot + grid - 1) / grid, Ctot, W);
+    if (warp == kKProducerWarp && lane < 2) {
+        const Pos x = find_pos<S2T>(sm.slen, sm.bpre, p.B,
+                                    (static_cast<int64_t>(cta + lane) * Ctot + grid - 1) / grid, Ctot, W);
+        sm.range[lane] = x;
+        // Only the range's first and last units can be shared with other CTAs:
+        // the CTA holding the first unit's first tile, and the one holding the
+        // last unit's last tile (for the split combine).
+        int own = cta;
+        if (x.b < p.B && x.t > 0) {
+            const int64_t cost = sm.bpre[x.b + 1] - sm.bpre[x.b];
+            const int64_t pu = static_cast<int64_t>(sm.bpre[x.b]) * W + static_cast<int64_t>(x.i) * cost;
+            own = lane == 0 ? cta_of(pu + kCU, Ctot, grid)
+                            : cta_of(pu + kCU + static_cast<int64_t>(tiles_of<S2T>(sm.slen[x.b]) - 1) * TC, Ctot,
+                                     grid);
+        }
+        sm.owner[lane] = own;
+    }
 
     // tensor memory: allocated by the MMA warp, address published in shared memory
     if (warp == kMmaWarp) tmem_alloc(&sm.tmem, TCOLS);
@@ -722,6 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ks_off = n2;
             }
             nrows = min(p.R - rc * NR, NR);
+            if (warp == 0 && lane < NR) sm.orow[hcount & 1][lane] = q_row(p, b, n2, rc * NR + lane);
 #pragma unroll
             for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
 #pragma unroll
@@ -935,18 +953,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ch = 32 * q4 + lane;
             const float vs = sm.vsc[hs][ch] * (1.0f / 448.0f);
             const int64_t u = static_cast<int64_t>(b) * W + x.i;
-            const int64_t cost = sm.bpre[b + 1] - sm.bpre[b];
-            const int64_t pu = static_cast<int64_t>(sm.bpre[b]) * W + static_cast<int64_t>(x.i) * cost;
-            const int cf = cta_of(pu + kCU, Ctot, grid);
-            const int cl = cta_of(pu + kCU + static_cast<int64_t>(T - 1) * TC, Ctot, grid);
+            const bool first_unit = b == start.b && x.i == start.i;
+            const bool last_unit = b == end.b && x.i == end.i;
+            const int cf = first_unit ? sm.owner[0] : cta;
+            const int cl = last_unit ? sm.owner[1] : cta;
             if (cf == cl) {
+                // BF16 rows staged in shared memory, then written 16 bytes per thread
+                __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm.pbuf);
 #pragma unroll
                 for (int k = 0; k < HR; ++k) {
                     const int rr = hh * HR + k;
-                    if (rr < nrows)
-                        p.out[q_row(p, b, n2, rc * NR + rr) * kD + ch] =
-                            __float2bfloat16_rn(__fdiv_rn(Oa[k] * vs, sm.wst[warp][3][rr]));
+                    stage[rr * kD + ch] = __float2bfloat16_rn(Oa[k] * vs * (1.0f / sm.wst[warp][3][rr]));
                 }
+                named_bar_sync(1, kNCW * 32);
+                const int64_t* orow = sm.orow[(hcount - 1) & 1];
+#pragma unroll
+                for (int it = 0; it < NR * 16 / (kNCW * 32); ++it) {
+                    const int item = it * kNCW * 32 + tid;
+                    const int rr = item >> 4, c8 = (item & 15) * 8;
+                    if (rr < nrows)
+                        *reinterpret_cast<uint4*>(p.out + orow[rr] * kD + c8) =
+                            *reinterpret_cast<const uint4*>(stage + rr * kD + c8);
+                }
+                named_bar_sync(1, kNCW * 32);   // staging free before the next tile's P8
             } else {
                 float* part = p.part + (u + cta) * kPartFloats;
 #pragma unroll
