@@ -47,7 +47,7 @@ class PaError(RuntimeError):
 
 class pa_decode_config(ctypes.Structure):
     _fields_ = [("s2_tile", ctypes.c_int), ("num_ctas", ctypes.c_int),
-                ("reserved", ctypes.c_int * 6)]
+                ("overlap_prologue", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
 
 
 def build(force: bool = False) -> str:
@@ -143,10 +143,11 @@ def _in_dtype(t):
 # Decode attention
 # --------------------------------------------------------------------------
 
-def _config(s2_tile: int, num_ctas: int):
+def _config(s2_tile: int, num_ctas: int, overlap_prologue: bool = False):
     c = pa_decode_config()
     c.s2_tile = s2_tile
     c.num_ctas = num_ctas
+    c.overlap_prologue = 1 if overlap_prologue else 0
     return c
 
 
@@ -175,7 +176,8 @@ class DecodeWorkspace:
 
 def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs, out, *,
            S1: int = 1, layout: int = LAYOUT_BSND, s2_tile: int = 512, softmax_scale=None,
-           workspace: DecodeWorkspace | None = None, num_ctas: int = 0, stream=None):
+           workspace: DecodeWorkspace | None = None, num_ctas: int = 0, stream=None,
+           overlap_prologue: bool = False):
     """Paged FP8 decode attention (in place into ``out``).
 
     q [B*S1, NQ, D] E4M3 (uint8 or float8_e4m3fn), q_scale float32 [B*S1, NQ],
@@ -183,6 +185,9 @@ def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_s
     [NB, NKV, BS, D] for BNBD), k_scale float32 (cache shape without D),
     v_scale float32 [B, NKV, D], block_table int32 [B, max_blocks],
     kv_act_seqs int32 [B], out bfloat16 [B*S1, NQ, D].
+    overlap_prologue: let the kernel's prologue overlap the preceding kernel
+    in the stream (that kernel must not write kv_act_seqs, block_table, q,
+    q_scale or v_scale); see pa_decode_config.overlap_prologue.
     """
     torch = _torch()
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
@@ -204,7 +209,7 @@ def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_s
     if workspace is None:
         workspace = DecodeWorkspace(B, S1, NQ, NKV, D, s2_tile=s2_tile, num_ctas=num_ctas,
                                     device=q.device)
-    cfg = _config(s2_tile, num_ctas)
+    cfg = _config(s2_tile, num_ctas, overlap_prologue)
     st = lib().pa_fp8_decode(_ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
                              _ptr(v_scale), _ptr(block_table), _ptr(kv_act_seqs), _ptr(out),
                              B, S1, NQ, NKV, D, BS, NB, block_table.shape[1], layout,

@@ -242,6 +242,19 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v)
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ---- programmatic dependent launch ----------------------------------------------
+// Lets the next kernel in the stream be scheduled before this one ends.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Blocks until the preceding kernel of the stream has completed and its
+// memory is visible (returns at once when the launch had no such dependency).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- async copies -------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes)
 {

@@ -165,6 +165,7 @@ struct DecodeParams {
     int* err;
     int64_t num_blocks;
     int B, S1, NQ, NKV, G, R, NRC, max_blocks, layout, grid, maxlen, ks_mode;
+    int overlap;   // launched with programmatic stream serialisation
     float sscale;  // softmax_scale * log2(e)
 };
 
@@ -334,6 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int W = p.NKV * p.NRC;
+    // The next kernel of the stream may be scheduled now (it waits for this
+    // one before touching anything this one writes).
+    grid_launch_dependents();
 
     if (tid == 0) {
         for (int i = 0; i < NSLOT; ++i) {
@@ -415,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (cta >= grid) {
         // no tiles for this CTA; it may still owe zero rows for empty sequences
+        grid_dependency_wait();
         if (warp < kNCW)
             for (int b = cta; b < p.B; b += p.grid)
                 if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
@@ -479,6 +484,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 #pragma unroll
         for (int j = 0; j < NBT; ++j) id0[j] = id1[j] = id2[j] = 0;
+        // the unit's Q rows (one bulk copy per run of consecutive rows), its
+        // q_scale values and its v_scale row
+        auto issue_header = [&](int b, int n2, int rc) {
+            const int hs = hcount & 1;
+            mbar_wait(&sm.hdr_empty[hs], ((hcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort);
+            const int r0 = rc * NR, r1 = min(p.R, r0 + NR);
+            mbar_arrive_expect_tx(&sm.hdr_full[hs], static_cast<uint32_t>((r1 - r0) * kD + kD * 4));
+            bulk_load_1d(&sm.vsc[hs][0], p.v_scale + (static_cast<int64_t>(b) * p.NKV + n2) * kD,
+                         kD * 4, &sm.hdr_full[hs]);
+            for (int r = r0; r < r1;) {
+                const int s = r / p.G, g0 = r - s * p.G;
+                const int n = min(p.G - g0, r1 - r);
+                const int64_t row = q_row(p, b, n2, r);
+                bulk_load_1d(&sm.qb[hs][r - r0][0], p.q + row * kD, static_cast<uint32_t>(n * kD),
+                             &sm.hdr_full[hs]);
+                for (int k = 0; k < n; ++k) cp_async4(&sm.qs[hs][r - r0 + k], p.q_scale + row + k, 4);
+                r += n;
+            }
+            cp_async_arrive_noinc(&sm.hdr_full[hs]);
+            ++hcount;
+        };
+        bool waited = false;
         Pos x1 = start;
         load_ids(start, id0);
         if (!pos_eq(start, end)) {
@@ -493,6 +520,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int b = x.b, n2 = x.i / p.NRC, rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
             const int len = sm.slen[b];
+            const bool need_hdr = isK && (first || t == 0);
+            bool hdr_done = false;
+            if (!waited) {
+                // inputs not written by the preceding kernel may be read before
+                // it ends; the KV cache and its scales only after
+                if (need_hdr && p.overlap) {
+                    issue_header(b, n2, rc);
+                    hdr_done = true;
+                }
+                grid_dependency_wait();
+                waited = true;
+            }
             const int nb = min(NBT, (len - t * S2T + kBS - 1) / kBS);
             // V blocks of a tile are requested only after its K blocks: K is
             // needed first (MM1, softmax), V only once P is known
@@ -562,28 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<volatile int*>(&sm.k_tiles) = tcount + 1;
             }
             // the unit's header after its first K blocks (K is the long pole; MM1
-            // needs both)
-            if (isK && (first || t == 0)) {
-                // the unit's Q rows (one bulk copy per run of consecutive rows),
-                // its q_scale values and its v_scale row
-                const int hs = hcount & 1;
-                mbar_wait(&sm.hdr_empty[hs], ((hcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort);
-                const int r0 = rc * NR, r1 = min(p.R, r0 + NR);
-                mbar_arrive_expect_tx(&sm.hdr_full[hs], static_cast<uint32_t>((r1 - r0) * kD + kD * 4));
-                bulk_load_1d(&sm.vsc[hs][0], p.v_scale + (static_cast<int64_t>(b) * p.NKV + n2) * kD,
-                             kD * 4, &sm.hdr_full[hs]);
-                for (int r = r0; r < r1;) {
-                    const int s = r / p.G, g0 = r - s * p.G;
-                    const int n = min(p.G - g0, r1 - r);
-                    const int64_t row = q_row(p, b, n2, r);
-                    bulk_load_1d(&sm.qb[hs][r - r0][0], p.q + row * kD, static_cast<uint32_t>(n * kD),
-                                 &sm.hdr_full[hs]);
-                    for (int k = 0; k < n; ++k) cp_async4(&sm.qs[hs][r - r0 + k], p.q_scale + row + k, 4);
-                    r += n;
-                }
-                cp_async_arrive_noinc(&sm.hdr_full[hs]);
-                ++hcount;
-            }
+            // needs both), unless it went out before the dependency wait
+            if (need_hdr && !hdr_done) issue_header(b, n2, rc);
             first = false;
             ++tcount;
             x = nx;
@@ -694,6 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rho = NR == 16 ? (lane >> 1) : lane;   // query row whose reductions this lane holds
     const bool rep = NR == 32 || (lane & 1) == 0;    // lane that publishes row rho
 
+    // out and the workspace are written only after the preceding kernel ended
+    grid_dependency_wait();
     // sequences of length 0 produce zero rows (no tile ever covers them)
     for (int b = cta; b < p.B; b += p.grid)
         if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
@@ -1139,6 +1160,21 @@ pa_status launch(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap
                                     static_cast<int>(smem));
     });
     PA_REQUIRE(attr == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode: smem attribute: %s", cudaGetErrorString(attr));
+    if (prm.overlap) {
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(static_cast<unsigned>(prm.grid));
+        lc.blockDim = dim3(kThreads);
+        lc.dynamicSmemBytes = smem;
+        lc.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&lc, decode_kernel<NR, S2T>, tk, tv, tks, prm);
+        PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode: launch: %s", cudaGetErrorString(e));
+        return PA_OK;
+    }
     decode_kernel<NR, S2T><<<prm.grid, kThreads, smem, st>>>(tk, tv, tks, prm);
     return check_launch("pa_fp8_decode");
 }
@@ -1259,6 +1295,7 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     prm.maxlen = static_cast<int>(maxlen);
     prm.ks_mode = ks_mode;
     prm.sscale = softmax_scale * 1.4426950408889634f;
+    prm.overlap = (cfg && cfg->overlap_prologue) ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pl.NR == 16) {

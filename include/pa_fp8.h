@@ -89,7 +89,17 @@ typedef struct pa_decode_config {
                       128, 256 or 512 are built. Default 512.                 */
     int num_ctas;  /* persistent grid size. Default: SM count x resident
                       CTAs per SM.                                            */
-    int reserved[6];
+    int overlap_prologue; /* 1: launch with programmatic stream serialisation
+                      so that the kernel's prologue (schedule, block ids, Q
+                      rows and scales) overlaps the tail of the preceding
+                      kernel in the stream. The kernel then reads
+                      kv_act_seqs, block_table, q, q_scale and v_scale
+                      before that kernel has finished -- the caller
+                      guarantees the preceding kernel does not write them --
+                      and waits for it before touching k_cache, v_cache,
+                      k_scale, out and the workspace. 0 (default): ordinary
+                      stream order.                                           */
+    int reserved[5];
 } pa_decode_config;
 
 /* Text of a status code (static storage). */
