@@ -43,9 +43,12 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic of one decode launch on this workload, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources it was taken with.
-# The decode's inputs other than the KV cache (lengths, block table, q and
-# its scales, v_scale) are never written by the append kernel before it, so
-# its prologue may overlap the append (pa_decode_config.overlap_prologue).
+# Programmatic stream serialisation between the step's kernels: the decode's
+# inputs other than the KV cache (lengths, block table, q and its scales,
+# v_scale) are never written by the append kernel before it, and the append's
+# inputs (new K/V rows, slots, batches, v_scale) are never written by the
+# previous step's decode, so each kernel's prologue may overlap the kernel
+# before it (overlap_prologue); cache reads and writes wait for it.
 OVERLAP = True
 
 DECODE_TRAFFIC = {"sources_sha1": "c5a0d936e57cbcb856df9fdd6162182e9d29e932",
@@ -300,7 +303,7 @@ def main():
 
     def append(c):
         pa.cache_quant_scatter(kn_d, vn_d, c.k_cache, c.v_cache, slot_d, c.k_scale, c.v_scale,
-                               tb_d, layout=case.layout)
+                               tb_d, layout=case.layout, overlap_prologue=OVERLAP)
 
     def attend(c):
         pa.decode(q8, qs, c.k_cache, c.k_scale, c.v_cache, c.v_scale, bt, act_d, out,
@@ -377,26 +380,29 @@ def main():
         torch.cuda.synchronize()
 
     # ---- end to end through the public API with host buffers ----
-    h_q8 = torch.empty_like(q8, device="cpu").pin_memory()
-    h_q8.copy_(q8)
-    h_qs = qs.cpu().pin_memory()
-    h_kn = knew.pin_memory()
-    h_vn = vnew.pin_memory()
-    h_slot = torch.from_numpy(slot).pin_memory()
-    h_act = torch.from_numpy(act_after).pin_memory()
-    h_bt = torch.from_numpy(case.block_table).pin_memory()
+    # The step's inputs travel in one pinned host buffer (one host-to-device
+    # copy per step); the output comes back with one device-to-host copy.
+    host_parts = [q8.cpu(), qs.cpu(), knew, vnew, torch.from_numpy(slot), torch.from_numpy(act_after),
+                  torch.from_numpy(case.block_table)]
+    offs, total = [], 0
+    for t in host_parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for t, o in zip(host_parts, offs):
+        n = t.numel() * t.element_size()
+        h_pack[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+    d_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+    d_q8, d_qs, d_kn, d_vn, d_slot, d_act, d_bt = [
+        d_pack[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        for t, o in zip(host_parts, offs)]
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d_q8, d_qs = torch.empty_like(q8), torch.empty_like(qs)
-    d_kn, d_vn = torch.empty_like(kn_d), torch.empty_like(vn_d)
-    d_slot, d_act, d_bt = torch.empty_like(slot_d), torch.empty_like(act_d), torch.empty_like(bt)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q8, h_qs, h_kn, h_vn, h_slot, h_act, h_bt))
+    h2d = total
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step(i):
         c = caches[i % copies]
-        for d, h in ((d_q8, h_q8), (d_qs, h_qs), (d_kn, h_kn), (d_vn, h_vn), (d_slot, h_slot),
-                     (d_act, h_act), (d_bt, h_bt)):
-            d.copy_(h, non_blocking=True)
+        d_pack.copy_(h_pack, non_blocking=True)
         pa.cache_quant_scatter(d_kn, d_vn, c.k_cache, c.v_cache, d_slot, c.k_scale, c.v_scale,
                                tb_d, layout=case.layout)
         pa.decode(d_q8, d_qs, c.k_cache, c.k_scale, c.v_cache, c.v_scale, d_bt, d_act, out,
@@ -456,8 +462,10 @@ def main():
                       % (copies, copies * cache_bytes / 1e6, l2 / 1e6),
                 "timing": "CUDA graphs replayed on one stream, CUDA events over the K steps",
                 "parallelism": "replicas" if world > 1 else "single GPU",
-                "decode_launch": ("programmatic dependent launch: the decode's prologue overlaps "
-                                  "the preceding kernel" if OVERLAP else "stream order"),
+                "launch": ("programmatic dependent launch: the append's loads and encoding "
+                           "overlap the previous decode, the decode's prologue overlaps the "
+                           "append; cache writes/reads wait for the preceding kernel"
+                           if OVERLAP else "stream order"),
             },
             "gpu_launches": 2 * args.steps,
             "roofline": {"bound": "hbm", "kernel": "pa_fp8_decode", "achieved": achieved,

@@ -58,6 +58,8 @@ def build(force: bool = False) -> str:
 def lib():
     """The loaded ctypes library (raises if it has not been built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -81,7 +83,7 @@ def lib():
                                            i64, i32, i32, P]
         L.pa_fp8_cache_scatter.restype = i32
         L.pa_fp8_cache_quant_scatter.argtypes = [P, P, i32, P, P, P, i32, P, P, P, i32, i64, i32,
-                                                 i32, i64, i32, i32, P]
+                                                 i32, i64, i32, i32, i32, P]
         L.pa_fp8_cache_quant_scatter.restype = i32
         L.pa_fp8_quantize_rows.argtypes = [P, i32, i64, i32, P, P, P]
         L.pa_fp8_quantize_rows.restype = i32
@@ -143,11 +145,18 @@ def _in_dtype(t):
 # Decode attention
 # --------------------------------------------------------------------------
 
+_configs = {}
+
+
 def _config(s2_tile: int, num_ctas: int, overlap_prologue: bool = False):
-    c = pa_decode_config()
-    c.s2_tile = s2_tile
-    c.num_ctas = num_ctas
-    c.overlap_prologue = 1 if overlap_prologue else 0
+    key = (s2_tile, num_ctas, bool(overlap_prologue))
+    c = _configs.get(key)
+    if c is None:
+        c = pa_decode_config()
+        c.s2_tile = s2_tile
+        c.num_ctas = num_ctas
+        c.overlap_prologue = 1 if overlap_prologue else 0
+        _configs[key] = c
     return c
 
 
@@ -263,10 +272,14 @@ def cache_scatter(key, value, key_cache, value_cache, slot_mapping, key_scale, k
 
 
 def cache_quant_scatter(key, value, key_cache, value_cache, slot_mapping, key_scale_cache,
-                        v_scale, token_batch, *, layout: int = LAYOUT_BNBD, stream=None):
+                        v_scale, token_batch, *, layout: int = LAYOUT_BNBD,
+                        overlap_prologue: bool = False, stream=None):
     """BF16/FP32 K/V quantised to E4M3 on append (in place): key per
     (token, head) with scale amax/448 stored to key_scale_cache, value against
-    v_scale[token_batch[i]]."""
+    v_scale[token_batch[i]]. overlap_prologue=True launches it with
+    programmatic stream serialisation: the inputs are read while the preceding
+    kernel may still run (it must not write them), the caches are written after
+    it has completed."""
     torch = _torch()
     _need(key, "key", (torch.float32, torch.bfloat16))
     _need(value, "value", (key.dtype,))
@@ -282,7 +295,8 @@ def cache_quant_scatter(key, value, key_cache, value_cache, slot_mapping, key_sc
                                           _ptr(value_cache), _ptr(slot_mapping),
                                           _slot_type(slot_mapping), _ptr(key_scale_cache),
                                           _ptr(v_scale), _ptr(token_batch), v_scale.shape[0], T, H,
-                                          D, NB, BS, layout, _stream(stream))
+                                          D, NB, BS, layout, int(bool(overlap_prologue)),
+                                          _stream(stream))
     _check(st, "pa_fp8_cache_quant_scatter")
 
 

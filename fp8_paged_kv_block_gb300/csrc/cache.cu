@@ -144,15 +144,96 @@ __global__ void scatter_bytes_kernel(const uint8_t* __restrict__ key, const uint
 // ---- quantise-on-append ----------------------------------------------------------
 // One warp per (token, head): key row -> per-row scale and codes, value row ->
 // codes against the sequence's per-channel scale.
-template <typename T>
-__global__ void quant_scatter_kernel(const T* __restrict__ key, const T* __restrict__ value,
-                                     uint8_t* __restrict__ key_cache, uint8_t* __restrict__ value_cache,
-                                     const void* __restrict__ slots, int slot_type,
-                                     float* __restrict__ key_scale_cache,
-                                     const float* __restrict__ v_scale,
-                                     const int* __restrict__ token_batch, int num_batches,
-                                     int64_t ntok, int H, int D, int64_t num_blocks, int BS, int layout)
+//
+// For D <= 128 * NC every lane keeps its NC groups of four values in
+// registers, so all loads (K/V rows, slot, batch, value scales) are issued and
+// every code is computed before griddepcontrol.wait; only the cache stores
+// follow it. Launched with programmatic stream serialisation the kernel thus
+// runs beside the tail of the preceding kernel and writes once that kernel has
+// completed; launched plainly the wait returns at once. Blocks are two warps
+// (kAppendThreads) so that they fit on an SM beside a resident decode CTA.
+constexpr int kAppendThreads = 64;
+
+template <typename T, int NC>
+__global__ void __launch_bounds__(kAppendThreads)
+quant_scatter_kernel(const T* __restrict__ key, const T* __restrict__ value,
+                     uint8_t* __restrict__ key_cache, uint8_t* __restrict__ value_cache,
+                     const void* __restrict__ slots, int slot_type,
+                     float* __restrict__ key_scale_cache, const float* __restrict__ v_scale,
+                     const int* __restrict__ token_batch, int num_batches, int64_t ntok, int H,
+                     int D, int64_t num_blocks, int BS, int layout)
 {
+    grid_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t th = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (th >= ntok * H) return;
+    const int64_t i = th / H;
+    const int j = static_cast<int>(th - i * H);
+    const T* krow = key + th * D;
+    const T* vrow = value + th * D;
+    float k[NC][4] = {}, v[NC][4] = {};
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int d = 128 * c + 4 * lane;
+        if (d < D) {
+            load4(krow + d, k[c]);
+            load4(vrow + d, v[c]);
+        }
+    }
+    const int64_t s = load_slot(slots, slot_type, i);
+    if (s < 0 || s >= num_blocks * BS) return;
+    int tb = __ldg(token_batch + i);
+    tb = tb < 0 ? 0 : (tb >= num_batches ? num_batches - 1 : tb);
+    const float* vs = v_scale + (static_cast<int64_t>(tb) * H + j) * D;
+    float4 sc[NC] = {};
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int d = 128 * c + 4 * lane;
+        if (d < D) {
+            sc[c] = __ldg(reinterpret_cast<const float4*>(vs + d));
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(k[c][0]), fabsf(k[c][1])),
+                                     fmaxf(fabsf(k[c][2]), fabsf(k[c][3]))));
+        }
+    }
+    amax = warp_max(amax);
+    const float ks = __fdiv_rn(amax, kE4M3Max);
+    uint32_t kc[NC], vc[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        kc[c] = encode4_div(k[c], ks);
+        const float q0 = sc[c].x == 0.0f ? 0.0f : __fdiv_rn(v[c][0], sc[c].x);
+        const float q1 = sc[c].y == 0.0f ? 0.0f : __fdiv_rn(v[c][1], sc[c].y);
+        const float q2 = sc[c].z == 0.0f ? 0.0f : __fdiv_rn(v[c][2], sc[c].z);
+        const float q3 = sc[c].w == 0.0f ? 0.0f : __fdiv_rn(v[c][3], sc[c].w);
+        vc[c] = e4m3x4(q0, q1, q2, q3);
+    }
+    const int64_t row = cache_row(layout, s / BS, s % BS, j, BS, H);
+    grid_dependency_wait();
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int d = 128 * c + 4 * lane;
+        if (d < D) {
+            *reinterpret_cast<uint32_t*>(key_cache + row * D + d) = kc[c];
+            *reinterpret_cast<uint32_t*>(value_cache + row * D + d) = vc[c];
+        }
+    }
+    if (lane == 0) key_scale_cache[row] = ks;
+}
+
+// Head sizes above 512: the same encoding in loops over the row, everything
+// after griddepcontrol.wait.
+template <typename T>
+__global__ void __launch_bounds__(kAppendThreads)
+quant_scatter_wide_kernel(const T* __restrict__ key, const T* __restrict__ value,
+                          uint8_t* __restrict__ key_cache, uint8_t* __restrict__ value_cache,
+                          const void* __restrict__ slots, int slot_type,
+                          float* __restrict__ key_scale_cache, const float* __restrict__ v_scale,
+                          const int* __restrict__ token_batch, int num_batches, int64_t ntok,
+                          int H, int D, int64_t num_blocks, int BS, int layout)
+{
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int lane = threadIdx.x & 31;
     const int64_t th = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (th >= ntok * H) return;
@@ -247,6 +328,38 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 inline unsigned int blocks_for(int64_t n, int per) { return static_cast<unsigned int>((n + per - 1) / per); }
 
+// Launches the quantise-on-append kernel for this head size, with
+// programmatic stream serialisation when `overlap` is set.
+template <typename T>
+cudaError_t launch_quant_scatter(const T* key, const T* value, unsigned int grid, cudaStream_t st,
+                                 bool overlap, void* key_cache, void* value_cache,
+                                 const void* slots, int slot_type, float* key_scale_cache,
+                                 const float* v_scale, const int32_t* token_batch,
+                                 int num_batches, int64_t ntok, int H, int D, int64_t num_blocks,
+                                 int BS, int layout)
+{
+    using Kern = void (*)(const T*, const T*, uint8_t*, uint8_t*, const void*, int, float*,
+                          const float*, const int*, int, int64_t, int, int, int64_t, int, int);
+    const Kern k = D <= 128   ? quant_scatter_kernel<T, 1>
+                   : D <= 256 ? quant_scatter_kernel<T, 2>
+                   : D <= 512 ? quant_scatter_kernel<T, 4>
+                              : quant_scatter_wide_kernel<T>;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(kAppendThreads);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, k, key, value, static_cast<uint8_t*>(key_cache),
+                              static_cast<uint8_t*>(value_cache), slots, slot_type,
+                              key_scale_cache, v_scale, token_batch, num_batches, ntok, H, D,
+                              num_blocks, BS, layout);
+}
+
 }  // namespace
 }  // namespace pa
 
@@ -298,7 +411,7 @@ extern "C" pa_status pa_fp8_cache_quant_scatter(const void* key, const void* val
                                                 const int32_t* token_batch, int num_batches,
                                                 int64_t num_tokens, int num_head, int head_size,
                                                 int64_t num_blocks, int block_size, int layout,
-                                                void* stream)
+                                                int overlap_prologue, void* stream)
 {
     PA_REQUIRE(key && value && key_cache && value_cache && slot_mapping && key_scale_cache &&
                    v_scale && token_batch,
@@ -320,20 +433,23 @@ extern "C" pa_status pa_fp8_cache_quant_scatter(const void* key, const void* val
                PA_ERR_INVALID, "pa_fp8_cache_quant_scatter: misaligned pointer");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t warps = num_tokens * num_head;
-    const unsigned int grid = blocks_for(warps * 32, 256);
+    const unsigned int grid = blocks_for(warps * 32, kAppendThreads);
+    cudaError_t e;
     if (in_dtype == PA_DTYPE_F32)
-        quant_scatter_kernel<float><<<grid, 256, 0, st>>>(
-            static_cast<const float*>(key), static_cast<const float*>(value),
-            static_cast<uint8_t*>(key_cache), static_cast<uint8_t*>(value_cache), slot_mapping,
-            slot_type, key_scale_cache, v_scale, token_batch, num_batches, num_tokens, num_head,
-            head_size, num_blocks, block_size, layout);
+        e = launch_quant_scatter(static_cast<const float*>(key), static_cast<const float*>(value),
+                                 grid, st, overlap_prologue != 0, key_cache, value_cache,
+                                 slot_mapping, slot_type, key_scale_cache, v_scale, token_batch,
+                                 num_batches, num_tokens, num_head, head_size, num_blocks,
+                                 block_size, layout);
     else
-        quant_scatter_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(key), static_cast<const __nv_bfloat16*>(value),
-            static_cast<uint8_t*>(key_cache), static_cast<uint8_t*>(value_cache), slot_mapping,
-            slot_type, key_scale_cache, v_scale, token_batch, num_batches, num_tokens, num_head,
-            head_size, num_blocks, block_size, layout);
-    return check_launch("pa_fp8_cache_quant_scatter");
+        e = launch_quant_scatter(static_cast<const __nv_bfloat16*>(key),
+                                 static_cast<const __nv_bfloat16*>(value), grid, st,
+                                 overlap_prologue != 0, key_cache, value_cache, slot_mapping,
+                                 slot_type, key_scale_cache, v_scale, token_batch, num_batches,
+                                 num_tokens, num_head, head_size, num_blocks, block_size, layout);
+    PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_cache_quant_scatter: launch: %s",
+               cudaGetErrorString(e));
+    return PA_OK;
 }
 
 extern "C" pa_status pa_fp8_quantize_rows(const void* x, int in_dtype, int64_t rows, int D,

@@ -253,6 +253,18 @@ PA_API pa_status pa_fp8_cache_scatter(const void* key, const void* value,
  * v_scale      float [num_batches, num_head, head_size].
  * token_batch  int32 [num_tokens], the sequence of each new token, in
  *              [0, num_batches).
+ * overlap_prologue  0: ordinary stream order. Non-zero: the kernel is
+ *              launched with programmatic stream serialisation; it reads key,
+ *              value, slot_mapping, token_batch and v_scale and computes all
+ *              codes while the preceding kernel of the stream may still run,
+ *              and writes the caches only after that kernel has completed
+ *              (griddepcontrol.wait). The caller guarantees that the preceding
+ *              kernel does not write those five inputs. It also lets the next
+ *              kernel launch early (a decode with overlap_prologue set then
+ *              overlaps this one the same way).
+ * Slots, alignment and errors as above; head_size a multiple of 4; key and
+ * value 16-byte (FP32) or 8-byte (BF16) aligned, caches 4-byte, v_scale
+ * 16-byte aligned, else PA_ERR_INVALID.
  * ------------------------------------------------------------------------ */
 PA_API pa_status pa_fp8_cache_quant_scatter(const void* key, const void* value, int in_dtype,
                                      void* key_cache, void* value_cache,
@@ -261,7 +273,7 @@ PA_API pa_status pa_fp8_cache_quant_scatter(const void* key, const void* value, 
                                      const int32_t* token_batch, int num_batches,
                                      int64_t num_tokens, int num_head, int head_size,
                                      int64_t num_blocks, int block_size, int layout,
-                                     void* stream);
+                                     int overlap_prologue, void* stream);
 
 /* ------------------------------------------------------------------------
  * Per-token quantiser ([PA] 量化策略: Query/Key per-token): each row of D

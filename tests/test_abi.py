@@ -102,7 +102,7 @@ def test_quantizers_reject_bad_arguments(L):
     assert L.pa_fp8_quantize_rows(None, 0, 10, 128, fake, fake, None) == 1
     assert L.pa_fp8_value_channel_scale(fake, 0, fake, 0, 10, 8, 128, fake, None) == 2
     assert L.pa_fp8_cache_quant_scatter(fake, fake, 0, fake, fake, fake, 0, fake, fake, fake, 1,
-                                        4, 8, 126, 2, 16, 1, None) == 5
+                                        4, 8, 126, 2, 16, 1, 0, None) == 5
 
 
 def test_product_path_has_no_oracle_dependency():

@@ -161,3 +161,117 @@ def test_append_quant_scatter_bitexact_and_attend(torch_cuda):
                            softmax_scale=ctx.softmax_scale, rows=rows)
     H.compare_bf16(H.to_u16(out), ref, rows=rows)
     assert ws.error_flags() == 0
+
+
+@pytest.mark.parametrize("overlap", [False, True])
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("D", [64, 128, 200, 384, 640])
+def test_quant_scatter_head_sizes(torch_cuda, D, dtype, overlap):
+    """Quantise-on-append for head sizes that take each kernel form (one, two
+    or four groups of 128 channels per warp in registers, and the looped form
+    above 512, with ragged last groups), FP32 and BF16 inputs, plain and with
+    programmatic serialisation: pre-filled BSND caches equal the oracle's
+    byte for byte, including a zero v_scale channel and a zero key row."""
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    T, Hh, NB, BS, NBT = 37, 3, 5, 16, 5
+    rng = np.random.default_rng(1000 + D)
+    k = rng.standard_normal((T, Hh, D)).astype(np.float32) * 3.0
+    v = rng.standard_normal((T, Hh, D)).astype(np.float32)
+    k[4, 1] = 0.0                                          # all-zero key row
+    tdt = getattr(torch, dtype)
+    kt, vt = torch.from_numpy(k).to(tdt), torch.from_numpy(v).to(tdt)
+    k32, v32 = kt.float().numpy(), vt.float().numpy()      # the values the kernel sees
+    slot = rng.choice(NB * BS, T, replace=False).astype(np.int64)
+    slot[rng.random(T) < 0.15] = -1
+    slot[0] = NB * BS + 3                                  # out of range: skipped
+    tb = rng.integers(0, NBT, T).astype(np.int32)
+    vs = (np.abs(rng.standard_normal((NBT, Hh, D))) / 100.0 + 1e-3).astype(np.float32)
+    vs[1, 2, 7] = 0.0
+    kc0 = rng.integers(0, 256, (NB, BS, Hh, D), dtype=np.uint8)
+    vc0 = rng.integers(0, 256, (NB, BS, Hh, D), dtype=np.uint8)
+    ks0 = rng.standard_normal((NB, BS, Hh)).astype(np.float32)
+    kc, vc, ks = (torch.from_numpy(a.copy()).cuda() for a in (kc0, vc0, ks0))
+    pa.cache_quant_scatter(kt.cuda(), vt.cuda(), kc, vc, torch.from_numpy(slot).cuda(), ks,
+                           torch.from_numpy(vs).cuda(), torch.from_numpy(tb).cuda(),
+                           layout=pa.LAYOUT_BSND, overlap_prologue=overlap)
+    torch.cuda.synchronize()
+    okc, ovc, oks = kc0.copy(), vc0.copy(), ks0.copy()
+    oracle.cache_quant_scatter(k32, v32, okc, ovc, slot, oks, vs, tb, layout=workloads.LAYOUT_BSND)
+    assert np.array_equal(kc.cpu().numpy(), okc)
+    assert np.array_equal(vc.cpu().numpy(), ovc)
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+
+
+def test_step_chain_overlap_in_graph(torch_cuda):
+    """decode -> append -> decode with overlap_prologue on all three launches,
+    eagerly and captured in a CUDA graph: the append's stores wait for the
+    first decode, the second decode sees the appended token, both outputs and
+    the cache match the oracle."""
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    case = workloads.custom("chain", 6, 1, 24, 2, [1, 127, 700, 1300, 2049, 3000], max_blocks=25)
+    inp = H.oracle_inputs(case)
+    dev = H.device_inputs(case)
+    ref0 = H.oracle_decode(case, inp)
+    knew, vnew, slot, act_after = workloads.step_tokens(case)
+    import dataclasses
+    case1 = dataclasses.replace(case, act=act_after)
+    oracle.cache_quant_scatter(knew.float().numpy(), vnew.float().numpy(), inp["kc"], inp["vc"],
+                               slot.astype(np.int64), inp["ksc"], inp["vs"],
+                               np.arange(case.B, dtype=np.int32), layout=case.layout)
+    ref1 = H.oracle_decode(case1, inp)
+    c = dev["cache"]
+    snap = [t.clone() for t in (c.k_cache, c.v_cache, c.k_scale)]
+    ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile)
+    shape = (case.B * case.S1, case.NQ, case.D)
+    o0 = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    o1 = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    kn, vn = knew.cuda(), vnew.cuda()
+    sl = torch.from_numpy(slot).cuda()
+    tb = torch.arange(case.B, dtype=torch.int32, device="cuda")
+    act0 = dev["act"]
+    act1 = torch.from_numpy(act_after).cuda()
+
+    def chain():
+        for act, out in ((act0, o0), (None, None), (act1, o1)):
+            if act is None:
+                pa.cache_quant_scatter(kn, vn, c.k_cache, c.v_cache, sl, c.k_scale, c.v_scale, tb,
+                                       layout=case.layout, overlap_prologue=True)
+                continue
+            pa.decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale,
+                      dev["block_table"], act, out, S1=case.S1, layout=case.layout,
+                      s2_tile=case.s2_tile, softmax_scale=case.softmax_scale, workspace=ws,
+                      overlap_prologue=True)
+
+    def check():
+        torch.cuda.synchronize()
+        assert ws.error_flags() == 0
+        H.compare_bf16(H.to_u16(o0), ref0)
+        H.compare_bf16(H.to_u16(o1), ref1)
+        assert np.array_equal(c.k_cache.cpu().numpy(), inp["kc"])
+        assert np.array_equal(c.v_cache.cpu().numpy(), inp["vc"])
+        assert np.array_equal(c.k_scale.cpu().numpy(), inp["ksc"])
+
+    def restore():
+        for t, s in zip((c.k_cache, c.v_cache, c.k_scale), snap):
+            t.copy_(s)
+        o0.fill_(float("nan"))
+        o1.fill_(float("nan"))
+
+    chain()
+    check()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        restore()
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        restore()
+        chain()
+    for _ in range(2):
+        g.replay()
+        check()
