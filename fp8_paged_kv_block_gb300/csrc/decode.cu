@@ -1009,41 +1009,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.hdr_empty[hs]);
             if (cf != cl) {
-                __threadfence();
+                // every consumer thread's partial stores precede the barrier; one
+                // thread then releases them with the count (and acquires the
+                // other parts when it is the last to arrive)
                 named_bar_sync(1, kNCW * 32);
                 if (tid == 0) {
-                    const int old = atomicAdd(p.counters + u, 1);
+                    int old;
+                    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                                 : "=r"(old)
+                                 : "l"(p.counters + u)
+                                 : "memory");
                     const int last = (old == cl - cf);
                     if (last) p.counters[u] = 0;
                     sm.flag = last;
                 }
                 named_bar_sync(1, kNCW * 32);
                 if (sm.flag) {
-                    __threadfence();
                     const int n = cl - cf + 1;
                     for (int item = tid; item < NR * 16; item += kNCW * 32) {
                         const int orow = item >> 4, d0 = (item & 15) * 8;
                         const int r = rc * NR + orow;
                         if (orow >= nrows) continue;
-                        float mx = -INFINITY;
-                        for (int k = 0; k < n; ++k)
-                            mx = fmaxf(mx, __ldcg(p.part + (u + cf + k) * kPartFloats + 32 * kD + orow));
-                        float lsm = 0.f;
+                        // one pass over the parts, four at a time with every load
+                        // issued first, rescaling to the running maximum
+                        float mx = -INFINITY, lsm = 0.f;
                         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        for (int k = 0; k < n; ++k) {
-                            const float* pp = p.part + (u + cf + k) * kPartFloats;
-                            const float sc = ex2(__ldcg(pp + 32 * kD + orow) - mx);
-                            lsm += __ldcg(pp + 32 * kD + 32 + orow) * sc;
-                            const float4 o4a = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0));
-                            const float4 o4b = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0 + 4));
-                            acc[0] += o4a.x * sc;
-                            acc[1] += o4a.y * sc;
-                            acc[2] += o4a.z * sc;
-                            acc[3] += o4a.w * sc;
-                            acc[4] += o4b.x * sc;
-                            acc[5] += o4b.y * sc;
-                            acc[6] += o4b.z * sc;
-                            acc[7] += o4b.w * sc;
+                        for (int k0 = 0; k0 < n; k0 += 4) {
+                            float mk[4], lk[4];
+                            float4 oa[4], ob[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                if (k0 + q < n) {
+                                    const float* pp = p.part + (u + cf + k0 + q) * kPartFloats;
+                                    mk[q] = __ldcg(pp + 32 * kD + orow);
+                                    lk[q] = __ldcg(pp + 32 * kD + 32 + orow);
+                                    oa[q] = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0));
+                                    ob[q] = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0 + 4));
+                                } else {
+                                    mk[q] = -INFINITY;
+                                    lk[q] = 0.f;
+                                    oa[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                    ob[q] = oa[q];
+                                }
+                            }
+                            const float mn = fmaxf(fmaxf(mx, fmaxf(mk[0], mk[1])), fmaxf(mk[2], mk[3]));
+                            const float c = ex2(mx - mn);
+                            lsm *= c;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] *= c;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float sc = ex2(mk[q] - mn);
+                                lsm += lk[q] * sc;
+                                acc[0] += oa[q].x * sc;
+                                acc[1] += oa[q].y * sc;
+                                acc[2] += oa[q].z * sc;
+                                acc[3] += oa[q].w * sc;
+                                acc[4] += ob[q].x * sc;
+                                acc[5] += ob[q].y * sc;
+                                acc[6] += ob[q].z * sc;
+                                acc[7] += ob[q].w * sc;
+                            }
+                            mx = mn;
                         }
                         uint4 o;
                         o.x = pack_bf16x2(__fdiv_rn(acc[0], lsm), __fdiv_rn(acc[1], lsm));
