@@ -88,7 +88,7 @@ __host__ __device__ constexpr uint32_t tmem_cols(int need)
 // consumers): as many as fit next to O^T in the 512 columns, at most 4.
 __host__ __device__ constexpr int s_buffers(int sc, int nr)
 {
-    return (4 * sc + nr <= 512) ? 4 : ((3 * sc + nr <= 512) ? 3 : 2);
+    return (4 * sc + 2 * nr <= 512) ? 4 : ((3 * sc + 2 * nr <= 512) ? 3 : 2);
 }
 
 struct Pos {
@@ -116,6 +116,7 @@ struct __align__(1024) DecodeSmemT {
     float red[2][kNCW][32];     // per-warp row maxima, double-buffered by tile
     float redl[kNCW][32];       // per-warp row sums at unit end
     alignas(16) float wst[kNCW][4][32];   // per-warp copies of row values
+    alignas(16) float wfold[2][kNCW][2][32];   // per-warp fold weights c1, c2 by tile parity
     int scan[kThreads / 32];
     int bpre[kMaxB + 1];
     int slen[kMaxB];
@@ -321,8 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int MBW = NBT >= 2 ? NBT / 2 : 1;  // blocks per consumer warp
     constexpr int SC = NBT * NR;                 // tensor-memory columns of one S^T buffer
     constexpr int NSB = s_buffers(SC, NR);       // S^T buffers
-    constexpr int OCOL = NSB * SC;               // first column of O^T
-    constexpr uint32_t TCOLS = tmem_cols(NSB * SC + NR);
+    constexpr int OCOL = NSB * SC;               // first column of O^T (two buffers of NR columns)
+    constexpr uint32_t TCOLS = tmem_cols(NSB * SC + 2 * NR);
     constexpr int HR = NR / 2;                   // O^T columns (query rows) per consumer warp
     constexpr int TC = S2T + kC0;
     constexpr int NSLOT = DecodeSmem<NR, S2T>::NSLOT;
@@ -735,10 +736,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O^T starts at zero: every MM2 MMA accumulates
         const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < HR; c += 8) tmem_st8(tl + OCOL + hh * HR + c, zero8);
+        for (int c = 0; c < HR; c += 8) {
+            tmem_st8(tl + OCOL + hh * HR + c, zero8);
+            tmem_st8(tl + OCOL + NR + hh * HR + c, zero8);
+        }
         tmem_wait_st();
         tc_fence_before();
     }
+    // Tile k's O^T (buffer k & 1) folded into Oa once its MM2 has completed,
+    // with the weights of tile k, then zeroed for tile k + 2.
+    auto fold = [&](int k) {
+        mbar_wait(&sm.o_full, k & 1, p.err, 512, &sm.abort);
+        tc_fence_after();
+        float ot[HR];
+        tmem_ld_cols<HR>(tl + OCOL + (k & 1) * NR + hh * HR, ot);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c4 = 0; c4 < HR / 4; ++c4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&sm.wfold[k & 1][warp][0][hh * HR + 4 * c4]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&sm.wfold[k & 1][warp][1][hh * HR + 4 * c4]);
+            Oa[4 * c4 + 0] = Oa[4 * c4 + 0] * a4.x + ot[4 * c4 + 0] * b4.x;
+            Oa[4 * c4 + 1] = Oa[4 * c4 + 1] * a4.y + ot[4 * c4 + 1] * b4.y;
+            Oa[4 * c4 + 2] = Oa[4 * c4 + 2] * a4.z + ot[4 * c4 + 2] * b4.z;
+            Oa[4 * c4 + 3] = Oa[4 * c4 + 3] * a4.w + ot[4 * c4 + 3] * b4.w;
+        }
+        // zeroed for the MMAs of tile k + 2, which come after that tile's
+        // row-maximum barrier
+        const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < HR; c += 8) tmem_st8(tl + OCOL + (k & 1) * NR + hh * HR + c, zero8);
+        tmem_wait_st();
+        tc_fence_before();
+    };
+    int pend = -1;   // tile whose O^T has not been folded yet
 
     for (Pos x = start; !pos_eq(x, end);) {
         const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
@@ -833,11 +863,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             Mref = Mn;
             if (rep) {
                 sm.wst[warp][0][rho] = mt;
-                sm.wst[warp][1][rho] = c1;
-                sm.wst[warp][2][rho] = c2;
+                sm.wfold[tcount & 1][warp][0][rho] = c1;
+                sm.wfold[tcount & 1][warp][1][rho] = c2;
             }
         }
         __syncwarp();
+        // the previous tile's MM2 ran while this tile's maxima were found
+        if (pend >= 0) fold(pend);
 
         // ---- P = 2^(x - tile max), row sums, P8 = E4M3(448 P) as the MM2 operand ----
         float ls[NR];
@@ -904,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort);
                         tc_fence_after();
                         const uint64_t vd = smem_desc(smem_u32(sm.ring[vsl[jj]]), 1024, 1024, kSmem128BSwizzle);
-                        umma_e4m3(tmem + OCOL, vd + 256 * q4,
+                        umma_e4m3(tmem + OCOL + (tcount & 1) * NR, vd + 256 * q4,
                                   pd + static_cast<uint64_t>(((mb * kBS + 32 * q4) * NR) >> 4), kIdescO, 1);
                         umma_commit(&sm.empty_bar[vsl[jj]]);
                         any = true;
@@ -918,39 +950,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         }
 
-        // ---- running sums, then this tile's O^T folded into the accumulator ----
-        float c1v[NR], c2v[NR];
+        // ---- running sums; this tile's O^T is folded with the next tile ----
 #pragma unroll
         for (int r4 = 0; r4 < NR / 4; ++r4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(&sm.wst[warp][1][4 * r4]);
-            const float4 b4 = *reinterpret_cast<const float4*>(&sm.wst[warp][2][4 * r4]);
-            c1v[4 * r4 + 0] = a4.x;
-            c1v[4 * r4 + 1] = a4.y;
-            c1v[4 * r4 + 2] = a4.z;
-            c1v[4 * r4 + 3] = a4.w;
-            c2v[4 * r4 + 0] = b4.x;
-            c2v[4 * r4 + 1] = b4.y;
-            c2v[4 * r4 + 2] = b4.z;
-            c2v[4 * r4 + 3] = b4.w;
+            const float4 a4 = *reinterpret_cast<const float4*>(&sm.wfold[tcount & 1][warp][0][4 * r4]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&sm.wfold[tcount & 1][warp][1][4 * r4]);
+            Lp[4 * r4 + 0] = Lp[4 * r4 + 0] * a4.x + ls[4 * r4 + 0] * b4.x;
+            Lp[4 * r4 + 1] = Lp[4 * r4 + 1] * a4.y + ls[4 * r4 + 1] * b4.y;
+            Lp[4 * r4 + 2] = Lp[4 * r4 + 2] * a4.z + ls[4 * r4 + 2] * b4.z;
+            Lp[4 * r4 + 3] = Lp[4 * r4 + 3] * a4.w + ls[4 * r4 + 3] * b4.w;
         }
-#pragma unroll
-        for (int r = 0; r < NR; ++r) Lp[r] = Lp[r] * c1v[r] + ls[r] * c2v[r];
-        mbar_wait(&sm.o_full, tcount & 1, p.err, 512, &sm.abort);
-        tc_fence_after();
-        {
-            float ot[HR];
-            tmem_ld_cols<HR>(tl + OCOL + hh * HR, ot);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < HR; ++k) Oa[k] = Oa[k] * c1v[hh * HR + k] + ot[k] * c2v[hh * HR + k];
-            // zero this warp's part of O^T for the next tile's MMAs (which come
-            // after the next tile's row-maximum barrier)
-            const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < HR; c += 8) tmem_st8(tl + OCOL + hh * HR + c, zero8);
-            tmem_wait_st();
-            tc_fence_before();
-        }
+        pend = tcount;
         vslot += nb;
         if (vslot >= NV) {
             vslot -= NV;
@@ -960,6 +970,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (t == T - 1 || pos_eq(nx, end)) {
             // ------------------------------ unit end ------------------------------
+            fold(pend);
+            pend = -1;
             float lsum[NR];
 #pragma unroll
             for (int r = 0; r < NR; ++r) lsum[r] = Lp[r];
