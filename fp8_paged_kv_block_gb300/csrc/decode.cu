@@ -1128,9 +1128,12 @@ pa_status make_cache_map(CUtensorMap* map, const void* base, uint64_t inner, uin
     cuuint64_t strides[1] = {inner};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBS)};
     cuuint32_t estr[2] = {1, 1};
+    // L2 promotion to 128 bytes, the row size: with PA_BSND a row is one head's
+    // 128 bytes of a token, and a larger promotion would also fetch the next
+    // head's bytes, which another CTA reads at another time
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     PA_REQUIRE(r == CUDA_SUCCESS, PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return PA_OK;
 }
