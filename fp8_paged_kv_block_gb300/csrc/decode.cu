@@ -69,6 +69,7 @@ constexpr int kC0 = 512;
 constexpr int kCU = 1024;
 constexpr int kPartFloats = 32 * kD + 64;    // O[32][128], M[32], L[32]
 constexpr size_t kWsHeader = 256;            // error flag + padding
+constexpr uint64_t kMergeWaitNs = 100000;     // the merging CTA's wait for the other parts
 
 // How one block's 128 key scales of one head arrive.
 enum : int {
@@ -1009,7 +1010,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<const uint4*>(stage + rr * kD + c8);
                 }
                 named_bar_sync(1, kNCW * 32);   // staging free before the next tile's P8
-            } else {
+            }
+            // A split unit's first CTA holds the range's last unit: it merges,
+            // normally without publishing its own part
+            const bool merger = cf != cl && cta == cf;
+            auto write_part = [&]() {
                 float* part = p.part + (u + cta) * kPartFloats;
 #pragma unroll
                 for (int k = 0; k < HR; ++k) part[(hh * HR + k) * kD + ch] = Oa[k] * vs;
@@ -1017,80 +1022,137 @@ __global__ void __launch_bounds__(kThreads, 1)
                     part[32 * kD + rho] = Mref;
                     part[32 * kD + 32 + rho] = L;
                 }
-            }
+            };
+            if (cf != cl && !merger) write_part();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.hdr_empty[hs]);
-            if (cf != cl) {
-                // every consumer thread's partial stores precede the barrier; one
-                // thread then releases them with the count (and acquires the
-                // other parts when it is the last to arrive)
-                named_bar_sync(1, kNCW * 32);
-                if (tid == 0) {
-                    int old;
-                    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
-                                 : "=r"(old)
-                                 : "l"(p.counters + u)
-                                 : "memory");
-                    const int last = (old == cl - cf);
-                    if (last) p.counters[u] = 0;
-                    sm.flag = last;
-                }
-                named_bar_sync(1, kNCW * 32);
-                if (sm.flag) {
-                    const int n = cl - cf + 1;
-                    for (int item = tid; item < NR * 16; item += kNCW * 32) {
-                        const int orow = item >> 4, d0 = (item & 15) * 8;
-                        const int r = rc * NR + orow;
-                        if (orow >= nrows) continue;
-                        // one pass over the parts, four at a time with every load
-                        // issued first, rescaling to the running maximum
-                        float mx = -INFINITY, lsm = 0.f;
-                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        for (int k0 = 0; k0 < n; k0 += 4) {
-                            float mk[4], lk[4];
-                            float4 oa[4], ob[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                if (k0 + q < n) {
-                                    const float* pp = p.part + (u + cf + k0 + q) * kPartFloats;
-                                    mk[q] = __ldcg(pp + 32 * kD + orow);
-                                    lk[q] = __ldcg(pp + 32 * kD + 32 + orow);
-                                    oa[q] = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0));
-                                    ob[q] = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0 + 4));
-                                } else {
-                                    mk[q] = -INFINITY;
-                                    lk[q] = 0.f;
-                                    oa[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                                    ob[q] = oa[q];
-                                }
-                            }
-                            const float mn = fmaxf(fmaxf(mx, fmaxf(mk[0], mk[1])), fmaxf(mk[2], mk[3]));
-                            const float c = ex2(mx - mn);
-                            lsm *= c;
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] *= c;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float sc = ex2(mk[q] - mn);
-                                lsm += lk[q] * sc;
-                                acc[0] += oa[q].x * sc;
-                                acc[1] += oa[q].y * sc;
-                                acc[2] += oa[q].z * sc;
-                                acc[3] += oa[q].w * sc;
-                                acc[4] += ob[q].x * sc;
-                                acc[5] += ob[q].y * sc;
-                                acc[6] += ob[q].z * sc;
-                                acc[7] += ob[q].w * sc;
-                            }
-                            mx = mn;
-                        }
-                        uint4 o;
-                        o.x = pack_bf16x2(__fdiv_rn(acc[0], lsm), __fdiv_rn(acc[1], lsm));
-                        o.y = pack_bf16x2(__fdiv_rn(acc[2], lsm), __fdiv_rn(acc[3], lsm));
-                        o.z = pack_bf16x2(__fdiv_rn(acc[4], lsm), __fdiv_rn(acc[5], lsm));
-                        o.w = pack_bf16x2(__fdiv_rn(acc[6], lsm), __fdiv_rn(acc[7], lsm));
-                        *reinterpret_cast<uint4*>(p.out + q_row(p, b, n2, r) * kD + d0) = o;
+            // rows of the unit combined from its parts (own: this CTA's part in
+            // shared memory when non-null, else every part from the workspace)
+            auto merge = [&](const float* own) {
+                const int n = cl - cf + 1;
+                for (int item = tid; item < NR * 16; item += kNCW * 32) {
+                    const int orow = item >> 4, d0 = (item & 15) * 8;
+                    const int r = rc * NR + orow;
+                    if (orow >= nrows) continue;
+                    // one pass over the parts, four at a time with every load
+                    // issued first, rescaling to the running maximum
+                    float mx = -INFINITY, lsm = 0.f;
+                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    int kfirst = 0;
+                    if (own != nullptr) {
+                        mx = own[32 * kD + orow];
+                        lsm = own[32 * kD + 32 + orow];
+                        const float4 a = *reinterpret_cast<const float4*>(own + orow * kD + d0);
+                        const float4 c = *reinterpret_cast<const float4*>(own + orow * kD + d0 + 4);
+                        acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+                        acc[4] = c.x; acc[5] = c.y; acc[6] = c.z; acc[7] = c.w;
+                        kfirst = 1;
                     }
+                    for (int k0 = kfirst; k0 < n; k0 += 4) {
+                        float mk[4], lk[4];
+                        float4 oa[4], ob[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (k0 + q < n) {
+                                const float* pp = p.part + (u + cf + k0 + q) * kPartFloats;
+                                mk[q] = __ldcg(pp + 32 * kD + orow);
+                                lk[q] = __ldcg(pp + 32 * kD + 32 + orow);
+                                oa[q] = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0));
+                                ob[q] = __ldcg(reinterpret_cast<const float4*>(pp + orow * kD + d0 + 4));
+                            } else {
+                                mk[q] = -INFINITY;
+                                lk[q] = 0.f;
+                                oa[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                ob[q] = oa[q];
+                            }
+                        }
+                        const float mn = fmaxf(fmaxf(mx, fmaxf(mk[0], mk[1])), fmaxf(mk[2], mk[3]));
+                        const float c = ex2(mx - mn);
+                        lsm *= c;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] *= c;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float sc = ex2(mk[q] - mn);
+                            lsm += lk[q] * sc;
+                            acc[0] += oa[q].x * sc;
+                            acc[1] += oa[q].y * sc;
+                            acc[2] += oa[q].z * sc;
+                            acc[3] += oa[q].w * sc;
+                            acc[4] += ob[q].x * sc;
+                            acc[5] += ob[q].y * sc;
+                            acc[6] += ob[q].z * sc;
+                            acc[7] += ob[q].w * sc;
+                        }
+                        mx = mn;
+                    }
+                    uint4 o;
+                    o.x = pack_bf16x2(__fdiv_rn(acc[0], lsm), __fdiv_rn(acc[1], lsm));
+                    o.y = pack_bf16x2(__fdiv_rn(acc[2], lsm), __fdiv_rn(acc[3], lsm));
+                    o.z = pack_bf16x2(__fdiv_rn(acc[4], lsm), __fdiv_rn(acc[5], lsm));
+                    o.w = pack_bf16x2(__fdiv_rn(acc[6], lsm), __fdiv_rn(acc[7], lsm));
+                    *reinterpret_cast<uint4*>(p.out + q_row(p, b, n2, r) * kD + d0) = o;
+                }
+            };
+            if (cf != cl) {
+                bool done = false;
+                if (merger) {
+                    // the other parts are normally complete by now (their CTAs
+                    // reach them at the start of their ranges): an acquire load
+                    // of their count, bounded so that a part whose CTA is not
+                    // running yet cannot hold this one
+                    if (tid == 0) {
+                        const int want = cl - cf;
+                        int ok = 0;
+                        const uint64_t t0 = globaltimer_ns();
+                        for (;;) {
+                            int v;
+                            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p.counters + u) : "memory");
+                            if (v == want) {
+                                ok = 1;
+                                break;
+                            }
+                            if (globaltimer_ns() - t0 > kMergeWaitNs) break;
+                            __nanosleep(64);
+                        }
+                        if (ok) p.counters[u] = 0;
+                        sm.flag = ok;
+                    }
+                    named_bar_sync(1, kNCW * 32);
+                    done = sm.flag != 0;
+                    if (done) {
+                        // this CTA's part staged in the ring (its last tile's
+                        // loads and MMAs are complete)
+                        float* own = reinterpret_cast<float*>(sm.ring[0]);
+#pragma unroll
+                        for (int k = 0; k < HR; ++k) own[(hh * HR + k) * kD + ch] = Oa[k] * vs;
+                        if (warp == 0 && rep) {
+                            own[32 * kD + rho] = Mref;
+                            own[32 * kD + 32 + rho] = L;
+                        }
+                        named_bar_sync(1, kNCW * 32);
+                        merge(own);
+                    } else {
+                        write_part();
+                    }
+                }
+                if (!done) {
+                    // every consumer thread's partial stores precede the barrier; one
+                    // thread then releases them with the count (and acquires the
+                    // other parts when it is the last to arrive)
+                    named_bar_sync(1, kNCW * 32);
+                    if (tid == 0) {
+                        int old;
+                        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                                     : "=r"(old)
+                                     : "l"(p.counters + u)
+                                     : "memory");
+                        const int last = (old == cl - cf);
+                        if (last) p.counters[u] = 0;
+                        sm.flag = last;
+                    }
+                    named_bar_sync(1, kNCW * 32);
+                    if (sm.flag) merge(nullptr);
                 }
             }
         }
