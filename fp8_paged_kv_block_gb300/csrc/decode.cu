@@ -15,29 +15,30 @@
 //    cut into contiguous per-CTA ranges balanced by token count (plus fixed
 //    per-unit and per-tile costs); ranges start and end on tile boundaries so
 //    the P-quantisation groups are those of the sequential walk. A unit split
-//    across CTAs is merged by whichever CTA finishes its part last
-//    (log-sum-exp combine through the workspace; no waiting on other CTAs).
-//  * Warp 8 (one thread) is the producer: per 128-token block one 2-D TMA
-//    load (128 rows x 128 bytes, 128-byte swizzle) of K or V into a
-//    shared-memory ring, plus the block's key scales with K; per unit the Q
-//    rows, q_scale and v_scale. Block ids are loaded one tile ahead.
-//  * Warp 9 owns the tensor memory and issues the tensor-core MMAs
-//    (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32, M = 128) from one thread:
+//    across CTAs is merged (log-sum-exp) by its first CTA, which reaches it
+//    last; the other parts are published through the workspace with a
+//    release count, and a bounded wait falls back to last-arriver merging.
+//  * Warp 8 (one thread) feeds the K ring: per 128-token block one 2-D TMA
+//    load (128 rows x 128 bytes, 128-byte swizzle); per unit the Q rows,
+//    q_scale and v_scale. Warp 9 (one thread) feeds the V ring the same way.
+//  * Warp 10 owns the tensor memory and issues MM1 from one thread
+//    (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32, M = 128):
 //      MM1  S^T[token][row]   = K_blk (K-major, the ring slot as loaded)
 //                               x Q^T (K-major, 128-byte swizzled rows)
-//      MM2  O^T[chan][row]    = V_blk^T (MN-major: the same ring slot)
-//                               x P8^T (MN-major, written by the consumers)
-//    S^T lives in tensor memory, double-buffered across tiles; O^T of one
-//    tile is a fresh tensor-memory accumulator.
+//    S^T lives in tensor memory, up to 4 tiles ahead of the consumers.
 //  * Warps 0-7 consume: tcgen05.ld of S^T (a lane = a token, a column = a
-//    query row), scaling by q_scale * k_scale, masking past kv_act_seqs, the
-//    tile's row maxima (butterfly over lanes, then over warps through shared
-//    memory), P = 2^(x - tile max), the row sums, E4M3 P8 = 448 * P written
-//    as the MM2 operand, then the tile's O^T folded into registers with the
-//    running-max rescale. Quantising against the tile's own maximum gives the
-//    same codes as quantising exp(S - running max) against its tile maximum
-//    (the ratio cancels the running max); the running max only weights whole
-//    tiles.
+//    query row), scaling by q_scale * k_scale (each thread loads its token's
+//    key scales a tile ahead), masking past kv_act_seqs, the tile's row
+//    maxima (butterfly over lanes, then over warps through shared memory),
+//    P = 2^(x - tile max), the row sums, E4M3 P8 = 448 * P written as the
+//    MM2 operand; each warp then issues the MM2 k-step of its own tokens:
+//      MM2  O^T[chan][row]   += V_blk^T (MN-major: the V ring slot)
+//                               x P8^T (MN-major)
+//    O^T is double-buffered by tile parity and folded into registers with the
+//    running-max rescale while the next tile's maxima are found. Quantising
+//    against the tile's own maximum gives the same codes as quantising
+//    exp(S - running max) against its tile maximum (the ratio cancels the
+//    running max); the running max only weights whole tiles.
 //  * Masked tokens get S = -inf (selected, never multiplied) and P = 0; the
 //    V rows of a partial last block are zeroed in shared memory before MM2
 //    (a stale E4M3 NaN code times 0 is NaN).
@@ -61,7 +62,6 @@ constexpr int kMmaWarp = kNCW + 2;          // tensor memory owner; issues MM1
 constexpr int kThreads = (kNCW + 3) * 32;
 constexpr int kKSlots = 5;                   // K ring; the V ring takes the other slots
 constexpr int kSlotBytes = kBS * kD;         // one 128-token block of one head
-constexpr int kKsFloats = 512;               // key-scale area per ring slot
 constexpr int kMaxB = 1024;
 // Work-balancing cost model in token units: a unit (batch, kv head, row
 // chunk) costs kCU + tokens + tiles * kC0 (fixed per-unit and per-tile costs).
@@ -70,13 +70,6 @@ constexpr int kCU = 1024;
 constexpr int kPartFloats = 32 * kD + 64;    // O[32][128], M[32], L[32]
 constexpr size_t kWsHeader = 256;            // error flag + padding
 constexpr uint64_t kMergeWaitNs = 100000;     // the merging CTA's wait for the other parts
-
-// How one block's 128 key scales of one head arrive.
-enum : int {
-    KS_CONTIG = 0,   // BNBD: 128 contiguous floats, one 512-byte bulk copy
-    KS_QUAD = 1,     // BSND, NKV % 4 == 0: 2-D TMA box of 4 heads x 128 rows
-    KS_WHOLE = 2     // BSND, NKV <= 3: the block's whole [128][NKV] region
-};
 
 __host__ __device__ constexpr uint32_t tmem_cols(int need)
 {
@@ -111,7 +104,6 @@ struct __align__(1024) DecodeSmemT {
     // (also the BF16 staging of a unit's output rows, NR x 128 x 2 bytes)
     alignas(1024) uint8_t pbuf[S2T * NR > NR * kD * 2 ? S2T * NR : NR * kD * 2];
     // key scales of one tile's blocks, double-buffered by tile parity
-    alignas(128) float ksb[2][S2T / kBS][kKsFloats];
     alignas(16) float vsc[2][kD];
     alignas(16) float qs[2][32];
     float red[2][kNCW][32];     // per-warp row maxima, double-buffered by tile
@@ -125,8 +117,6 @@ struct __align__(1024) DecodeSmemT {
     uint64_t empty_bar[NS];
     uint64_t hdr_full[2];
     uint64_t hdr_empty[2];
-    uint64_t ks_full[2];
-    uint64_t ks_empty[2];
     uint64_t s_full[4];
     uint64_t s_empty[4];
     uint64_t o_full;
@@ -166,7 +156,7 @@ struct DecodeParams {
     int* counters;
     int* err;
     int64_t num_blocks;
-    int B, S1, NQ, NKV, G, R, NRC, max_blocks, layout, grid, maxlen, ks_mode;
+    int B, S1, NQ, NKV, G, R, NRC, max_blocks, layout, grid, maxlen;
     int overlap;   // launched with programmatic stream serialisation
     float sscale;  // softmax_scale * log2(e)
 };
@@ -317,7 +307,7 @@ __device__ __forceinline__ int ring_slot(int slot, uint32_t ph, int j, uint32_t*
 template <int NR, int S2T>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmKS, const DecodeParams p)
+                  const DecodeParams p)
 {
     constexpr int NBT = S2T / kBS;               // 128-token blocks (MMA M-blocks) per tile
     constexpr int MBW = NBT >= 2 ? NBT / 2 : 1;  // blocks per consumer warp
@@ -352,8 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.hdr_full[i], 2);           // byte-counted copies + the q_scale cp.async
             mbar_init(&sm.hdr_empty[i], 1 + kNCW);   // last MM1 of the unit + every consumer warp
-            mbar_init(&sm.ks_full[i], 1);
-            mbar_init(&sm.ks_empty[i], kNCW);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&sm.s_full[i], 1);
@@ -466,10 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool isK = warp == kKProducerWarp;
         const CUtensorMap* tm = isK ? &tmK : &tmV;
         asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
-        if (isK && p.ks_mode == KS_QUAD) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmKS) : "memory");
         const uint64_t pol = l2_evict_first_policy();
-        const int ks_bytes = p.ks_mode == KS_CONTIG ? kBS * 4
-                                                    : (p.ks_mode == KS_QUAD ? kBS * 16 : kBS * 4 * p.NKV);
         const int base = isK ? 0 : NK, nring = isK ? NK : NV;
         int slot = 0;
         uint32_t ph = 0;
@@ -553,12 +538,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // this tile's key scales go to their own buffer (tile parity kb)
-            const int kb = tcount & 1;
-            if (isK) {
-                mbar_wait(&sm.ks_empty[kb], ((tcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort);
-                mbar_arrive_expect_tx(&sm.ks_full[kb], static_cast<uint32_t>(nb * ks_bytes));
-            }
 #pragma unroll
             for (int j = 0; j < NBT; ++j) {
                 if (j >= nb) break;
@@ -576,17 +555,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_arrive_expect_tx(&sm.full_bar[sl], kSlotBytes);
                 tma_load_2d(sm.ring[sl], tm, x0, y0, &sm.full_bar[sl], pol);
-                if (isK) {
-                    float* kdst = sm.ksb[kb][j];
-                    if (p.ks_mode == KS_CONTIG)
-                        bulk_load_1d(kdst, p.k_scale + (static_cast<int64_t>(blk) * p.NKV + n2) * kBS, kBS * 4,
-                                     &sm.ks_full[kb]);
-                    else if (p.ks_mode == KS_QUAD)
-                        tma_load_2d_nohint(kdst, &tmKS, n2 & ~3, blk * kBS, &sm.ks_full[kb]);
-                    else
-                        bulk_load_1d(kdst, p.k_scale + static_cast<int64_t>(blk) * kBS * p.NKV,
-                                     static_cast<uint32_t>(ks_bytes), &sm.ks_full[kb]);
-                }
                 ++fills;
                 if (++slot == nring) {
                     slot = 0;
@@ -615,10 +583,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n > 0) mbar_wait_drain(&sm.full_bar[base + s], static_cast<uint32_t>(n - 1) & 1u, p.err, 1024);
         }
         if (isK) {
-            for (int h = 0; h < 2; ++h) {
-                const int n = tcount / 2 + (h < tcount % 2 ? 1 : 0);
-                if (n > 0) mbar_wait_drain(&sm.ks_full[h], static_cast<uint32_t>(n - 1) & 1u, p.err, 1024);
-            }
             for (int h = 0; h < 2; ++h) {
                 const int n = hcount / 2 + (h < hcount % 2 ? 1 : 0);
                 if (n > 0) mbar_wait_drain(&sm.hdr_full[h], static_cast<uint32_t>(n - 1) & 1u, p.err, 1024);
@@ -721,7 +685,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = cta; b < p.B; b += p.grid)
         if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
 
-    int ks_st = 1, ks_off = 0;
     int vslot = 0;
     uint32_t vph = 0;
     int hcount = 0, tcount = 0, hs = 0, nrows = 0;
@@ -770,6 +733,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
     };
     int pend = -1;   // tile whose O^T has not been folded yet
+    // Key scales of this thread's token (lane) in each of its blocks, read
+    // from global memory through L2 one tile ahead of their use (the block
+    // ids one tile before that), so that the loads are in flight while the
+    // current tile is processed and no copy engine or shared memory is used.
+    const int ktok = 32 * q4 + lane;
+    auto tile_ids = [&](const Pos& y, int (&ids)[MBW]) {
+        const int nby = min(NBT, (sm.slen[y.b] - y.t * S2T + kBS - 1) / kBS);
+        const int* row = p.block_table + static_cast<int64_t>(y.b) * p.max_blocks + y.t * NBT;
+#pragma unroll
+        for (int jj = 0; jj < MBW; ++jj) {
+            const int mb = hh * MBW + jj;
+            ids[jj] = mb < nby ? __ldg(row + mb) : -1;
+        }
+    };
+    auto tile_ks = [&](const Pos& y, const int (&ids)[MBW], float (&dst)[MBW]) {
+        const int n2y = y.i / p.NRC;
+#pragma unroll
+        for (int jj = 0; jj < MBW; ++jj) {
+            int blk = ids[jj];
+            if (blk < 0 || blk >= p.num_blocks) blk = 0;
+            const int64_t idx = p.layout == PA_LAYOUT_BSND
+                                    ? (static_cast<int64_t>(blk) * kBS + ktok) * p.NKV + n2y
+                                    : (static_cast<int64_t>(blk) * p.NKV + n2y) * kBS + ktok;
+            dst[jj] = __ldcg(p.k_scale + idx);
+        }
+    };
+    float ksn[MBW];   // key scales of the next tile
+    int idn[MBW];     // block ids of the tile after it
+#pragma unroll
+    for (int jj = 0; jj < MBW; ++jj) {
+        ksn[jj] = 0.f;
+        idn[jj] = -1;
+    }
+    if (!pos_eq(start, end)) {
+        int id0[MBW];
+        tile_ids(start, id0);
+        tile_ks(start, id0, ksn);
+        const Pos y2 = pos_next<S2T>(sm.slen, sm.bpre, p.B, start, W);
+        if (!pos_eq(y2, end)) tile_ids(y2, idn);
+    }
 
     for (Pos x = start; !pos_eq(x, end);) {
         const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
@@ -780,16 +783,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (first || t == 0) {
             hs = hcount & 1;
             mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
-            if (p.ks_mode == KS_CONTIG) {
-                ks_st = 1;
-                ks_off = 0;
-            } else if (p.ks_mode == KS_QUAD) {
-                ks_st = 4;
-                ks_off = n2 & 3;
-            } else {
-                ks_st = p.NKV;
-                ks_off = n2;
-            }
             nrows = min(p.R - rc * NR, NR);
             if (warp == 0 && lane < NR) sm.orow[hcount & 1][lane] = q_row(p, b, n2, rc * NR + lane);
 #pragma unroll
@@ -804,32 +797,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int valid = min(S2T, len - t * S2T);
         const int nb = (valid + kBS - 1) / kBS;
         const int sb = tcount % NSB;
+        float ksv[MBW];
+#pragma unroll
+        for (int jj = 0; jj < MBW; ++jj) ksv[jj] = ksn[jj];
+        if (!pos_eq(nx, end)) {
+            tile_ks(nx, idn, ksn);
+            const Pos nnx = pos_next<S2T>(sm.slen, sm.bpre, p.B, nx, W);
+            if (!pos_eq(nnx, end)) tile_ids(nnx, idn);
+        }
 
         // ---- S^T of this warp's blocks and their key scales ----
         mbar_wait(&sm.s_full[sb], (tcount / NSB) & 1, p.err, 256, &sm.abort);
         tc_fence_after();
         float sv[MBW][NR];
-        float ksv[MBW];
 #pragma unroll
         for (int jj = 0; jj < MBW; ++jj) {
             const int mb = hh * MBW + jj;
-            ksv[jj] = 0.f;
             if (mb < nb) tmem_ld_cols<NR>(tl + sb * SC + mb * NR, sv[jj]);
-        }
-        const int kb = tcount & 1;
-        mbar_wait(&sm.ks_full[kb], (tcount >> 1) & 1, p.err, 16, &sm.abort);
-#pragma unroll
-        for (int jj = 0; jj < MBW; ++jj) {
-            const int mb = hh * MBW + jj;
-            if (mb < nb) ksv[jj] = sm.ksb[kb][mb][(32 * q4 + lane) * ks_st + ks_off];
         }
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&sm.s_empty[sb]);
-            mbar_arrive(&sm.ks_empty[kb]);
-        }
+        if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
 
         // ---- scores x = S * q_scale * scale * log2(e) * k_scale; tile row maxima ----
         float qsc[NR];
@@ -1200,24 +1189,6 @@ pa_status make_cache_map(CUtensorMap* map, const void* base, uint64_t inner, uin
     return PA_OK;
 }
 
-// 2-D float view of PA_BSND key scales [num_blocks*128 rows][NKV] with a box
-// of 4 heads x 128 rows (NKV % 4 == 0).
-pa_status make_kscale_map(CUtensorMap* map, const float* base, int NKV, uint64_t rows)
-{
-    auto enc = tensor_map_encoder();
-    PA_REQUIRE(enc != nullptr, PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(NKV), rows};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(NKV) * 4};
-    cuuint32_t box[2] = {4, static_cast<cuuint32_t>(kBS)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    PA_REQUIRE(r == CUDA_SUCCESS, PA_ERR_CUDA, "cuTensorMapEncodeTiled (key scales) failed (%d)",
-               static_cast<int>(r));
-    return PA_OK;
-}
-
 struct Plan {
     int S2T, NR, NRC, R, G, grid;
     int64_t U;
@@ -1253,7 +1224,7 @@ pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_confi
 }
 
 template <int NR, int S2T>
-pa_status launch(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tks,
+pa_status launch(const CUtensorMap& tk, const CUtensorMap& tv,
                  const DecodeParams& prm, cudaStream_t st)
 {
     const size_t smem = sizeof(DecodeSmem<NR, S2T>) + 1024;
@@ -1275,11 +1246,11 @@ pa_status launch(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap
         at[0].val.programmaticStreamSerializationAllowed = 1;
         lc.attrs = at;
         lc.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&lc, decode_kernel<NR, S2T>, tk, tv, tks, prm);
+        const cudaError_t e = cudaLaunchKernelEx(&lc, decode_kernel<NR, S2T>, tk, tv, prm);
         PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode: launch: %s", cudaGetErrorString(e));
         return PA_OK;
     }
-    decode_kernel<NR, S2T><<<prm.grid, kThreads, smem, st>>>(tk, tv, tks, prm);
+    decode_kernel<NR, S2T><<<prm.grid, kThreads, smem, st>>>(tk, tv, prm);
     return check_launch("pa_fp8_decode");
 }
 
@@ -1292,7 +1263,6 @@ struct SmemLayoutChecks {
     static_assert(offsetof(S, ring) % 1024 == 0, "ring alignment");
     static_assert(offsetof(S, qb) % 1024 == 0, "Q operand alignment");
     static_assert(offsetof(S, pbuf) % 128 == 0, "P operand alignment");
-    static_assert(offsetof(S, ksb) % 128 == 0, "key-scale buffer alignment");
     static_assert(offsetof(S, vsc) % 16 == 0, "vsc alignment");
     static_assert(offsetof(S, wst) % 16 == 0, "wst alignment");
     static_assert(sizeof(S) + 1024 <= 232448, "decode shared memory over budget");
@@ -1340,15 +1310,9 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     PA_REQUIRE(layout == PA_LAYOUT_BSND || layout == PA_LAYOUT_BNBD, PA_ERR_INVALID,
                "pa_fp8_decode: unknown layout %d", layout);
     PA_REQUIRE(aligned(q, 16) && aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(v_scale, 16) &&
-                   aligned(k_scale, 16) && aligned(out, 16),
+                   aligned(k_scale, 4) && aligned(out, 16),
                PA_ERR_INVALID,
-               "pa_fp8_decode: misaligned pointer (q, caches, key/value scales and out need 16 bytes)");
-    int ks_mode = KS_CONTIG;
-    if (layout == PA_LAYOUT_BSND) {
-        PA_REQUIRE(NKV % 4 == 0 || NKV <= 3, PA_ERR_UNSUPPORTED,
-                   "pa_fp8_decode: PA_BSND key scales with NKV=%d (multiples of 4 and 1-3 are built)", NKV);
-        ks_mode = NKV % 4 == 0 ? KS_QUAD : KS_WHOLE;
-    }
+               "pa_fp8_decode: misaligned pointer (q, caches, v_scale and out need 16 bytes, k_scale 4)");
     const int64_t rows = num_blocks * kBS * (layout == PA_LAYOUT_BNBD ? NKV : 1);
     PA_REQUIRE(rows < (int64_t(1) << 31), PA_ERR_UNSUPPORTED, "pa_fp8_decode: cache too large for 32-bit TMA rows");
     const int64_t maxlen = static_cast<int64_t>(max_blocks_per_seq) * kBS;
@@ -1360,18 +1324,12 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     PA_REQUIRE(workspace_bytes >= pl.total, PA_ERR_WORKSPACE,
                "pa_fp8_decode: workspace %zu bytes < %zu required", workspace_bytes, pl.total);
 
-    CUtensorMap tk, tv, tks;
+    CUtensorMap tk, tv;
     const uint64_t inner = layout == PA_LAYOUT_BSND ? static_cast<uint64_t>(NKV) * kD : kD;
     st = make_cache_map(&tk, k_cache, inner, static_cast<uint64_t>(rows));
     if (st != PA_OK) return st;
     st = make_cache_map(&tv, v_cache, inner, static_cast<uint64_t>(rows));
     if (st != PA_OK) return st;
-    if (ks_mode == KS_QUAD) {
-        st = make_kscale_map(&tks, k_scale, NKV, static_cast<uint64_t>(num_blocks) * kBS);
-        if (st != PA_OK) return st;
-    } else {
-        tks = tk;  // not read by the kernel in this mode
-    }
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeParams prm;
@@ -1397,19 +1355,18 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     prm.layout = layout;
     prm.grid = pl.grid;
     prm.maxlen = static_cast<int>(maxlen);
-    prm.ks_mode = ks_mode;
     prm.sscale = softmax_scale * 1.4426950408889634f;
     prm.overlap = (cfg && cfg->overlap_prologue) ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pl.NR == 16) {
-        if (pl.S2T == 128) return launch<16, 128>(tk, tv, tks, prm, s);
-        if (pl.S2T == 256) return launch<16, 256>(tk, tv, tks, prm, s);
-        return launch<16, 512>(tk, tv, tks, prm, s);
+        if (pl.S2T == 128) return launch<16, 128>(tk, tv, prm, s);
+        if (pl.S2T == 256) return launch<16, 256>(tk, tv, prm, s);
+        return launch<16, 512>(tk, tv, prm, s);
     }
-    if (pl.S2T == 128) return launch<32, 128>(tk, tv, tks, prm, s);
-    if (pl.S2T == 256) return launch<32, 256>(tk, tv, tks, prm, s);
-    return launch<32, 512>(tk, tv, tks, prm, s);
+    if (pl.S2T == 128) return launch<32, 128>(tk, tv, prm, s);
+    if (pl.S2T == 256) return launch<32, 256>(tk, tv, prm, s);
+    return launch<32, 512>(tk, tv, prm, s);
 }
 
 // ---------------------------------------------------------------------------

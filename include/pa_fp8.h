@@ -152,11 +152,10 @@ PA_API const char* pa_last_error(void);
  *                this workspace (e.g. cudaMemset once after allocation);
  *                every call leaves them zero again. Calls that share a
  *                workspace must not overlap in time (same stream is fine).
- * Limits: B <= 1024; PA_BSND key scales need NKV a multiple of 4 or NKV <= 3;
- * s2_tile (cfg) 128, 256 or 512 (default 512). Other values return
- * PA_ERR_UNSUPPORTED before anything is enqueued.
- * Alignment: q, k_cache, k_scale, v_cache, v_scale and out 16-byte aligned
- * (PA_ERR_INVALID otherwise).
+ * Limits: B <= 1024; s2_tile (cfg) 128, 256 or 512 (default 512). Other
+ * values return PA_ERR_UNSUPPORTED before anything is enqueued.
+ * Alignment: q, k_cache, v_cache, v_scale and out 16-byte aligned, k_scale
+ * 4-byte aligned (PA_ERR_INVALID otherwise).
  * Errors on the device: every wait inside the kernel is bounded (about 2 s);
  * a wait that gives up sets a non-zero word at the start of the workspace
  * and the output is undefined. The call itself has returned PA_OK by then:

@@ -122,6 +122,16 @@ def test_decode_s1_two_rows_per_head(torch_cuda):
     _run_case(case, num_ctas=4)
 
 
+@pytest.mark.parametrize("layout", [workloads.LAYOUT_BSND, workloads.LAYOUT_BNBD])
+@pytest.mark.parametrize("nkv", [3, 5, 6, 7])
+def test_decode_kv_head_counts(torch_cuda, nkv, layout):
+    """Kv head counts that are not multiples of 4 (every head's key scale is
+    read per token, whatever the PA_BSND row width)."""
+    case = workloads.custom("nkv%d" % nkv, 5, 1, 2 * nkv, nkv, [3, 130, 700, 1025, 2049],
+                            layout=layout)
+    _run_case(case)
+
+
 def test_decode_large_group(torch_cuda):
     """64 query rows per kv head: two 32-row chunks per (batch, kv head)."""
     case = workloads.custom("biggroup", 2, 1, 64, 1, [300, 900], s2_tile=256)
