@@ -60,7 +60,7 @@ constexpr int kKProducerWarp = kNCW;        // K blocks, key scales, per-unit he
 constexpr int kVProducerWarp = kNCW + 1;    // V blocks
 constexpr int kMmaWarp = kNCW + 2;          // tensor memory owner; issues MM1
 constexpr int kThreads = (kNCW + 3) * 32;
-constexpr int kKSlots = 5;                   // K ring; the V ring takes the other slots
+constexpr int kKSlots = 4;                   // K ring (one s2 tile of 512); the V ring takes the other slots
 constexpr int kSlotBytes = kBS * kD;         // one 128-token block of one head
 constexpr int kMaxB = 1024;
 // Work-balancing cost model in token units: a unit (batch, kv head, row
@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NSLOT = DecodeSmem<NR, S2T>::NSLOT;
     constexpr int NK = kKSlots, NV = NSLOT - kKSlots;
     static_assert(NV >= NBT, "the V ring must hold one tile");
+    static_assert(NK >= NBT, "the K ring must hold one tile (the MM1 slot walk wraps once per tile)");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
