@@ -148,14 +148,14 @@ def _in_dtype(t):
 _configs = {}
 
 
-def _config(s2_tile: int, num_ctas: int, overlap_prologue: bool = False):
-    key = (s2_tile, num_ctas, bool(overlap_prologue))
+def _config(s2_tile: int, num_ctas: int, overlap_prologue=0):
+    key = (s2_tile, num_ctas, int(overlap_prologue))
     c = _configs.get(key)
     if c is None:
         c = pa_decode_config()
         c.s2_tile = s2_tile
         c.num_ctas = num_ctas
-        c.overlap_prologue = 1 if overlap_prologue else 0
+        c.overlap_prologue = int(overlap_prologue)
         _configs[key] = c
     return c
 
@@ -186,7 +186,7 @@ class DecodeWorkspace:
 def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs, out, *,
            S1: int = 1, layout: int = LAYOUT_BSND, s2_tile: int = 512, softmax_scale=None,
            workspace: DecodeWorkspace | None = None, num_ctas: int = 0, stream=None,
-           overlap_prologue: bool = False):
+           overlap_prologue: int = 0):
     """Paged FP8 decode attention (in place into ``out``).
 
     q [B*S1, NQ, D] E4M3 (uint8 or float8_e4m3fn), q_scale float32 [B*S1, NQ],
@@ -194,9 +194,11 @@ def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_s
     [NB, NKV, BS, D] for BNBD), k_scale float32 (cache shape without D),
     v_scale float32 [B, NKV, D], block_table int32 [B, max_blocks],
     kv_act_seqs int32 [B], out bfloat16 [B*S1, NQ, D].
-    overlap_prologue: let the kernel's prologue overlap the preceding kernel
-    in the stream (that kernel must not write kv_act_seqs, block_table, q,
-    q_scale or v_scale); see pa_decode_config.overlap_prologue.
+    overlap_prologue: 1 (or True) lets the kernel's prologue overlap the
+    preceding kernel in the stream (that kernel must not write kv_act_seqs,
+    block_table, q, q_scale or v_scale); 2 also lets it load the cache blocks
+    below each sequence's S1 newest positions early (that kernel must not
+    write the cache there); see pa_decode_config.overlap_prologue.
     """
     torch = _torch()
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):

@@ -157,7 +157,7 @@ struct DecodeParams {
     int* err;
     int64_t num_blocks;
     int B, S1, NQ, NKV, G, R, NRC, max_blocks, layout, grid, maxlen;
-    int overlap;   // launched with programmatic stream serialisation
+    int overlap;   // programmatic stream serialisation: 0 off, 1 prologue, 2 also older cache blocks
     float sscale;  // softmax_scale * log2(e)
 };
 
@@ -512,13 +512,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool hdr_done = false;
             if (!waited) {
                 // inputs not written by the preceding kernel may be read before
-                // it ends; the KV cache and its scales only after
+                // it ends; the KV cache only after (with overlap 2, only the
+                // blocks that hold one of a sequence's S1 newest positions)
                 if (need_hdr && p.overlap) {
                     issue_header(b, n2, rc);
                     hdr_done = true;
                 }
-                grid_dependency_wait();
-                waited = true;
+                if (p.overlap < 2) {
+                    grid_dependency_wait();
+                    waited = true;
+                }
             }
             const int nb = min(NBT, (len - t * S2T + kBS - 1) / kBS);
             // V blocks of a tile are requested only after its K blocks: K is
@@ -543,6 +546,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < NBT; ++j) {
                 if (j >= nb) break;
                 const int sl = base + slot;
+                if (!waited && t * S2T + (j + 1) * kBS > len - p.S1) {
+                    grid_dependency_wait();
+                    waited = true;
+                }
                 mbar_wait(&sm.empty_bar[sl], ph ^ 1, p.err, 4, &sm.abort);
                 int blk = id0[j];
                 if (blk < 0 || blk >= p.num_blocks) blk = 0;
@@ -1210,6 +1217,8 @@ pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_confi
                "pa_fp8_decode: s2_tile %d is not a multiple of block_size 128", pl->S2T);
     PA_REQUIRE(pl->S2T == 128 || pl->S2T == 256 || pl->S2T == 512, PA_ERR_UNSUPPORTED,
                "pa_fp8_decode: s2_tile %d (128, 256 and 512 are built)", pl->S2T);
+    PA_REQUIRE(!cfg || (cfg->overlap_prologue >= 0 && cfg->overlap_prologue <= 2), PA_ERR_INVALID,
+               "pa_fp8_decode: overlap_prologue %d (0, 1 or 2)", cfg ? cfg->overlap_prologue : 0);
     pl->G = NQ / NKV;
     pl->R = S1 * pl->G;
     pl->NR = pl->R <= 16 ? 16 : 32;
@@ -1357,7 +1366,7 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     prm.grid = pl.grid;
     prm.maxlen = static_cast<int>(maxlen);
     prm.sscale = softmax_scale * 1.4426950408889634f;
-    prm.overlap = (cfg && cfg->overlap_prologue) ? 1 : 0;
+    prm.overlap = cfg ? cfg->overlap_prologue : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pl.NR == 16) {

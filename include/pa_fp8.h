@@ -98,7 +98,16 @@ typedef struct pa_decode_config {
                       guarantees the preceding kernel does not write them --
                       and waits for it before touching k_cache, v_cache,
                       k_scale, out and the workspace. 0 (default): ordinary
-                      stream order.                                           */
+                      stream order.
+                      2: as 1, and the K/V cache blocks that hold only
+                      positions below kv_act_seqs[b] - S1 of their sequence
+                      are also loaded (and MM1 run on them) before the
+                      preceding kernel has finished; the caller guarantees
+                      that kernel writes no K/V cache entry there (it may
+                      write each sequence's S1 newest positions, as the
+                      append of a decode step does). Key scales, the newest
+                      blocks, out and the workspace still wait for it.
+                      Other values return PA_ERR_INVALID.                     */
     int reserved[5];
 } pa_decode_config;
 

@@ -87,6 +87,11 @@ def test_decode_rejects_bad_arguments_without_launching(L):
     cfg.s2_tile = 1024
     assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 128, ctypes.byref(cfg),
                                           ctypes.byref(n)) == 5
+    cfg.s2_tile = 512
+    cfg.overlap_prologue = 3
+    assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 128, ctypes.byref(cfg),
+                                          ctypes.byref(n)) == 2
+    assert b"overlap_prologue" in L.pa_last_error()
     P = ctypes.c_void_p
     fake = P(256)
     st = L.pa_fp8_decode(fake, fake, None, fake, fake, fake, fake, fake, fake, 16, 1, 96, 8, 128,

@@ -203,11 +203,13 @@ def test_quant_scatter_head_sizes(torch_cuda, D, dtype, overlap):
     assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
 
 
-def test_step_chain_overlap_in_graph(torch_cuda):
-    """decode -> append -> decode with overlap_prologue on all three launches,
-    eagerly and captured in a CUDA graph: the append's stores wait for the
-    first decode, the second decode sees the appended token, both outputs and
-    the cache match the oracle."""
+@pytest.mark.parametrize("mode", [1, 2])
+def test_step_chain_overlap_in_graph(torch_cuda, mode):
+    """decode -> append -> decode with programmatic serialisation on all three
+    launches (decode mode 1: prologue only; mode 2: also the cache blocks
+    below each sequence's newest position), eagerly and captured in a CUDA
+    graph: the append's stores wait for the first decode, the second decode
+    sees the appended token, both outputs and the cache match the oracle."""
     torch = torch_cuda
     import fp8_paged_kv_block_gb300 as pa
     case = workloads.custom("chain", 6, 1, 24, 2, [1, 127, 700, 1300, 2049, 3000], max_blocks=25)
@@ -242,7 +244,7 @@ def test_step_chain_overlap_in_graph(torch_cuda):
             pa.decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale,
                       dev["block_table"], act, out, S1=case.S1, layout=case.layout,
                       s2_tile=case.s2_tile, softmax_scale=case.softmax_scale, workspace=ws,
-                      overlap_prologue=True)
+                      overlap_prologue=mode)
 
     def check():
         torch.cuda.synchronize()
@@ -253,11 +255,16 @@ def test_step_chain_overlap_in_graph(torch_cuda):
         assert np.array_equal(c.v_cache.cpu().numpy(), inp["vc"])
         assert np.array_equal(c.k_scale.cpu().numpy(), inp["ksc"])
 
+    tick = torch.zeros(1, device="cuda")
+
     def restore():
         for t, s in zip((c.k_cache, c.v_cache, c.k_scale), snap):
             t.copy_(s)
         o0.fill_(float("nan"))
         o1.fill_(float("nan"))
+        # the first decode may read old cache blocks while its predecessor
+        # runs (mode 2): that predecessor is a kernel that writes no cache
+        tick.add_(1)
 
     chain()
     check()

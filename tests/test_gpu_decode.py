@@ -239,3 +239,52 @@ def test_overlap_prologue_back_to_back_and_in_graph(torch_cuda):
     torch.cuda.synchronize()
     assert ws.error_flags() == 0
     H.compare_bf16(H.to_u16(outs[2]), ref)
+
+
+def test_overlap_mode2_back_to_back_and_in_graph(torch_cuda):
+    """overlap_prologue=2: cache blocks below each sequence's newest position
+    are loaded before the preceding kernel has finished. Back-to-back decodes
+    (which write no cache) on one workspace, eagerly and in a CUDA graph behind
+    a kernel that writes no cache, match the oracle."""
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    case = workloads.custom("overlap2", 6, 1, 24, 2, [1, 127, 700, 1300, 2049, 3000], max_blocks=25)
+    inp = H.oracle_inputs(case)
+    dev = H.device_inputs(case)
+    ref = H.oracle_decode(case, inp)
+    c = dev["cache"]
+    ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile)
+    outs = [torch.full((case.B * case.S1, case.NQ, case.D), float("nan"), dtype=torch.bfloat16,
+                       device="cuda") for _ in range(3)]
+
+    def run(out):
+        pa.decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale,
+                  dev["block_table"], dev["act"], out, S1=case.S1, layout=case.layout,
+                  s2_tile=case.s2_tile, softmax_scale=case.softmax_scale, workspace=ws,
+                  overlap_prologue=2)
+
+    torch.cuda.synchronize()
+    run(outs[0])
+    run(outs[1])
+    torch.cuda.synchronize()
+    assert ws.error_flags() == 0
+    for o in outs[:2]:
+        H.compare_bf16(H.to_u16(o), ref)
+    tick = torch.zeros(1, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tick.add_(1)
+        run(outs[2])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    outs[2].fill_(float("nan"))
+    with torch.cuda.graph(g):
+        tick.add_(1)
+        for _ in range(3):
+            run(outs[2])
+    g.replay()
+    torch.cuda.synchronize()
+    assert ws.error_flags() == 0
+    H.compare_bf16(H.to_u16(outs[2]), ref)
