@@ -687,12 +687,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rho = NR == 16 ? (lane >> 1) : lane;   // query row whose reductions this lane holds
     const bool rep = NR == 32 || (lane & 1) == 0;    // lane that publishes row rho
 
-    // out and the workspace are written only after the preceding kernel ended
-    grid_dependency_wait();
-    // sequences of length 0 produce zero rows (no tile ever covers them)
-    for (int b = cta; b < p.B; b += p.grid)
-        if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
-
     int vslot = 0;
     uint32_t vph = 0;
     int hcount = 0, tcount = 0, hs = 0, nrows = 0;
@@ -774,13 +768,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ksn[jj] = 0.f;
         idn[jj] = -1;
     }
+    // block ids (not written by the preceding kernel) before its end; key
+    // scales, out and the workspace only after it
+    int id0[MBW];
     if (!pos_eq(start, end)) {
-        int id0[MBW];
         tile_ids(start, id0);
-        tile_ks(start, id0, ksn);
         const Pos y2 = pos_next<S2T>(sm.slen, sm.bpre, p.B, start, W);
         if (!pos_eq(y2, end)) tile_ids(y2, idn);
     }
+    grid_dependency_wait();
+    if (!pos_eq(start, end)) tile_ks(start, id0, ksn);
+    // sequences of length 0 produce zero rows (no tile ever covers them)
+    for (int b = cta; b < p.B; b += p.grid)
+        if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
 
     for (Pos x = start; !pos_eq(x, end);) {
         const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
