@@ -106,7 +106,7 @@ struct __align__(1024) DecodeSmemT {
     // key scales of one tile's blocks, double-buffered by tile parity
     alignas(16) float vsc[2][kD];
     alignas(16) float qs[2][32];
-    float red[2][kNCW][32];     // per-warp row maxima, double-buffered by tile
+    alignas(16) float red[2][32][kNCW];   // per-warp row maxima (row-major), double-buffered by tile
     float redl[kNCW][32];       // per-warp row sums at unit end
     alignas(16) float wst[kNCW][4][32];   // per-warp copies of row values
     alignas(16) float wfold[2][kNCW][2][32];   // per-warp fold weights c1, c2 by tile parity
@@ -231,6 +231,13 @@ __device__ __forceinline__ int cta_of(int64_t s, int64_t Ctot, int grid)
 {
     const int64_t c = (s * grid) / Ctot;
     return c >= grid ? grid - 1 : static_cast<int>(c);
+}
+
+// kv head of unit index i (i = n2 * NRC + row chunk); one chunk per head is
+// the common case and needs no division
+__device__ __forceinline__ int head_of(const DecodeParams& p, int i)
+{
+    return p.NRC == 1 ? i : i / p.NRC;
 }
 
 __device__ __forceinline__ int64_t q_row(const DecodeParams& p, int b, int n2, int r)
@@ -506,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 x1 = pos_next<S2T>(sm.slen, sm.bpre, p.B, nx, W);
                 load_ids(x1, id2);
             }
-            const int b = x.b, n2 = x.i / p.NRC, rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
+            const int b = x.b, n2 = head_of(p, x.i), rc = x.i - n2 * p.NRC, t = x.t;
             const int len = sm.slen[b];
             const bool need_hdr = isK && (first || t == 0);
             bool hdr_done = false;
@@ -611,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool first = true;
         for (Pos x = start; !pos_eq(x, end);) {
             const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
-            const int rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
+            const int rc = x.i - head_of(p, x.i) * p.NRC, t = x.t;
             const int len = sm.slen[x.b];
             const int valid = min(S2T, len - t * S2T);
             const int nb = (valid + kBS - 1) / kBS;
@@ -741,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // current tile is processed and no copy engine or shared memory is used.
     const int ktok = 32 * q4 + lane;
     auto tile_ids = [&](const Pos& y, int (&ids)[MBW]) {
-        const int nby = min(NBT, (sm.slen[y.b] - y.t * S2T + kBS - 1) / kBS);
+        const int nby = min(NBT, (sm.slen[y.b] - y.t * S2T + kBS - 1) / kBS);   // y.b < B here
         const int* row = p.block_table + static_cast<int64_t>(y.b) * p.max_blocks + y.t * NBT;
 #pragma unroll
         for (int jj = 0; jj < MBW; ++jj) {
@@ -750,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     };
     auto tile_ks = [&](const Pos& y, const int (&ids)[MBW], float (&dst)[MBW]) {
-        const int n2y = y.i / p.NRC;
+        const int n2y = head_of(p, y.i);
 #pragma unroll
         for (int jj = 0; jj < MBW; ++jj) {
             int blk = ids[jj];
@@ -768,13 +775,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         ksn[jj] = 0.f;
         idn[jj] = -1;
     }
+    // The walk is carried in registers: the current tile, the next two, and
+    // their sequence lengths (a tile's successor needs only its own length).
+    auto advance = [&](Pos y, int leny, int& lnext) {
+        if (++y.t < tiles_of<S2T>(leny)) {
+            lnext = leny;
+            return y;
+        }
+        y.t = 0;
+        if (++y.i < W) {
+            lnext = leny;
+            return y;
+        }
+        y.i = 0;
+        y.b = next_nonempty(sm.bpre, y.b + 1, p.B);
+        lnext = y.b < p.B ? sm.slen[y.b] : 0;
+        return y;
+    };
+    int lenx = pos_eq(start, end) ? 0 : sm.slen[start.b];
+    int len1 = 0, len2 = 0;
+    Pos x1 = end, x2 = end;
+    if (!pos_eq(start, end)) x1 = advance(start, lenx, len1);
+    if (!pos_eq(x1, end)) x2 = advance(x1, len1, len2);
     // block ids (not written by the preceding kernel) before its end; key
     // scales, out and the workspace only after it
     int id0[MBW];
     if (!pos_eq(start, end)) {
         tile_ids(start, id0);
-        const Pos y2 = pos_next<S2T>(sm.slen, sm.bpre, p.B, start, W);
-        if (!pos_eq(y2, end)) tile_ids(y2, idn);
+        if (!pos_eq(x1, end)) tile_ids(x1, idn);
     }
     grid_dependency_wait();
     if (!pos_eq(start, end)) tile_ks(start, id0, ksn);
@@ -783,9 +811,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
 
     for (Pos x = start; !pos_eq(x, end);) {
-        const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
-        const int b = x.b, n2 = x.i / p.NRC, rc = x.i - (x.i / p.NRC) * p.NRC, t = x.t;
-        const int len = sm.slen[b];
+        const Pos nx = x1;
+        const int b = x.b, n2 = head_of(p, x.i), rc = x.i - n2 * p.NRC, t = x.t;
+        const int len = lenx;
         const int T = tiles_of<S2T>(len);
 
         if (first || t == 0) {
@@ -793,6 +821,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
             nrows = min(p.R - rc * NR, NR);
             if (warp == 0 && lane < NR) sm.orow[hcount & 1][lane] = q_row(p, b, n2, rc * NR + lane);
+            // this warp's copy of q_scale * softmax_scale * log2(e) per row (0
+            // past the chunk's rows); the slot holds the row sums at unit end
+            if (lane < NR) sm.wst[warp][3][lane] = lane < nrows ? sm.qs[hs][lane] * p.sscale : 0.f;
+            __syncwarp();
 #pragma unroll
             for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
 #pragma unroll
@@ -810,9 +842,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jj = 0; jj < MBW; ++jj) ksv[jj] = ksn[jj];
         if (!pos_eq(nx, end)) {
             tile_ks(nx, idn, ksn);
-            const Pos nnx = pos_next<S2T>(sm.slen, sm.bpre, p.B, nx, W);
-            if (!pos_eq(nnx, end)) tile_ids(nnx, idn);
+            if (!pos_eq(x2, end)) tile_ids(x2, idn);
         }
+        // the walk moves on by one tile
+        lenx = len1;
+        x1 = x2;
+        len1 = len2;
+        if (!pos_eq(x2, end)) x2 = advance(x2, len2, len2);
 
         // ---- S^T of this warp's blocks and their key scales ----
         mbar_wait(&sm.s_full[sb], (tcount / NSB) & 1, p.err, 256, &sm.abort);
@@ -831,7 +867,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- scores x = S * q_scale * scale * log2(e) * k_scale; tile row maxima ----
         float qsc[NR];
 #pragma unroll
-        for (int r = 0; r < NR; ++r) qsc[r] = r < nrows ? sm.qs[hs][r] * p.sscale : 0.f;
+        for (int r4 = 0; r4 < NR / 4; ++r4) {
+            const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
+            qsc[4 * r4 + 0] = q4v.x;
+            qsc[4 * r4 + 1] = q4v.y;
+            qsc[4 * r4 + 2] = q4v.z;
+            qsc[4 * r4 + 3] = q4v.w;
+        }
         float mloc[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) mloc[r] = -INFINITY;
@@ -850,11 +892,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float wmax = lane_reduce<NR, true>(mloc, lane);
         const int rb = tcount & 1;
-        if (rep) sm.red[rb][warp][rho] = wmax;
+        if (rep) sm.red[rb][rho][warp] = wmax;
         named_bar_sync(1, kNCW * 32);
-        float mt = sm.red[rb][0][rho];
-#pragma unroll
-        for (int w = 1; w < kNCW; ++w) mt = fmaxf(mt, sm.red[rb][w][rho]);
+        float mt;
+        {
+            const float4 a = *reinterpret_cast<const float4*>(&sm.red[rb][rho][0]);
+            const float4 c = *reinterpret_cast<const float4*>(&sm.red[rb][rho][4]);
+            mt = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(c.x, c.y), fmaxf(c.z, c.w)));
+        }
         {
             const float Mn = fmaxf(Mref, mt);
             const float c1 = ex2(Mref - Mn), c2 = ex2(mt - Mn);
