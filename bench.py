@@ -54,8 +54,8 @@ FALLBACK_HBM_GBS = 6800.0
 OVERLAP_DECODE = 2
 OVERLAP_APPEND = True
 
-DECODE_TRAFFIC = {"sources_sha1": "43f1f7e848619fc8c05692c513faf4c137f58c82",
-                  "bytes_per_launch": 57873408 + 90880}
+DECODE_TRAFFIC = {"sources_sha1": "16b8f8007852e09fdafb8ca5185c7fe1af22db69",
+                  "bytes_per_launch": 57871360 + 85248}
 
 
 def parse_args():
