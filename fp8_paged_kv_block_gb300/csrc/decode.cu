@@ -299,16 +299,40 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v)
     }
 }
 
-template <int NSLOT>
+// Slot and phase parity of the j-th block (j < NBT) after (slot, ph) in a ring
+// of NSLOT; a ring that holds a tile wraps at most once.
+template <int NSLOT, int NBT>
 __device__ __forceinline__ int ring_slot(int slot, uint32_t ph, int j, uint32_t* par)
 {
-    int s = slot + j;
-    *par = ph;
-    if (s >= NSLOT) {
-        s -= NSLOT;
-        *par ^= 1u;
+    if constexpr (NBT <= NSLOT) {
+        int s = slot + j;
+        *par = ph;
+        if (s >= NSLOT) {
+            s -= NSLOT;
+            *par ^= 1u;
+        }
+        return s;
+    } else {
+        const int k = slot + j;
+        *par = ph ^ static_cast<uint32_t>((k / NSLOT) & 1);
+        return k % NSLOT;
     }
-    return s;
+}
+
+// Advance (slot, ph) by n <= NBT blocks in a ring of NSLOT.
+template <int NSLOT, int NBT>
+__device__ __forceinline__ void ring_advance(int& slot, uint32_t& ph, int n)
+{
+    slot += n;
+    if constexpr (NBT <= NSLOT) {
+        if (slot >= NSLOT) {
+            slot -= NSLOT;
+            ph ^= 1u;
+        }
+    } else {
+        ph ^= static_cast<uint32_t>((slot / NSLOT) & 1);
+        slot %= NSLOT;
+    }
 }
 
 template <int NR, int S2T>
@@ -325,9 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int HR = NR / 2;                   // O^T columns (query rows) per consumer warp
     constexpr int TC = S2T + kC0;
     constexpr int NSLOT = DecodeSmem<NR, S2T>::NSLOT;
-    constexpr int NK = kKSlots, NV = NSLOT - kKSlots;
+    // K ring: one tile up to s2 tile 512; with longer tiles the V ring takes a
+    // whole tile (MM2 needs every block of the tile) and K the rest
+    constexpr int NK = NBT <= kKSlots ? kKSlots : NSLOT - NBT, NV = NSLOT - NK;
     static_assert(NV >= NBT, "the V ring must hold one tile");
-    static_assert(NK >= NBT, "the K ring must hold one tile (the MM1 slot walk wraps once per tile)");
+    static_assert(NK >= 1, "no K ring slot left");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -517,11 +543,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int len = sm.slen[b];
             const bool need_hdr = isK && (first || t == 0);
             bool hdr_done = false;
+            // MM1 needs the header; when the K ring is shorter than a tile the
+            // tile's later K blocks wait for MM1 on its first ones, so the
+            // header goes out before them
+            if (need_hdr && NK < NBT) {
+                issue_header(b, n2, rc);
+                hdr_done = true;
+            }
             if (!waited) {
                 // inputs not written by the preceding kernel may be read before
                 // it ends; the KV cache only after (with overlap 2, only the
                 // blocks that hold one of a sequence's S1 newest positions)
-                if (need_hdr && p.overlap) {
+                if (need_hdr && !hdr_done && p.overlap) {
                     issue_header(b, n2, rc);
                     hdr_done = true;
                 }
@@ -650,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t qd = smem_desc(smem_u32(&sm.qb[hs][0][0]), 16, 1024, kSmem128BSwizzle);
                     for (int j = 0; j < nb; ++j) {
                         uint32_t par;
-                        const int s = ring_slot<NK>(slot, ph, j, &par);
+                        const int s = ring_slot<NK, NBT>(slot, ph, j, &par);
                         mbar_wait(&sm.full_bar[s], par, p.err, 16, &sm.abort);
                         tc_fence_after();
                         const uint64_t kd = smem_desc(smem_u32(sm.ring[s]), 16, 1024, kSmem128BSwizzle);
@@ -663,11 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (t == tiles_of<S2T>(len) - 1 || pos_eq(nx, end)) umma_commit(&sm.hdr_empty[hs]);
                 }
                 __syncwarp();
-                slot += nb;
-                if (slot >= NK) {
-                    slot -= NK;
-                    ph ^= 1;
-                }
+                ring_advance<NK, NBT>(slot, ph, nb);
             }
             first = false;
             ++tcount;
@@ -956,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < MBW; ++jj) {
                 const int mb = hh * MBW + jj;
-                vsl[jj] = NK + ring_slot<NV>(vslot, vph, mb, &vpar[jj]);
+                vsl[jj] = NK + ring_slot<NV, NBT>(vslot, vph, mb, &vpar[jj]);
                 if (mb < nb && (mb + 1) * kBS > valid) {
                     mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort);
                     const int row = 32 * q4 + lane;
@@ -1004,11 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Lp[4 * r4 + 3] = Lp[4 * r4 + 3] * a4.w + ls[4 * r4 + 3] * b4.w;
         }
         pend = tcount;
-        vslot += nb;
-        if (vslot >= NV) {
-            vslot -= NV;
-            vph ^= 1;
-        }
+        ring_advance<NV, NBT>(vslot, vph, nb);
         ++tcount;
 
         if (t == T - 1 || pos_eq(nx, end)) {
@@ -1260,13 +1285,17 @@ pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_confi
     pl->S2T = (cfg && cfg->s2_tile) ? cfg->s2_tile : 512;
     PA_REQUIRE(pl->S2T > 0 && pl->S2T % kBS == 0, PA_ERR_INVALID,
                "pa_fp8_decode: s2_tile %d is not a multiple of block_size 128", pl->S2T);
-    PA_REQUIRE(pl->S2T == 128 || pl->S2T == 256 || pl->S2T == 512, PA_ERR_UNSUPPORTED,
-               "pa_fp8_decode: s2_tile %d (128, 256 and 512 are built)", pl->S2T);
+    PA_REQUIRE(pl->S2T == 128 || pl->S2T == 256 || pl->S2T == 512 || pl->S2T == 1024, PA_ERR_UNSUPPORTED,
+               "pa_fp8_decode: s2_tile %d (128, 256, 512 and 1024 are built)", pl->S2T);
     PA_REQUIRE(!cfg || (cfg->overlap_prologue >= 0 && cfg->overlap_prologue <= 2), PA_ERR_INVALID,
                "pa_fp8_decode: overlap_prologue %d (0, 1 or 2)", cfg ? cfg->overlap_prologue : 0);
     pl->G = NQ / NKV;
     pl->R = S1 * pl->G;
     pl->NR = pl->R <= 16 ? 16 : 32;
+    // 1024-token tiles: three S^T buffers of 8 x 16 columns fit the tensor
+    // memory next to O^T, 8 x 32 do not
+    PA_REQUIRE(pl->S2T < 1024 || pl->NR == 16, PA_ERR_UNSUPPORTED,
+               "pa_fp8_decode: s2_tile 1024 needs at most 16 query rows per kv head (S1 x group = %d)", pl->R);
     pl->NRC = (pl->R + pl->NR - 1) / pl->NR;
     pl->U = static_cast<int64_t>(B) * NKV * pl->NRC;
     int grid = (cfg && cfg->num_ctas > 0) ? cfg->num_ctas : device_sm_count();
@@ -1324,6 +1353,7 @@ struct SmemLayoutChecks {
     static constexpr bool ok = true;
 };
 static_assert(SmemLayoutChecks<16, 128>::ok && SmemLayoutChecks<16, 256>::ok && SmemLayoutChecks<16, 512>::ok &&
+                  SmemLayoutChecks<16, 1024>::ok &&
                   SmemLayoutChecks<32, 128>::ok && SmemLayoutChecks<32, 256>::ok && SmemLayoutChecks<32, 512>::ok,
               "shared memory layout");
 
@@ -1417,7 +1447,8 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     if (pl.NR == 16) {
         if (pl.S2T == 128) return launch<16, 128>(tk, tv, prm, s);
         if (pl.S2T == 256) return launch<16, 256>(tk, tv, prm, s);
-        return launch<16, 512>(tk, tv, prm, s);
+        if (pl.S2T == 512) return launch<16, 512>(tk, tv, prm, s);
+        return launch<16, 1024>(tk, tv, prm, s);
     }
     if (pl.S2T == 128) return launch<32, 128>(tk, tv, prm, s);
     if (pl.S2T == 256) return launch<32, 256>(tk, tv, prm, s);

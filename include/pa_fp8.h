@@ -86,7 +86,8 @@ typedef enum pa_index_type {
 typedef struct pa_decode_config {
     int s2_tile;   /* KV tile of the online softmax and the P-quantisation
                       group ([PA] 配置说明: s2_tile). Multiple of block_size;
-                      128, 256 or 512 are built. Default 512.                 */
+                      128, 256 and 512 are built, and 1024 (the pages' tile
+                      for long sequences) when S1 x NQ/NKV <= 16. Default 512. */
     int num_ctas;  /* persistent grid size. Default: SM count x resident
                       CTAs per SM.                                            */
     int overlap_prologue; /* 1: launch with programmatic stream serialisation
@@ -161,8 +162,9 @@ PA_API const char* pa_last_error(void);
  *                this workspace (e.g. cudaMemset once after allocation);
  *                every call leaves them zero again. Calls that share a
  *                workspace must not overlap in time (same stream is fine).
- * Limits: B <= 1024; s2_tile (cfg) 128, 256 or 512 (default 512). Other
- * values return PA_ERR_UNSUPPORTED before anything is enqueued.
+ * Limits: B <= 1024; s2_tile (cfg) 128, 256, 512 (default) or 1024 (1024
+ * needs S1 x NQ/NKV <= 16). Other values return PA_ERR_UNSUPPORTED before
+ * anything is enqueued.
  * Alignment: q, k_cache, v_cache, v_scale and out 16-byte aligned, k_scale
  * 4-byte aligned (PA_ERR_INVALID otherwise).
  * Errors on the device: every wait inside the kernel is bounded (about 2 s);

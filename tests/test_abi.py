@@ -84,10 +84,18 @@ def test_decode_rejects_bad_arguments_without_launching(L):
     cfg.s2_tile = 100
     assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 128, ctypes.byref(cfg),
                                           ctypes.byref(n)) == 2
-    cfg.s2_tile = 1024
+    cfg.s2_tile = 2048
     assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 128, ctypes.byref(cfg),
                                           ctypes.byref(n)) == 5
+    cfg.s2_tile = 1024   # built for up to 16 query rows per kv head
+    cfg.num_ctas = 152   # no device query (no GPU here)
+    assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 128, ctypes.byref(cfg),
+                                          ctypes.byref(n)) == 0
+    assert L.pa_fp8_decode_workspace_size(16, 2, 96, 8, 128, ctypes.byref(cfg),
+                                          ctypes.byref(n)) == 5
+    assert b"1024" in L.pa_last_error()
     cfg.s2_tile = 512
+    cfg.num_ctas = 0
     cfg.overlap_prologue = 3
     assert L.pa_fp8_decode_workspace_size(16, 1, 96, 8, 128, ctypes.byref(cfg),
                                           ctypes.byref(n)) == 2

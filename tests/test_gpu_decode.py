@@ -85,7 +85,7 @@ def test_cache_build_bitexact(torch_cuda, layout):
 # Decode parity
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("s2_tile", [128, 256, 512])
+@pytest.mark.parametrize("s2_tile", [128, 256, 512, 1024])
 @pytest.mark.parametrize("layout", [workloads.LAYOUT_BSND, workloads.LAYOUT_BNBD])
 def test_decode_tiny(torch_cuda, s2_tile, layout):
     _run_case(workloads.tiny(s2_tile=s2_tile, layout=layout))
@@ -288,3 +288,23 @@ def test_overlap_mode2_back_to_back_and_in_graph(torch_cuda):
     torch.cuda.synchronize()
     assert ws.error_flags() == 0
     H.compare_bf16(H.to_u16(outs[2]), ref)
+
+
+@pytest.mark.parametrize("num_ctas", [0, 5, 37])
+def test_decode_s2_tile_1024(torch_cuda, num_ctas):
+    """1024-token s2 tiles (the pages' tile for long sequences): P quantised
+    over each 1024-token tile, a K ring shorter than a tile, ragged lengths
+    across several tiles and CTA splits."""
+    case = workloads.custom("s2t1024", 6, 1, 24, 2, [1, 1023, 1025, 2100, 4096, 5000],
+                            s2_tile=1024)
+    _run_case(case, num_ctas=num_ctas)
+
+
+def test_decode_long_context_s2_tile_1024_sampled(torch_cuda):
+    """The long-context workload (kv lengths 32K-128K, K outliers) with
+    1024-token tiles, sampled rows."""
+    case = workloads.long_ctx(s2_tile=1024)
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(case.B * case.NQ, 24, replace=False))
+    batches = np.unique(rows // case.NQ)
+    _run_case(case, rows=rows, batches=batches)
