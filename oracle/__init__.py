@@ -72,6 +72,12 @@ def _load():
         lib.or_cache_quant_scatter.argtypes = [P, P, P, P, P, P, P, P, i64, i32, i32, i32,
                                                i64, i32, i32]
         lib.or_cache_quant_scatter.restype = None
+        lib.or_kvc_concat_bytes.argtypes = [i32, i32]
+        lib.or_kvc_concat_bytes.restype = i64
+        lib.or_kvc_min_head_dim.argtypes = [i32, i32]
+        lib.or_kvc_min_head_dim.restype = i64
+        lib.or_kv_compress_epilog.argtypes = [P, i64, i32, P, i64, i32, i64, i32, P, i32, i32]
+        lib.or_kv_compress_epilog.restype = None
         lib.or_pa_decode.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                      i32, i64, i32, i32, i32, f32, P, i64]
         lib.or_pa_decode.restype = ctypes.c_int
@@ -209,6 +215,30 @@ def cache_quant_scatter(key, value, key_cache, value_cache, slot_mapping,
     lib.or_cache_quant_scatter(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
                                _ptr(slot), _ptr(key_scale_cache), _ptr(vs), _ptr(tb),
                                T, H, Dk, Dv, NB, BS, layout)
+
+
+def kvc_concat_bytes(d, quant_mode):
+    """Bytes one KV-compress-epilog row writes (rope + nope codes + scales)."""
+    return int(_load().or_kvc_concat_bytes(d, quant_mode))
+
+
+def kvc_min_head_dim(d, quant_mode):
+    """Smallest cache row pitch for KV compress epilog rows of width d."""
+    return int(_load().or_kvc_min_head_dim(d, quant_mode))
+
+
+def kv_compress_epilog(x, cache, block_num, block_size, block_stride, head_dim, slot_mapping,
+                       quant_mode, round_scale):
+    """In-place KV compress epilog (modes 0/1). x: float32 [bs, d] holding BF16
+    values; cache: uint8 array of block_num * block_stride bytes."""
+    lib = _load()
+    x = _c(x, np.float32)
+    slot = _c(slot_mapping, np.int64)
+    assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"]
+    assert cache.size >= block_num * block_stride
+    bs, d = x.shape
+    lib.or_kv_compress_epilog(_ptr(x), bs, d, _ptr(cache), block_num, block_size, block_stride,
+                              head_dim, _ptr(slot), quant_mode, int(bool(round_scale)))
 
 
 # --------------------------------------------------------------------------

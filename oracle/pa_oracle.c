@@ -292,6 +292,105 @@ void or_cache_quant_scatter(const float* key, const float* value, uint8_t* key_c
 }
 
 /* ---------------------------------------------------------------------- */
+/* KV compress epilog, modes 0 and 1 ([KC] 功能说明与计算公式 场景 1 / 场景 2, */
+/* 约束说明 headDim, kvCacheCol 的源码级解读).                              */
+/* A BF16 row x[d] (d % 64 == 0, d > 64) is split into the nope part        */
+/* x[0, d-64) and the rope part x[d-64, d). The cache row (head_dim bytes)  */
+/* receives [rope as BF16, 128 B][nope as E4M3, d-64 B][one scale per group */
+/* of 64 nope values: BF16 (mode 0) or E8M0 (mode 1)]; its other bytes and  */
+/* rows whose slot is -1 or out of range are left as they are.              */
+/* ---------------------------------------------------------------------- */
+
+/* Bytes written per row. */
+int64_t or_kvc_concat_bytes(int d, int quant_mode)
+{
+    int64_t groups = (d - 64 + 63) / 64;
+    return (int64_t)(d - 64) + 64 * 2 + groups * (quant_mode == 0 ? 2 : 1);
+}
+
+/* Smallest head_dim (row pitch) the cache must have: the written bytes,
+ * rounded up to 32 for mode 0 and not rounded for mode 1. */
+int64_t or_kvc_min_head_dim(int d, int quant_mode)
+{
+    int64_t c = or_kvc_concat_bytes(d, quant_mode);
+    return quant_mode == 0 ? (c + 31) / 32 * 32 : c;
+}
+
+/* Exponent k of the E8M0 scale 2^k for a group scale s > 0: with
+ * round_scale the power of two at or above s (the scale rounded up, [KC]
+ * roundScale), without it the power of two at or below s (the exponent of
+ * s, its mantissa dropped); clamped to E8M0's finite range [-127, 127]. */
+static int e8m0_exponent(float s, int round_scale)
+{
+    int e, k;
+    frexp((double)s, &e); /* s = f * 2^e, f in [0.5, 1) */
+    k = e - 1;            /* 2^k <= s < 2^(k+1)       */
+    if (round_scale && ldexp(1.0, k) < (double)s)
+        k += 1;
+    if (k < -127)
+        k = -127;
+    if (k > 127)
+        k = 127;
+    return k;
+}
+
+/* x: the BF16 rows as their exact float values [bs][d]; cache: block_num
+ * blocks of block_stride bytes, row r of a block at r * head_dim. */
+void or_kv_compress_epilog(const float* x, int64_t bs, int d, uint8_t* cache, int64_t block_num,
+                           int block_size, int64_t block_stride, int head_dim, const int64_t* slot,
+                           int quant_mode, int round_scale)
+{
+    const int nope = d - 64;
+    const int groups = (nope + 63) / 64;
+    int64_t i;
+    for (i = 0; i < bs; ++i) {
+        const float* xr = x + i * d;
+        int64_t s = slot[i];
+        uint8_t* row;
+        int g, j;
+        if (s < 0 || s >= block_num * block_size)
+            continue;
+        row = cache + (s / block_size) * block_stride + (s % block_size) * (int64_t)head_dim;
+        for (j = 0; j < 64; ++j) { /* rope part, BF16 little-endian, first */
+            uint16_t h = or_bf16_from_float(xr[nope + j]);
+            row[2 * j] = (uint8_t)(h & 0xFF);
+            row[2 * j + 1] = (uint8_t)(h >> 8);
+        }
+        for (g = 0; g < groups; ++g) {
+            const float* xg = xr + 64 * g;
+            const int n = nope - 64 * g < 64 ? nope - 64 * g : 64;
+            uint8_t* codes = row + 128 + 64 * g;
+            float amax = 0.0f, scale;
+            for (j = 0; j < n; ++j)
+                if (fabsf(xg[j]) > amax)
+                    amax = fabsf(xg[j]);
+            scale = amax / 448.0f; /* scale_g = max|x_g| / FP8_MAX */
+            if (quant_mode == 0) {
+                uint8_t* sc = row + 128 + nope + 2 * g;
+                uint16_t h = or_bf16_from_float(scale);
+                for (j = 0; j < n; ++j)
+                    codes[j] = (scale == 0.0f) ? 0 : or_e4m3_encode(xg[j] / scale);
+                sc[0] = (uint8_t)(h & 0xFF);
+                sc[1] = (uint8_t)(h >> 8);
+            } else {
+                uint8_t* sc = row + 128 + nope + g;
+                if (scale == 0.0f) {
+                    for (j = 0; j < n; ++j)
+                        codes[j] = 0;
+                    sc[0] = 0;
+                } else {
+                    const int k = e8m0_exponent(scale, round_scale);
+                    const float p = (float)ldexp(1.0, k);
+                    for (j = 0; j < n; ++j)
+                        codes[j] = or_e4m3_encode(xg[j] / p);
+                    sc[0] = (uint8_t)(k + 127);
+                }
+            }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
 /* Paged FP8 decode attention ([PA] 计算流程 steps 1-10, 循环结构).         */
 /*                                                                         */
 /* q [B*S1, NQ, D] E4M3, q_scale [B*S1, NQ] (dequant), k/v caches in the   */

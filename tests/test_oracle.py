@@ -456,3 +456,163 @@ def test_decode_rows_subset_matches_full():
     assert np.array_equal(flat_p[rows], flat_f[rows])
     mask = np.ones(len(flat_p), bool); mask[rows] = False
     assert not flat_p[mask].any()
+
+
+# ---------------------------------------------------------------------------
+# KV compress epilog, modes 0/1 ("CANN ops-transformer aclnnKvCompressEpilog
+# 算子详解": 计算公式 场景 1/2, 约束说明, kvCacheCol 的源码级解读)
+# ---------------------------------------------------------------------------
+
+def _kvc_run(x, mode, round_scale, *, head_dim=None, block_num=3, block_size=4, slots=None,
+             fill=0xA5, stride_pad=0):
+    """Run the oracle on rows x (float32 of BF16 values) into a pre-filled
+    cache; return the cache and its layout."""
+    bs, d = x.shape
+    head_dim = head_dim or oracle.kvc_min_head_dim(d, mode)
+    stride = block_size * head_dim + stride_pad
+    cache = np.full(block_num * stride, fill, np.uint8)
+    slots = np.arange(bs) if slots is None else np.asarray(slots)
+    oracle.kv_compress_epilog(x, cache, block_num, block_size, stride, head_dim, slots, mode,
+                              round_scale)
+    return cache, head_dim, stride, block_size
+
+
+def _kvc_row(cache, slot, head_dim, stride, block_size):
+    base = (slot // block_size) * stride + (slot % block_size) * head_dim
+    return cache[base:base + head_dim]
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def test_kvc_row_widths_printed_on_the_page():
+    """约束说明: d=256 and d=512 with quantMode=1 need headDim >= 323 and 583
+    (the page's own examples); mode 0 rounds the row up to 32 bytes."""
+    assert oracle.kvc_min_head_dim(256, 1) == 323
+    assert oracle.kvc_min_head_dim(512, 1) == 583
+    # concatCol = (d-64) + 64*2 + groups * scale bytes
+    assert oracle.kvc_concat_bytes(256, 0) == 192 + 128 + 3 * 2
+    assert oracle.kvc_min_head_dim(256, 0) == 352
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_kvc_constant_group_closed_form(mode):
+    """A group of equal values c: scale c/448, every code E4M3(448) = 0x7E
+    (mode 0); with a power-of-two scale 2^ceil(log2(c/448)) the code is
+    E4M3(c / 2^k) (mode 1). The rope part is the last 64 columns as BF16."""
+    d = 192
+    x = np.zeros((1, d), np.float32)
+    x[0, :64] = 3.0          # group 0
+    x[0, 64:128] = -0.25     # group 1
+    x[0, 128:] = _bf16(np.linspace(-2, 2, 64))   # rope
+    cache, hd, st, bsz = _kvc_run(x, mode, True)
+    row = _kvc_row(cache, 0, hd, st, bsz)
+    rope = row[:128].view(np.uint16)
+    assert np.array_equal(rope, oracle.bf16_from_float(x[0, 128:]))
+    codes = row[128:128 + 128]
+    if mode == 0:
+        assert np.all(codes[:64] == 0x7E) and np.all(codes[64:] == 0xFE)
+        sc = row[256:260].view(np.uint16)
+        assert np.array_equal(sc, oracle.bf16_from_float(np.array([3.0 / 448, 0.25 / 448], np.float32)))
+    else:
+        # 3/448 -> 2^-7 (3 * 128 = 384, code 0x7C); 0.25/448 -> 2^-10 (-256, code 0xF8)
+        assert np.all(codes[:64] == 0x7C) and np.all(codes[64:] == 0xF8)
+        assert list(row[256:258]) == [127 - 7, 127 - 10]
+    assert np.all(row[oracle.kvc_concat_bytes(d, mode):] == 0xA5)   # bytes past the row
+
+
+def test_kvc_spike_and_zero_groups():
+    """[v, 0, ...] encodes v as 448 and the rest as 0; an all-zero group has
+    scale 0 and zero codes in both modes."""
+    d = 256
+    x = np.zeros((1, d), np.float32)
+    x[0, 5] = -7.5
+    for mode in (0, 1):
+        cache, hd, st, bsz = _kvc_run(x, mode, True)
+        row = _kvc_row(cache, 0, hd, st, bsz)
+        codes = row[128:128 + 192]
+        if mode == 0:
+            assert codes[5] == 0xFE and np.count_nonzero(codes) == 1
+            assert list(row[320:326]) == list(oracle.bf16_from_float(
+                np.array([7.5 / 448, 0, 0], np.float32)).view(np.uint8))
+        else:
+            # 7.5/448 -> 2^-5: 7.5 * 32 = 240 (code 0xF7)
+            assert codes[5] == 0xF7 and np.count_nonzero(codes) == 1
+            assert list(row[320:323]) == [127 - 5, 0, 0]
+
+
+@pytest.mark.parametrize("round_scale", [True, False])
+def test_kvc_mode1_power_of_two_bounds(round_scale):
+    """Mode 1: every group scale is a power of two within a factor 2 of
+    amax/448 (at or above it with roundScale, at or below it without), so the
+    largest decoded |code| lies in [224, 448] with roundScale and is 448
+    (saturated or exact) without; codes times the scale reproduce x within
+    E4M3's half-ulp."""
+    rng = np.random.default_rng(5)
+    d, bs = 512, 6
+    x = _bf16(rng.standard_normal((bs, d)) * np.exp2(rng.uniform(-30, 30, (bs, 1))))
+    cache, hd, st, bsz = _kvc_run(x, 1, round_scale, block_num=2, block_size=4)
+    nope = d - 64
+    for i in range(bs):
+        row = _kvc_row(cache, i, hd, st, bsz)
+        codes = row[128:128 + nope].reshape(-1, 64)
+        k = row[128 + nope:128 + nope + nope // 64].astype(np.int64) - 127
+        dec = oracle.e4m3_decode(codes)
+        xg = x[i, :nope].reshape(-1, 64)
+        amax = np.abs(xg).max(axis=1)
+        s = np.exp2(k.astype(np.float64))
+        exact = amax.astype(np.float64) / 448
+        if round_scale:
+            assert np.all(s >= exact) and np.all(s < 2 * exact)
+            top = np.abs(dec).max(axis=1)
+            assert np.all(top <= 448) and np.all(top >= 224)   # amax/s in (224, 448], rounded
+        else:
+            assert np.all(s <= exact) and np.all(s > exact / 2)
+            assert np.all(np.abs(dec).max(axis=1) == 448)
+        deq = dec * s[:, None]
+        inrange = np.abs(xg / s[:, None]) <= 448
+        err = np.abs(deq - xg)[inrange]
+        bound = np.maximum(np.abs(xg) * 2.0 ** -4, (s[:, None] * 2.0 ** -10 + 0 * xg))[inrange]
+        assert np.all(err <= bound * (1 + 1e-12))
+
+
+def test_kvc_mode0_error_bound_and_scale_definition():
+    """Mode 0: the stored BF16 scale is BF16(amax/448) and codes times the
+    FP32 scale reproduce x within E4M3's half-ulp (subnormal step for tiny
+    values)."""
+    rng = np.random.default_rng(6)
+    d, bs = 1024, 4
+    x = _bf16(rng.standard_normal((bs, d)) * 3.0)
+    cache, hd, st, bsz = _kvc_run(x, 0, True, block_num=2, block_size=2)
+    nope = d - 64
+    for i in range(bs):
+        row = _kvc_row(cache, i, hd, st, bsz)
+        xg = x[i, :nope].reshape(-1, 64)
+        scale = (np.abs(xg).max(axis=1).astype(np.float32) / np.float32(448)).astype(np.float32)
+        sc = row[128 + nope:128 + nope + 2 * (nope // 64)].view(np.uint16)
+        assert np.array_equal(sc, oracle.bf16_from_float(scale))
+        dec = oracle.e4m3_decode(row[128:128 + nope].reshape(-1, 64))
+        err = np.abs(dec * scale[:, None].astype(np.float64) - xg)
+        bound = np.maximum(np.abs(xg) * 2.0 ** -4, scale[:, None] * 2.0 ** -10)
+        assert np.all(err <= bound * (1 + 1e-6))
+
+
+def test_kvc_slots_skip_and_untouched_bytes():
+    """Slot -1 and out-of-range slots are skipped; rows not addressed and the
+    bytes past each written row keep their values; rows land at
+    block * block_stride + offset * head_dim (non-contiguous blocks)."""
+    rng = np.random.default_rng(8)
+    d = 256
+    x = _bf16(rng.standard_normal((5, d)))
+    slots = np.array([3, -1, 10, 99, 6])
+    cache, hd, st, bsz = _kvc_run(x, 1, True, head_dim=400, block_num=3, block_size=4,
+                                  slots=slots, stride_pad=77)
+    ref = np.full_like(cache, 0xA5)
+    for i, s in enumerate(slots):
+        if 0 <= s < 12:
+            one, *_ = _kvc_run(x[i:i + 1], 1, True, head_dim=400, block_num=1, block_size=1,
+                               slots=[0])
+            base = (s // 4) * st + (s % 4) * 400
+            ref[base:base + 400] = one[:400]
+    assert np.array_equal(cache, ref)
