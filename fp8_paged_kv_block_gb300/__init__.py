@@ -9,6 +9,7 @@ Functions take torch CUDA tensors and work in place (outputs are arguments):
   decode(...)              paged FP8 decode attention -> BF16
   cache_scatter(...)       FP8 K/V (+ key_scale) append by slot_mapping
   cache_quant_scatter(...) BF16/FP32 K/V quantised to E4M3 on append
+  kv_compress_epilog(...)  BF16 rows to rope (BF16) + grouped E4M3 nope (modes 0/1)
   quantize_rows(...)       per-token E4M3 quantiser (Q, K)
   value_channel_scale(...) per-channel V dequant scale
 """
@@ -85,6 +86,9 @@ def lib():
         L.pa_fp8_cache_quant_scatter.argtypes = [P, P, i32, P, P, P, i32, P, P, P, i32, i64, i32,
                                                  i32, i64, i32, i32, i32, P]
         L.pa_fp8_cache_quant_scatter.restype = i32
+        L.pa_fp8_kv_compress_epilog.argtypes = [P, i64, i32, i64, i32, P, i64, i32, P, i32, i32,
+                                                i32, i32, P]
+        L.pa_fp8_kv_compress_epilog.restype = i32
         L.pa_fp8_quantize_rows.argtypes = [P, i32, i64, i32, P, P, P]
         L.pa_fp8_quantize_rows.restype = i32
         L.pa_fp8_value_channel_scale.argtypes = [P, i32, P, i32, i64, i32, i32, P, P]
@@ -300,6 +304,30 @@ def cache_quant_scatter(key, value, key_cache, value_cache, slot_mapping, key_sc
                                           D, NB, BS, layout, int(bool(overlap_prologue)),
                                           _stream(stream))
     _check(st, "pa_fp8_cache_quant_scatter")
+
+
+def kv_compress_epilog(cache, x, slot_mapping, *, quant_group_size: int = 64, quant_mode: int = 1,
+                       round_scale: bool = True, stream=None):
+    """KV compress epilog (modes 0 and 1), in place: cache uint8
+    [block_num, block_size, 1, head_dim] (blocks may be strided), x bfloat16
+    [bs, d], slot_mapping int32/int64 [bs]. Each row is written as the rope
+    part (last 64 values) in BF16, the rest in E4M3 groups of 64, then the
+    group scales (BF16 in mode 0, E8M0 in mode 1)."""
+    torch = _torch()
+    _need(cache, "cache", (torch.uint8,), contiguous=False)
+    _need(x, "x", (torch.bfloat16,))
+    _need(slot_mapping, "slot_mapping", (torch.int32, torch.int64))
+    if cache.dim() != 4 or cache.shape[2] != 1:
+        raise ValueError("cache must be [block_num, block_size, 1, head_dim]")
+    NB, BS, _, HD = cache.shape
+    if cache.stride(3) != 1 or cache.stride(1) != HD:
+        raise ValueError("cache rows must be contiguous within a block")
+    bs, d = x.shape
+    st = lib().pa_fp8_kv_compress_epilog(_ptr(cache), NB, BS, cache.stride(0), HD, _ptr(x), bs, d,
+                                         _ptr(slot_mapping), _slot_type(slot_mapping),
+                                         quant_group_size, quant_mode, int(bool(round_scale)),
+                                         _stream(stream))
+    _check(st, "pa_fp8_kv_compress_epilog")
 
 
 def quantize_rows(x, codes, scale, *, stream=None):

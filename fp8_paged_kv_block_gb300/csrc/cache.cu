@@ -260,6 +260,97 @@ quant_scatter_wide_kernel(const T* __restrict__ key, const T* __restrict__ value
     }
 }
 
+// ---- KV compress epilog (modes 0 and 1) ---------------------------------------------
+// One warp per row of x (d BF16 values): the last 64 values (rope) are stored
+// first as BF16, the first d - 64 (nope) as E4M3 in groups of 64 with one scale
+// per group after them: BF16(amax / 448) in mode 0, a power of two 2^k stored
+// as the E8M0 byte k + 127 in mode 1 (k rounded up from amax / 448 with
+// round_scale, the exponent of amax / 448 without). The row pitch may be odd,
+// so the stores are bytes.
+constexpr int kKvcThreads = 128;
+
+// floor(log2(s)) of a positive finite float and whether s is a power of two.
+__device__ __forceinline__ int floor_log2_pos(float s, bool* pow2)
+{
+    const uint32_t u = __float_as_uint(s);
+    const int e = static_cast<int>((u >> 23) & 0xFF);
+    const uint32_t m = u & 0x7FFFFFu;
+    if (e != 0) {
+        *pow2 = m == 0;
+        return e - 127;
+    }
+    *pow2 = (m & (m - 1)) == 0;            // subnormal: s = m * 2^-149
+    return (31 - __clz(static_cast<int>(m))) - 149;
+}
+
+// 2^k as a float for k in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float pow2f(int k)
+{
+    return k >= -126 ? __uint_as_float(static_cast<uint32_t>(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+__global__ void __launch_bounds__(kKvcThreads)
+kv_compress_epilog_kernel(uint8_t* __restrict__ cache, int64_t block_num, int block_size,
+                          int64_t block_stride, int head_dim, const __nv_bfloat16* __restrict__ x,
+                          int64_t bs, int d, const void* __restrict__ slots, int slot_type,
+                          int quant_mode, int round_scale)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (r >= bs) return;
+    const int64_t s = load_slot(slots, slot_type, r);
+    if (s < 0 || s >= block_num * block_size) return;
+    uint8_t* row = cache + (s / block_size) * block_stride + (s % block_size) * static_cast<int64_t>(head_dim);
+    const uint32_t* xr = reinterpret_cast<const uint32_t*>(x + r * d);   // BF16 pairs
+    const int nope = d - 64;
+    // rope: 64 BF16 = 128 bytes, 4 per lane
+    {
+        const uint32_t v = __ldg(xr + (nope >> 1) + lane);
+        uint8_t* dst = row + 4 * lane;
+        dst[0] = static_cast<uint8_t>(v);
+        dst[1] = static_cast<uint8_t>(v >> 8);
+        dst[2] = static_cast<uint8_t>(v >> 16);
+        dst[3] = static_cast<uint8_t>(v >> 24);
+    }
+    const int groups = nope / 64;
+    for (int g = 0; g < groups; ++g) {
+        const uint32_t v = __ldg(xr + 32 * g + lane);
+        const float x0 = __uint_as_float(v << 16), x1 = __uint_as_float(v & 0xFFFF0000u);
+        const float amax = warp_max(fmaxf(fabsf(x0), fabsf(x1)));
+        const float scale = __fdiv_rn(amax, kE4M3Max);
+        uint16_t codes;
+        if (quant_mode == 0) {
+            codes = scale == 0.0f ? 0 : e4m3x2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
+            if (lane == 0) {
+                // BF16 of the (finite, non-negative) scale: round to nearest even
+                // on the FP32 bit pattern
+                const uint32_t u = __float_as_uint(scale);
+                const uint32_t hb = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+                uint8_t* sc = row + 128 + nope + 2 * g;
+                sc[0] = static_cast<uint8_t>(hb);
+                sc[1] = static_cast<uint8_t>(hb >> 8);
+            }
+        } else {
+            int k = 0;
+            if (scale != 0.0f) {
+                bool p2;
+                k = floor_log2_pos(scale, &p2);
+                if (round_scale && !p2) ++k;
+                k = k < -127 ? -127 : (k > 127 ? 127 : k);
+                const float p = pow2f(k);
+                codes = e4m3x2(__fdiv_rn(x0, p), __fdiv_rn(x1, p));
+            } else {
+                codes = 0;
+                k = -127;
+            }
+            if (lane == 0) row[128 + nope + g] = static_cast<uint8_t>(k + 127);
+        }
+        uint8_t* dst = row + 128 + 64 * g + 2 * lane;
+        dst[0] = static_cast<uint8_t>(codes);
+        dst[1] = static_cast<uint8_t>(codes >> 8);
+    }
+}
+
 // ---- per-row quantiser -------------------------------------------------------------
 template <typename T>
 __global__ void quantize_rows_kernel(const T* __restrict__ x, int64_t rows, int D,
@@ -450,6 +541,38 @@ extern "C" pa_status pa_fp8_cache_quant_scatter(const void* key, const void* val
     PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_cache_quant_scatter: launch: %s",
                cudaGetErrorString(e));
     return PA_OK;
+}
+
+extern "C" pa_status pa_fp8_kv_compress_epilog(void* cache, int64_t block_num, int block_size,
+                                               int64_t block_stride, int head_dim, const void* x,
+                                               int64_t bs, int d, const void* slot_mapping,
+                                               int slot_type, int quant_group_size, int quant_mode,
+                                               int round_scale, void* stream)
+{
+    PA_REQUIRE(cache && x && slot_mapping, PA_ERR_NULLPTR, "pa_fp8_kv_compress_epilog: NULL tensor pointer");
+    PA_REQUIRE(bs > 0 && block_num > 0 && block_size > 0 && head_dim > 0, PA_ERR_INVALID,
+               "pa_fp8_kv_compress_epilog: empty or negative size");
+    PA_REQUIRE(d % 64 == 0 && d > 64 && d <= 8192, PA_ERR_INVALID,
+               "pa_fp8_kv_compress_epilog: d %d (a multiple of 64 in (64, 8192])", d);
+    PA_REQUIRE(quant_mode == 0 || quant_mode == 1, quant_mode == 2 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID,
+               "pa_fp8_kv_compress_epilog: quant_mode %d (0 and 1 are built)", quant_mode);
+    PA_REQUIRE(quant_group_size == 64, PA_ERR_INVALID,
+               "pa_fp8_kv_compress_epilog: quant_group_size %d (modes 0 and 1 use 64)", quant_group_size);
+    PA_REQUIRE(slot_type == PA_INDEX_I32 || slot_type == PA_INDEX_I64, PA_ERR_INVALID,
+               "pa_fp8_kv_compress_epilog: unknown slot type %d", slot_type);
+    const int64_t concat = (d - 64) + 128 + static_cast<int64_t>((d - 64) / 64) * (quant_mode == 0 ? 2 : 1);
+    const int64_t min_col = quant_mode == 0 ? (concat + 31) / 32 * 32 : concat;
+    PA_REQUIRE(head_dim >= min_col, PA_ERR_INVALID,
+               "pa_fp8_kv_compress_epilog: head_dim %d < %lld bytes a row needs", head_dim,
+               static_cast<long long>(min_col));
+    PA_REQUIRE(block_stride >= static_cast<int64_t>(block_size) * head_dim, PA_ERR_INVALID,
+               "pa_fp8_kv_compress_epilog: block_stride %lld < block_size * head_dim",
+               static_cast<long long>(block_stride));
+    PA_REQUIRE(aligned(x, 4), PA_ERR_INVALID, "pa_fp8_kv_compress_epilog: misaligned x");
+    kv_compress_epilog_kernel<<<blocks_for(bs * 32, kKvcThreads), kKvcThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint8_t*>(cache), block_num, block_size, block_stride, head_dim,
+        static_cast<const __nv_bfloat16*>(x), bs, d, slot_mapping, slot_type, quant_mode, round_scale);
+    return check_launch("pa_fp8_kv_compress_epilog");
 }
 
 extern "C" pa_status pa_fp8_quantize_rows(const void* x, int in_dtype, int64_t rows, int D,

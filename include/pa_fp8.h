@@ -286,6 +286,39 @@ PA_API pa_status pa_fp8_cache_quant_scatter(const void* key, const void* value, 
                                      int overlap_prologue, void* stream);
 
 /* ------------------------------------------------------------------------
+ * KV compress epilog, modes 0 and 1 ([KC] 功能说明, 计算公式 场景 1 and 场景 2,
+ * 约束说明, kvCacheCol 的源码级解读). In place. For each row i < bs of x with
+ * s = slot_mapping[i] (skipped if s < 0 or s >= block_num * block_size), the
+ * cache row at byte offset (s / block_size) * block_stride +
+ * (s % block_size) * head_dim receives, in this order:
+ *   bytes [0, 128)           x[i][d-64 .. d) (the rope part) as BF16,
+ *   bytes [128, 128 + d-64)  x[i][0 .. d-64) (the nope part) as E4M3 codes,
+ *                            quantised in groups of 64: scale_g =
+ *                            max|x_g| / 448 (FP32 IEEE division),
+ *                            code = E4M3(x / scale_g) round-to-nearest-even,
+ *                            saturating (all-zero group: scale 0, codes 0);
+ *   then one scale per group: mode 0 BF16(scale_g) (2 bytes, little-endian);
+ *   mode 1 one E8M0 byte k + 127 for the power of two 2^k used instead of
+ *   scale_g: the one at or above scale_g with round_scale, the one at or
+ *   below it (scale_g's exponent) without, k clamped to [-127, 127]; codes
+ *   are E4M3(x / 2^k) (an all-zero group stores byte 0).
+ * Other bytes of the row, and rows no slot names, are left unchanged.
+ * cache       uint8, block_num blocks of block_stride bytes (>= block_size *
+ *             head_dim; blocks need not be contiguous), rows of head_dim bytes.
+ * head_dim    >= (d - 64) + 128 + (d - 64) / 64 * (2 or 1) bytes, rounded
+ *             up to 32 for mode 0 (d = 256, mode 1: 323).
+ * x           BF16 [bs, d], d a multiple of 64 in (64, 8192], 4-byte aligned.
+ * slot_mapping int32 or int64 [bs] (slot_type); slots should be unique.
+ * quant_group_size must be 64. quant_mode 2 (HiFloat8 rope, FP4 nope) returns
+ * PA_ERR_UNSUPPORTED; other invalid arguments PA_ERR_INVALID.
+ * ------------------------------------------------------------------------ */
+PA_API pa_status pa_fp8_kv_compress_epilog(void* cache, int64_t block_num, int block_size,
+                                    int64_t block_stride, int head_dim, const void* x,
+                                    int64_t bs, int d, const void* slot_mapping, int slot_type,
+                                    int quant_group_size, int quant_mode, int round_scale,
+                                    void* stream);
+
+/* ------------------------------------------------------------------------
  * Per-token quantiser ([PA] 量化策略: Query/Key per-token): each row of D
  * values gets dequant scale s = max|x| / 448 and codes E4M3(x / s)
  * (round-to-nearest-even, saturating; an all-zero row gives s = 0, codes 0).

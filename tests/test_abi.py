@@ -28,7 +28,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for need in ("pa_fp8_decode", "pa_fp8_decode_workspace_size", "pa_fp8_cache_scatter",
                  "pa_fp8_cache_quant_scatter", "pa_fp8_quantize_rows",
-                 "pa_fp8_value_channel_scale", "pa_status_string", "pa_last_error"):
+                 "pa_fp8_value_channel_scale", "pa_fp8_kv_compress_epilog", "pa_status_string",
+                 "pa_last_error"):
         assert need in names
 
 
@@ -127,3 +128,22 @@ def test_product_path_has_no_oracle_dependency():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "liboracle" not in text and "pa_oracle" not in text, f
+
+
+def test_kv_compress_epilog_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    fake = P(256)
+    f = L.pa_fp8_kv_compress_epilog
+    f.restype = ctypes.c_int
+    f.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int, P, ctypes.c_int64,
+                  ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+    # cache, NB, BS, stride, head_dim, x, bs, d, slots, slot type, group, mode, round, stream
+    assert f(None, 8, 16, 16 * 384, 384, fake, 4, 256, fake, 0, 64, 1, 1, None) == 1
+    assert f(fake, 8, 16, 16 * 384, 384, fake, 4, 200, fake, 0, 64, 1, 1, None) == 2   # d % 64
+    assert f(fake, 8, 16, 16 * 384, 384, fake, 4, 64, fake, 0, 64, 1, 1, None) == 2    # d > 64
+    assert f(fake, 8, 16, 16 * 384, 384, fake, 4, 256, fake, 0, 32, 1, 1, None) == 2   # group 64
+    assert f(fake, 8, 16, 16 * 384, 384, fake, 4, 256, fake, 0, 64, 2, 1, None) == 5   # HiF8/FP4
+    assert f(fake, 8, 16, 16 * 322, 322, fake, 4, 256, fake, 0, 64, 1, 1, None) == 2   # 323 bytes
+    assert b"323" in L.pa_last_error()
+    assert f(fake, 8, 16, 16 * 326, 326, fake, 4, 256, fake, 0, 64, 0, 1, None) == 2   # mode 0: 352
+    assert f(fake, 8, 16, 15 * 384, 384, fake, 4, 256, fake, 0, 64, 1, 1, None) == 2   # block stride

@@ -282,3 +282,39 @@ def test_step_chain_overlap_in_graph(torch_cuda, mode):
     for _ in range(2):
         g.replay()
         check()
+
+
+@pytest.mark.parametrize("round_scale", [True, False])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("d", [128, 256, 576, 1024])
+def test_kv_compress_epilog_bitexact(torch_cuda, d, mode, round_scale):
+    """KV compress epilog, modes 0/1: BF16 rows with a wide dynamic range,
+    zero and one-spike groups, int32/int64 slots with -1 and out-of-range
+    entries, blocks at a stride larger than the block (non-contiguous) and an
+    odd row pitch: every cache byte equals the oracle's."""
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    rng = np.random.default_rng(900 + d + 10 * mode + int(round_scale))
+    bs, NB, BS = 45, 7, 8
+    x = (rng.standard_normal((bs, d)) * np.exp2(rng.uniform(-40, 40, (bs, 1)))).astype(np.float32)
+    x[3, :64] = 0.0                          # zero group
+    x[4, :] = 0.0
+    x[4, 70] = -3.5                          # one spike
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    xf = xb.float().numpy()
+    head_dim = oracle.kvc_min_head_dim(d, mode) + 3          # odd pitch
+    pitch = (BS + 2) * head_dim                              # strided blocks
+    slots = rng.choice(NB * BS, bs, replace=False).astype(np.int64)
+    slots[rng.random(bs) < 0.1] = -1
+    slots[7] = NB * BS + 5
+    for slot_dtype in (torch.int32, torch.int64):
+        base = torch.from_numpy(rng.integers(0, 256, NB * pitch, dtype=np.uint8)).cuda()
+        ref = base.cpu().numpy().copy()
+        cache = base.view(NB, BS + 2, 1, head_dim)[:, :BS]
+        pa.kv_compress_epilog(cache, xb.cuda(), torch.from_numpy(slots).to(slot_dtype).cuda(),
+                              quant_mode=mode, round_scale=round_scale)
+        torch.cuda.synchronize()
+        oracle.kv_compress_epilog(xf, ref, NB, BS, pitch, head_dim, slots, mode, round_scale)
+        got = base.cpu().numpy()
+        bad = np.nonzero(got != ref)[0]
+        assert bad.size == 0, (slot_dtype, bad[:10], got[bad[:10]], ref[bad[:10]])
