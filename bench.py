@@ -54,8 +54,8 @@ FALLBACK_HBM_GBS = 6800.0
 OVERLAP_DECODE = 2
 OVERLAP_APPEND = True
 
-DECODE_TRAFFIC = {"sources_sha1": "16b8f8007852e09fdafb8ca5185c7fe1af22db69",
-                  "bytes_per_launch": 57871360 + 85248}
+DECODE_TRAFFIC = {"sources_sha1": "7a0f808934febb1bf199e314f196c867adb2dfdb",
+                  "bytes_per_launch": 57871616 + 131328}
 
 
 def parse_args():
