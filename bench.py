@@ -38,6 +38,9 @@ import workloads  # noqa: E402
 
 METRIC = "FP8 paged decode attn: achieved HBM GB/s (% of peak), µs/step at GLM-4.5 shape"
 UNIT = "GB/s"
+WORKLOAD = ("glm45_decode_step: append 1 BF16 token/seq (quantise-on-append scatter) + FP8 "
+            "paged GQA decode; B=16 S1=1 NQ=96 NKV=8 D=128 block_size=128 kv~U[1,4096] "
+            "s2_tile=512 PA_BSND")
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic of one decode launch on this workload, from an ncu capture
@@ -71,11 +74,62 @@ def parse_args():
     return ap.parse_args()
 
 
-def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+# --------------------------------------------------------------------------
+# ranks: one process per GPU, each a whole replica of the step (the path has no
+# exchange step, so there is no data-path collective); the host joins the ranks
+# only to start and stop the clock together and to take the slowest rank's time
+# --------------------------------------------------------------------------
+
+def dist_env(env=None):
+    """(rank, world_size, local_rank) as torchrun exports them; 1 process by default."""
+    env = os.environ if env is None else env
+    rank = int(env.get("RANK", "0"))
+    world = int(env.get("WORLD_SIZE", "1"))
+    local = int(env.get("LOCAL_RANK", str(rank)))
+    if world < 1 or not 0 <= rank < world or local < 0:
+        raise ValueError("bad rank environment: RANK=%d WORLD_SIZE=%d LOCAL_RANK=%d"
+                         % (rank, world, local))
     return rank, world, local
+
+
+def init_ranks(world, backend, device=None):
+    """Join the process group (NCCL on GPUs; gloo for host-only use)."""
+    if world > 1:
+        import torch.distributed as dist
+        if device is None:
+            dist.init_process_group(backend)
+        else:
+            dist.init_process_group(backend, device_id=device)
+
+
+def finish_ranks(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device="cpu"):
+    """The largest of every rank's x (each rank passes its own; all get the max)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world, bytes_per_step, steps, ms):
+    """Whole-job GB/s: the bytes all ranks processed over the slowest rank's ms."""
+    if ms <= 0:
+        raise ValueError("non-positive time %r ms" % (ms,))
+    return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
 
 
 def kernel_sources_sha1() -> str:
@@ -240,8 +294,7 @@ def reference_arm(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": full / (value * 1e9) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f32",
         "data": "synthetic",
-        "config": {"workload": "glm45_decode B=16 S1=1 NQ=96 NKV=8 D=128 bs=128 "
-                               "kv~U[1,4096] s2_tile=512 PA_BSND", "sample_rows": len(rows)},
+        "config": {"workload": WORKLOAD, "sample_rows": len(rows)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "%d query rows (whole units) per step, decode only; "
                                    "ms_per_step extrapolated to the full step by bytes" % len(rows)},
@@ -269,9 +322,7 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+    init_ranks(world, "nccl", dev)
     pa.build()
     pa.lib()
 
@@ -356,13 +407,8 @@ def main():
         if n % cyc:
             tails[n % cyc].replay()
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     def timed(graphs, n):
-        barrier()
+        barrier(world)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -373,14 +419,8 @@ def main():
         run_steps(graphs, n)
         e1.record()
         torch.cuda.synchronize()
-        barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     clocks = ClockSampler(local)
     # warm-up (untimed)
@@ -436,7 +476,7 @@ def main():
         e2e_step(i)
     torch.cuda.synchronize()
     n_e2e = args.steps
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -454,15 +494,11 @@ def main():
     ms_e2e = timed(g_e2e, n_e2e)
     clk = clocks.stop()
     assert ws.error_flags() == 0, "decode kernel reported a wait timeout"
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_e2e_eager], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e_eager = float(t.item())
+    ms_e2e_eager = max_over_ranks(ms_e2e_eager, world, dev)
 
     ms_step = ms_total / args.steps
     ms_dec_launch = ms_dec / args.steps
-    value = world * bytes_per_step * args.steps / (ms_total * 1e-3) / 1e9
+    value = whole_job_gbs(world, bytes_per_step, args.steps, ms_total)
     peak, peak_src = measured_hbm_peak()
     achieved = dec_bytes / (ms_dec_launch * 1e-3) / 1e9
     sha = kernel_sources_sha1()
@@ -481,9 +517,7 @@ def main():
             "us_per_step": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3+f32", "data": "synthetic",
             "config": {
-                "workload": "glm45_decode_step: append 1 BF16 token/seq (quantise-on-append "
-                            "scatter) + FP8 paged GQA decode; B=16 S1=1 NQ=96 NKV=8 D=128 "
-                            "block_size=128 kv~U[1,4096] s2_tile=512 PA_BSND",
+                "workload": WORKLOAD,
                 "B": case.B, "kv_tokens": int(act_after.sum()), "bytes_per_step": bytes_per_step,
                 "decode_bytes": dec_bytes, "append_bytes": app_bytes,
                 "l2": "inputs larger than L2: %d cache copies rotated (%.0f MB > %.0f MB L2)"
@@ -504,7 +538,7 @@ def main():
                          "us_per_launch": ms_dec_launch * 1e3,
                          "us_per_launch_stream_order": ms_dec0 / args.steps * 1e3,
                          "algorithmic_bytes_per_launch": dec_bytes},
-            "e2e": {"value": world * bytes_per_step * n_e2e / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+            "e2e": {"value": whole_job_gbs(world, bytes_per_step, n_e2e, ms_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_step": ms_e2e / n_e2e * 1e3,
                     "issue": "the public-API calls of a step (pinned H2D copy, append, decode, "
@@ -515,9 +549,7 @@ def main():
             "tokens_per_s": world * case.B * case.S1 * args.steps / (ms_total * 1e-3),
         }
         print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    finish_ranks(world)
 
 
 if __name__ == "__main__":
