@@ -81,6 +81,9 @@ def _load():
         lib.or_pa_decode.argtypes = [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                      i32, i64, i32, i32, i32, f32, P, i64]
         lib.or_pa_decode.restype = ctypes.c_int
+        lib.or_mla_sparse_decode.argtypes = [P, P, P, i64, P, i32, P, P, P, P, i32, i32, i32,
+                                             i32, i64, i32, i32, f32, P, i64]
+        lib.or_mla_sparse_decode.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -285,4 +288,55 @@ def pa_decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_ac
                           max_blocks, layout, s2_tile, softmax_scale, _ptr(r), nrows)
     if rc != 0:
         raise ValueError("or_pa_decode rejected its arguments")
+    return (out, out32) if want_f32 else out
+
+
+# --------------------------------------------------------------------------
+# MLA sparse attention with FP8 anti-quantisation (decode)
+# --------------------------------------------------------------------------
+
+MLA_DN = 512
+MLA_DR = 64
+MLA_ROW_USED = 656
+
+
+def mla_sparse_decode(q_nope, q_rope, cache, topk_indices, block_table, kv_act_seqs, *, S1,
+                      block_size=128, s2_tile=128, softmax_scale=None, rows=None,
+                      want_f32=False):
+    """MLA sparse FP8 decode (the steps are listed in ``pa_oracle.c``).
+
+    q_nope uint16 (BF16 bits) [T, NQ, 512], q_rope uint16 [T, NQ, 64] with
+    T = B*S1; cache uint8 [num_blocks*block_size, row_bytes >= 656] packed rows
+    (E4M3 kn | BF16 kr | 4 FP32 scales); topk_indices int32 [T, topk];
+    block_table int32 [B, max_blocks]; kv_act_seqs int32 [B]. Returns BF16 bits
+    uint16 [T, NQ, 512] (and the float32 values before the cast when
+    ``want_f32``). ``rows`` restricts the work to the flat rows ``t*NQ + h``;
+    other rows are left zero.
+    """
+    lib = _load()
+    qn = _c(q_nope, np.uint16)
+    qr = _c(q_rope, np.uint16)
+    kv = _c(cache, np.uint8)
+    tk = _c(topk_indices, np.int32)
+    bt = _c(block_table, np.int32)
+    act = _c(kv_act_seqs, np.int32)
+    T, NQ, dn = qn.shape
+    assert dn == MLA_DN and qr.shape == (T, NQ, MLA_DR)
+    B = act.shape[0]
+    assert T == B * S1 and tk.shape[0] == T
+    rows_total, row_bytes = kv.shape
+    assert rows_total % block_size == 0
+    num_blocks = rows_total // block_size
+    if softmax_scale is None:
+        softmax_scale = float(np.float32(1.0) / np.sqrt(np.float32(MLA_DN + MLA_DR)))
+    out = np.zeros((T, NQ, MLA_DN), dtype=np.uint16)
+    out32 = np.zeros((T, NQ, MLA_DN), dtype=np.float32) if want_f32 else None
+    r = None if rows is None else _c(rows, np.int64)
+    nrows = 0 if r is None else r.size
+    rc = lib.or_mla_sparse_decode(_ptr(qn), _ptr(qr), _ptr(kv), row_bytes, _ptr(tk),
+                                  tk.shape[1], _ptr(bt), _ptr(act), _ptr(out), _ptr(out32), B,
+                                  S1, NQ, block_size, num_blocks, bt.shape[1], s2_tile,
+                                  softmax_scale, _ptr(r), nrows)
+    if rc != 0:
+        raise ValueError("or_mla_sparse_decode rejected its arguments")
     return (out, out32) if want_f32 else out

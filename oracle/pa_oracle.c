@@ -17,6 +17,10 @@
  *  [KC]  "CANN ops-transformer aclnnKvCompressEpilog 算子详解": section
  *        计算公式, 场景 1 (scale_g = max|x_g| / FP8_MAX, q = round(x / scale_g)),
  *        and the FP8_E4M3FN max value 448 quoted there.
+ *  [MS]  "PyPTO-Gym 算子实战：DeepSeek V32 MLA 的 Sparse Attention FP8
+ *        反量化算子（Ascend 950PR）解析与验证": sections 核心参数与 KV Cache
+ *        布局, API 签名与 Decode / Prefill 差异, 计算流程：5 层嵌套循环,
+ *        关键实现细节, 在线反量化与 Online Softmax 的实现细节.
  *
  * Precision: every step is done in the precision the pages fix (FP32 for
  * dequant, softmax and accumulation; E4M3 for Q/K/V/P; BF16 output). The two
@@ -539,5 +543,174 @@ int or_pa_decode(const uint8_t* q, const float* q_scale, const uint8_t* k_cache,
     free(P);
     free(P8);
     free(O);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* MLA sparse attention with FP8 anti-quantisation, decode ([MS] 核心参数与 */
+/* KV Cache 布局, API 签名, 计算流程: 5 层嵌套循环, 关键实现细节,          */
+/* 在线反量化与 Online Softmax 的实现细节).                                 */
+/*                                                                         */
+/* Fixed sizes: kv_lora_rank 512 (the "nope" part), qk_rope_dim 64, so a   */
+/* query/key head is 576 wide; one KV head shared by all NQ query heads.   */
+/* Cache row (row_bytes >= 656 bytes apart, [MS] pads them to 672):        */
+/*   [0, 512)    kn, E4M3 codes;                                            */
+/*   [512, 640)  kr, 64 BF16 values (little-endian);                        */
+/*   [640, 656)  4 FP32 dequant scales, one per 128 channels of kn.         */
+/* q_nope [T*NQ][512], q_rope [T*NQ][64] BF16 bits, T = B*S1 query tokens, */
+/* token t = b*S1 + s. topk_indices [T][topk] int32: positions in the      */
+/* sequence of the selected keys. block_table [B][max_blocks] int32,       */
+/* kv_act_seqs [B]. out [T*NQ][512] BF16 bits (out_f32: before the cast).  */
+/*                                                                         */
+/* For query token t and head h:                                           */
+/*  - cur = clamp(kv_act_seqs[b] - S1 + 1 + s, 0, topk): only the first    */
+/*    cur selected keys take part ([MS] 关键实现细节, 动态序列裁剪).         */
+/*  - those keys are walked in s2_tile-sized tiles; key j of a tile:       */
+/*    idx = topk_indices[t][j]; physical row                               */
+/*    block_table[b][idx / BS] * BS + idx % BS (a block id of -1, or any   */
+/*    id outside the pool, is read as block 0).                            */
+/*    An idx outside [0, kv_act_seqs[b]) takes no part (the pages only     */
+/*    produce valid positions; masking is the plain reading of "-1" pads). */
+/*  - dequant: kn_j[c] = BF16(FP32(E4M3(code)) * scale[c / 128]);          */
+/*    k_j = [kn_j, kr_j] (576), q = [q_nope, q_rope] (576).                */
+/*  - C1: s_j = q . k_j, FP32 result (products of BF16 are exact; summed   */
+/*    in double and rounded once); S_j = s_j * softmax_scale.              */
+/*  - V1 per tile: m = max S_j, p_j = exp(S_j - m), l = sum p_j (FP32),    */
+/*    P_j = BF16(p_j).                                                     */
+/*  - C2: o[c] = sum_j P_j * kn_j[c] for c < 512 (V reuses kn), FP32.      */
+/*  - online update: the first tile sets O = o, L = l, M = m; a later tile */
+/*    takes Mn = max(M, m), a = exp(M - Mn), b = exp(m - Mn),              */
+/*    O = O * a + o * b, L = L * a + l * b, M = Mn.                         */
+/*  - out[c] = BF16(O[c] / L).                                             */
+/* A tile with no valid key changes nothing; a row with no valid key at    */
+/* all gets zeros (the pages are silent on both).                          */
+/* rows (optional) restricts the work to the listed flat rows t*NQ + h.    */
+/* Returns 0, or -1 on bad arguments / allocation failure.                 */
+/* ---------------------------------------------------------------------- */
+int or_mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const uint8_t* cache,
+                         int64_t row_bytes, const int32_t* topk_indices, int topk,
+                         const int32_t* block_table, const int32_t* kv_act_seqs, uint16_t* out,
+                         float* out_f32, int B, int S1, int NQ, int BS, int64_t num_blocks,
+                         int max_blocks, int s2_tile, float softmax_scale, const int64_t* rows,
+                         int64_t nrows)
+{
+    enum { DN = 512, DR = 64, DK = 576 };
+    float* kn;   /* [s2_tile][512] dequantised kn of the tile (BF16 values) */
+    float* kr;   /* [s2_tile][64]  */
+    float* S;
+    float* P;
+    uint8_t* ok;
+    double q[DK];
+    float O[DN];
+    int64_t total = (int64_t)B * S1 * NQ, ri;
+    if (B <= 0 || S1 <= 0 || NQ <= 0 || BS <= 0 || topk < 0 || s2_tile <= 0 ||
+        row_bytes < 656 || num_blocks <= 0 || max_blocks <= 0)
+        return -1;
+    kn = (float*)malloc(sizeof(float) * (size_t)s2_tile * DN);
+    kr = (float*)malloc(sizeof(float) * (size_t)s2_tile * DR);
+    S = (float*)malloc(sizeof(float) * (size_t)s2_tile);
+    P = (float*)malloc(sizeof(float) * (size_t)s2_tile);
+    ok = (uint8_t*)malloc((size_t)s2_tile);
+    if (!kn || !kr || !S || !P || !ok) {
+        free(kn); free(kr); free(S); free(P); free(ok);
+        return -1;
+    }
+    for (ri = 0; ri < (rows ? nrows : total); ++ri) {
+        int64_t row = rows ? rows[ri] : ri; /* t*NQ + h */
+        int64_t t;
+        int b, s, act, cur, j0, c, any = 0;
+        float M = -INFINITY, L = 0.0f;
+        if (row < 0 || row >= total)
+            continue;
+        t = row / NQ;
+        b = (int)(t / S1);
+        s = (int)(t % S1);
+        act = kv_act_seqs[b];
+        cur = act - S1 + 1 + s;
+        if (cur < 0)
+            cur = 0;
+        if (cur > topk)
+            cur = topk;
+        for (c = 0; c < DN; ++c) {
+            q[c] = or_bf16_to_float(q_nope[row * DN + c]);
+            O[c] = 0.0f;
+        }
+        for (c = 0; c < DR; ++c)
+            q[DN + c] = or_bf16_to_float(q_rope[row * DR + c]);
+        for (j0 = 0; j0 < cur; j0 += s2_tile) {
+            int n = (cur - j0 < s2_tile) ? cur - j0 : s2_tile, j;
+            float m = -INFINITY, l = 0.0f;
+            /* gather + dequant + C1 + scale */
+            for (j = 0; j < n; ++j) {
+                int idx = topk_indices[t * topk + j0 + j];
+                const uint8_t* kv;
+                float sc[4];
+                int blk;
+                double acc = 0.0;
+                ok[j] = (uint8_t)(idx >= 0 && idx < act);
+                if (!ok[j])
+                    continue;
+                blk = block_table[(int64_t)b * max_blocks + idx / BS];
+                if (blk < 0 || blk >= num_blocks)
+                    blk = 0;
+                kv = cache + ((int64_t)blk * BS + idx % BS) * row_bytes;
+                memcpy(sc, kv + 640, sizeof(sc));
+                for (c = 0; c < DN; ++c) {
+                    float f = (float)or_e4m3_decode(kv[c]) * sc[c / 128];
+                    kn[(int64_t)j * DN + c] = or_bf16_to_float(or_bf16_from_float(f));
+                }
+                for (c = 0; c < DR; ++c)
+                    kr[(int64_t)j * DR + c] =
+                        or_bf16_to_float((uint16_t)(kv[DN + 2 * c] | (kv[DN + 2 * c + 1] << 8)));
+                for (c = 0; c < DN; ++c)
+                    acc += q[c] * (double)kn[(int64_t)j * DN + c];
+                for (c = 0; c < DR; ++c)
+                    acc += q[DN + c] * (double)kr[(int64_t)j * DR + c];
+                S[j] = (float)acc * softmax_scale;
+                if (S[j] > m)
+                    m = S[j];
+            }
+            if (m == -INFINITY)
+                continue; /* no valid key in this tile */
+            /* V1: tile-local softmax numerator, its sum and the BF16 cast */
+            for (j = 0; j < n; ++j) {
+                float p = ok[j] ? expf(S[j] - m) : 0.0f;
+                l += p;
+                P[j] = or_bf16_to_float(or_bf16_from_float(p));
+            }
+            /* C2 and the online update */
+            {
+                float a = 1.0f, bb = 1.0f, Mn = m;
+                if (any) {
+                    Mn = (M > m) ? M : m;
+                    a = expf(M - Mn);
+                    bb = expf(m - Mn);
+                }
+                for (c = 0; c < DN; ++c) {
+                    double acc = 0.0;
+                    float o;
+                    for (j = 0; j < n; ++j)
+                        if (ok[j])
+                            acc += (double)P[j] * (double)kn[(int64_t)j * DN + c];
+                    o = (float)acc;
+                    O[c] = any ? O[c] * a + o * bb : o;
+                }
+                L = any ? L * a + l * bb : l;
+                M = Mn;
+                any = 1;
+            }
+        }
+        for (c = 0; c < DN; ++c) {
+            float o = any ? O[c] / L : 0.0f;
+            out[row * DN + c] = or_bf16_from_float(o);
+            if (out_f32)
+                out_f32[row * DN + c] = o;
+        }
+    }
+    free(kn);
+    free(kr);
+    free(S);
+    free(P);
+    free(ok);
     return 0;
 }

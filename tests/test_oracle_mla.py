@@ -1,0 +1,301 @@
+"""Pins for the MLA sparse FP8 decode oracle (no GPU).
+
+The oracle (``oracle.mla_sparse_decode``) follows the steps of the DeepSeek
+V3.2 MLA sparse attention FP8 anti-quantisation page. Here it is checked
+against things other than itself: brute-force FP64 attention, closed forms
+computed with torch's float8_e4m3fn / bfloat16 conversions, the online merge
+written out for keys in separate tiles, and invariances (padding bytes,
+physical block placement, entries past the visible count, masked entries,
+key order within a tile).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+DN, DR = 512, 64
+
+
+def small_case(B=2, S1=2, NQ=4, act=(300, 41), topk=64, seed=7, frac_invalid=0.0, BS=128):
+    return workloads.mla("small", B, S1, list(act), NQ=NQ, topk=topk,
+                         seed=workloads.BASE_SEED + 300 + seed, frac_invalid=frac_invalid, BS=BS)
+
+
+def run(case, cache=None, topk=None, s2_tile=None, bt=None, want_f32=True, rows=None):
+    qn, qr = case.q_bits()
+    return oracle.mla_sparse_decode(
+        qn, qr, case.cache() if cache is None else cache,
+        case.topk_indices() if topk is None else topk,
+        case.block_table if bt is None else bt, case.act, S1=case.S1, block_size=case.BS,
+        s2_tile=case.s2_tile if s2_tile is None else s2_tile, softmax_scale=case.softmax_scale,
+        rows=rows, want_f32=want_f32)
+
+
+# ---- independent dequantisation with torch ---------------------------------
+
+def torch_keys(case, cache, rows):
+    """(kn BF16 values as float64 [n, 512], kr float64 [n, 64]) of the given
+    physical rows, dequantised with torch: E4M3 -> float32, times the FP32
+    scale of each 128-channel group, rounded to BF16."""
+    r = torch.from_numpy(cache[np.asarray(rows)].copy())
+    codes = r[:, :DN].contiguous().view(torch.float8_e4m3fn).to(torch.float32)
+    scale = r[:, DN + 2 * DR:DN + 2 * DR + 16].contiguous().view(torch.float32)
+    kn = (codes * scale.repeat_interleave(128, dim=1)).to(torch.bfloat16).to(torch.float64)
+    kr = r[:, DN:DN + 2 * DR].contiguous().view(torch.bfloat16).to(torch.float64)
+    return kn.numpy(), kr.numpy()
+
+
+def torch_query(case, t, h):
+    qn, qr = case.q_bf16()
+    return np.concatenate([qn[t, h].double().numpy(), qr[t, h].double().numpy()])
+
+
+def selected(case, t):
+    """Physical rows of token t's valid selected keys, in list order."""
+    b, s = divmod(t, case.S1)
+    n = int(case.cur()[t])
+    idx = case.topk_indices()[t, :n].astype(np.int64)
+    idx = idx[(idx >= 0) & (idx < case.act[b])]
+    return case.physical_rows(idx, np.full(idx.shape, b))
+
+
+# ---- brute force ------------------------------------------------------------
+
+@pytest.mark.parametrize("s2_tile", [128, 16, 5])
+def test_mla_vs_bruteforce_fp64(s2_tile):
+    """Unquantised-softmax FP64 attention over the dequantised keys: the
+    oracle differs only by the BF16 casts of the keys and P."""
+    case = small_case(frac_invalid=0.1)
+    cache = case.cache()
+    _, out32 = run(case, cache=cache, s2_tile=s2_tile)
+    worst = 0.0
+    for t in range(case.T):
+        rows = selected(case, t)
+        for h in range(case.NQ):
+            if rows.size == 0:
+                assert not out32[t, h].any()
+                continue
+            codes = cache[rows, :DN]
+            sc = cache[rows, DN + 2 * DR:DN + 2 * DR + 16].copy().view(np.float32)
+            kn = oracle.e4m3_decode(codes) * np.repeat(sc.astype(np.float64), 128, axis=1)
+            kr = cache[rows, DN:DN + 2 * DR].copy().view(np.uint16).astype(np.uint32) << 16
+            kr = kr.view(np.float32).astype(np.float64)
+            q = torch_query(case, t, h)
+            s = (np.concatenate([kn, kr], axis=1) @ q) * case.softmax_scale
+            w = np.exp(s - s.max())
+            ref = (w / w.sum()) @ kn
+            worst = max(worst, float(np.abs(out32[t, h] - ref).max()))
+    # BF16 keys and P carry 2^-9 relative error each
+    assert worst < 2e-2, worst
+
+
+# ---- closed forms -----------------------------------------------------------
+
+def test_mla_single_key_gives_its_bf16_nope_row():
+    """One visible key: P = 1 and L = 1, so every head outputs that key's
+    dequantised, BF16-rounded nope row, bit for bit."""
+    case = small_case(act=(1, 1), S1=1, B=2, topk=8)
+    cache = case.cache()
+    out = run(case, cache=cache, want_f32=False)
+    for t in range(case.T):
+        rows = selected(case, t)
+        assert rows.size == 1
+        kn, _ = torch_keys(case, cache, rows)
+        want = torch.from_numpy(kn[0]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        for h in range(case.NQ):
+            assert np.array_equal(out[t, h], want)
+
+
+def _two_key_case(gap):
+    """One token, two visible keys; the second key's rope part is shifted so
+    that its score is `gap` below the first's."""
+    case = small_case(B=1, S1=1, NQ=2, act=(2,), topk=2)
+    cache = case.cache()
+    rows = selected(case, 0)
+    return case, cache, rows
+
+
+def test_mla_two_keys_one_tile_closed_form():
+    """Two keys in one tile: O = (P_1 kn_1 + P_2 kn_2) / (p_1 + p_2) with
+    p = exp(S - max S) and P = BF16(p) (the numerator uses the BF16 P, the sum
+    the FP32 p). Scores include the rope part."""
+    case, cache, rows = _two_key_case(0.0)
+    _, out32 = run(case, cache=cache, s2_tile=128)
+    kn, kr = torch_keys(case, cache, rows)
+    for h in range(case.NQ):
+        q = torch_query(case, 0, h)
+        s = (np.concatenate([kn, kr], axis=1) @ q) * np.float64(np.float32(case.softmax_scale))
+        p = np.exp(s - s.max())
+        P = torch.from_numpy(p.astype(np.float32)).to(torch.bfloat16).double().numpy()
+        want = (P @ kn) / p.sum()
+        np.testing.assert_allclose(out32[0, h], want, rtol=2e-5, atol=1e-6)
+        # dropping the rope part would change the weights
+        s_nr = (kn @ q[:DN]) * case.softmax_scale
+        assert abs((s - s.max())[0] - (s_nr - s_nr.max())[0]) > 1e-3 or \
+            abs((s - s.max())[1] - (s_nr - s_nr.max())[1]) > 1e-3
+
+
+def test_mla_two_keys_two_tiles_online_merge():
+    """Keys in separate tiles (s2_tile 1): each tile has P = 1 exactly, so the
+    merge O = a o_1 + b o_2, L = a + b with a = exp(m_1 - M), b = exp(m_2 - M)
+    gives the exact softmax weighting of the two BF16 nope rows."""
+    case, cache, rows = _two_key_case(0.0)
+    _, out32 = run(case, cache=cache, s2_tile=1)
+    kn, kr = torch_keys(case, cache, rows)
+    for h in range(case.NQ):
+        q = torch_query(case, 0, h)
+        s = (np.concatenate([kn, kr], axis=1) @ q) * np.float64(np.float32(case.softmax_scale))
+        w = np.exp(s - s.max())
+        want = (w @ kn) / w.sum()
+        np.testing.assert_allclose(out32[0, h], want, rtol=2e-5, atol=1e-6)
+
+
+def test_mla_tile_size_changes_only_the_bf16_rounding_of_p():
+    """Tile-local P: with one tile per key there is no BF16 rounding of P at
+    all; with one tile for all keys there is. The two agree to BF16 accuracy
+    but not bit for bit."""
+    case = small_case(B=1, S1=1, act=(60,), topk=64)
+    cache = case.cache()
+    _, a = run(case, cache=cache, s2_tile=1)
+    _, b = run(case, cache=cache, s2_tile=128)
+    assert not np.array_equal(a, b)
+    np.testing.assert_allclose(a, b, atol=2e-3 * np.abs(a).max())
+
+
+# ---- the visible count, masking and addressing --------------------------------
+
+def test_mla_visible_count_rule():
+    """Token s of a sequence of length n attends to min(n - S1 + 1 + s, topk)
+    selected keys: entries past that count are never read, and a token with
+    no visible key gets zeros."""
+    case = small_case(B=3, S1=3, act=(200, 2, 1), topk=64)
+    assert case.cur().tolist() == [64, 64, 64, 0, 1, 2, 0, 0, 1]
+    cache = case.cache()
+    tk = case.topk_indices().copy()
+    base = run(case, cache=cache, topk=tk, want_f32=False)
+    cur = case.cur()
+    t2 = tk.copy()
+    for t in range(case.T):
+        # fill the unread tail with valid positions of the sequence
+        b = t // case.S1
+        t2[t, cur[t]:] = np.arange(case.topk - cur[t]) % max(int(case.act[b]), 1)
+    assert np.array_equal(run(case, cache=cache, topk=t2, want_f32=False), base)
+    for t in np.nonzero(cur == 0)[0]:
+        assert not base[t].any()
+
+
+def test_mla_masked_entries_take_no_part():
+    """Within one tile, entries that are -1 or past kv_act_seqs contribute
+    nothing: the output equals that of the list with them removed."""
+    case = small_case(B=1, S1=1, act=(100,), topk=64)
+    cache = case.cache()
+    tk = case.topk_indices().copy()
+    n = int(case.cur()[0])
+    bad = tk.copy()
+    bad[0, 3] = -1
+    bad[0, 10] = case.act[0]          # one past the end
+    bad[0, 20] = case.act[0] + 500
+    keep = [j for j in range(n) if j not in (3, 10, 20)]
+    comp = np.full_like(tk, -1)
+    comp[0, :len(keep)] = tk[0, keep]
+    _, a = run(case, cache=cache, topk=bad)
+    _, b = run(case, cache=cache, topk=comp)
+    np.testing.assert_allclose(a, b, rtol=1e-6, atol=1e-7)
+
+
+def test_mla_key_order_within_a_tile():
+    """Permuting the selected entries of a one-tile list changes only the
+    order of FP32 sums."""
+    case = small_case(B=1, S1=1, act=(120,), topk=64)
+    cache = case.cache()
+    tk = case.topk_indices().copy()
+    n = int(case.cur()[0])
+    perm = tk.copy()
+    perm[0, :n] = tk[0, np.random.default_rng(3).permutation(n)]
+    _, a = run(case, cache=cache, topk=tk)
+    _, b = run(case, cache=cache, topk=perm)
+    np.testing.assert_allclose(a, b, rtol=1e-5, atol=1e-7)
+
+
+def test_mla_block_placement_invariance():
+    """Moving the physical blocks and rewriting the block table accordingly
+    leaves every output bit unchanged."""
+    case = small_case(B=2, S1=2, act=(300, 130), topk=64)
+    cache = case.cache()
+    base = run(case, cache=cache, want_f32=False)
+    nb = case.num_blocks
+    perm = np.random.default_rng(11).permutation(nb)      # old block i -> new perm[i]
+    moved = np.empty_like(cache).reshape(nb, case.BS, -1)
+    moved[perm] = cache.reshape(nb, case.BS, -1)
+    bt = np.where(case.block_table >= 0, perm[np.maximum(case.block_table, 0)], -1).astype(np.int32)
+    assert np.array_equal(run(case, cache=moved.reshape(cache.shape), bt=bt, want_f32=False), base)
+
+
+def test_mla_padding_and_unread_bytes_are_not_read():
+    """Bytes 656..671 of every row, and every row no valid entry selects, may
+    hold anything."""
+    case = small_case(B=2, S1=2, act=(300, 130), topk=64, frac_invalid=0.05)
+    cache = case.cache()
+    base = run(case, cache=cache, want_f32=False)
+    noisy = cache.copy()
+    noisy[:, 656:] = np.random.default_rng(5).integers(0, 256, size=noisy[:, 656:].shape)
+    used = case.rows_used()
+    unused = np.setdiff1d(np.arange(cache.shape[0]), used)
+    noisy[unused] = 0x7F        # E4M3 NaN codes
+    assert np.array_equal(run(case, cache=noisy, want_f32=False), base)
+    # and the generator's own sparse cache gives the same result
+    assert np.array_equal(run(case, cache=case.cache(rows=used), want_f32=False), base)
+
+
+def test_mla_group_scale_assignment():
+    """The scale of group g multiplies exactly channels 128g..128g+127 of kn:
+    doubling one group's scale of the single visible key doubles (before the
+    BF16 cast, exactly) that group's output channels only."""
+    case = small_case(B=1, S1=1, act=(1,), topk=4)
+    cache = case.cache()
+    row = selected(case, 0)[0]
+    _, a = run(case, cache=cache)
+    for g in range(4):
+        c2 = cache.copy()
+        sc = c2[row, 640:656].copy().view(np.float32)
+        sc[g] *= 2
+        c2[row, 640:656] = sc.view(np.uint8)
+        _, b = run(case, cache=c2)
+        sel = np.zeros(DN, bool)
+        sel[128 * g:128 * (g + 1)] = True
+        np.testing.assert_array_equal(b[0, :, ~sel], a[0, :, ~sel])
+        np.testing.assert_allclose(b[0, :, sel], 2 * a[0, :, sel], rtol=2 ** -8)
+
+
+def test_mla_rows_subset_matches_full():
+    case = small_case(frac_invalid=0.05)
+    cache = case.cache()
+    full = run(case, cache=cache, want_f32=False)
+    rows = np.array([0, 5, 7, case.T * case.NQ - 1], dtype=np.int64)
+    part = run(case, cache=cache, rows=rows, want_f32=False)
+    flat_f, flat_p = full.reshape(-1, DN), part.reshape(-1, DN)
+    assert np.array_equal(flat_p[rows], flat_f[rows])
+    others = np.setdiff1d(np.arange(flat_p.shape[0]), rows)
+    assert not flat_p[others].any()
+
+
+def test_mla_page_cases_shapes():
+    """The page's decode cases: b=4 s_q=2 lengths [65536, 16381, 666, 15] and
+    b=64 s_q=2 lengths 65536; topk 2048, 128 heads, block size 128."""
+    c = workloads.mla_page_ragged()
+    assert (c.B, c.S1, c.NQ, c.topk, c.BS) == (4, 2, 128, 2048, 128)
+    assert c.cur().tolist() == [2048, 2048, 2048, 2048, 665, 666, 14, 15]
+    tk = c.topk_indices()
+    for t in range(c.T):
+        n = int(c.cur()[t])
+        b, s = divmod(t, c.S1)
+        sel = tk[t, :n]
+        assert len(np.unique(sel)) == n and sel.min() >= 0
+        assert sel.max() < c.act[b] - c.S1 + 1 + s
+        assert (tk[t, n:] == -1).all()
+    c64 = workloads.mla_page_b64()
+    assert (c64.B, c64.S1, int(c64.act.min()), int(c64.act.max())) == (64, 2, 65536, 65536)

@@ -309,6 +309,205 @@ def append(frac_skip: float = 0.05, B: int = 64, lo: int = 512, hi: int = 8192) 
     return AppendCase(ctx=ctx, slot_mapping=slot, seed=seed)
 
 
+# --------------------------------------------------------------------------
+# MLA sparse decode (DeepSeek-V3.2 shape): 128 query heads sharing one latent
+# KV head of 512 "nope" + 64 rope channels; each query token selects `topk`
+# positions of its sequence through top-k indices.
+# --------------------------------------------------------------------------
+
+MLA_DN = 512
+MLA_DR = 64
+MLA_ROW_BYTES = 672     # 656 used bytes padded to 672
+
+
+def _mix64(x: np.ndarray) -> np.ndarray:
+    """splitmix64 finaliser (a counter-based hash) on uint64 arrays."""
+    x = (x ^ (x >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+    x = (x ^ (x >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+    return x ^ (x >> np.uint64(31))
+
+
+def _hashed_words(seed: int, rows: np.ndarray, nwords: int, lane: int) -> np.ndarray:
+    """uint64 [len(rows), nwords]: hashed (seed, lane, row, word) counters, so
+    a row's content depends on its id alone, whatever subset is drawn."""
+    key = _mix64(np.array([seed * 1000003 + lane], dtype=np.uint64))[0]
+    ctr = (np.asarray(rows, dtype=np.uint64)[:, None] * np.uint64(nwords)
+           + np.arange(nwords, dtype=np.uint64)[None, :])
+    with np.errstate(over="ignore"):
+        return _mix64(ctr ^ key)
+
+
+def _uniform01(words: np.ndarray) -> np.ndarray:
+    """float64 in (0, 1) from the top 53 bits."""
+    return ((words >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / (1 << 53))
+
+
+@dataclasses.dataclass
+class MlaCase:
+    """One MLA sparse decode workload. Cache rows are drawn as raw bytes:
+    E4M3 codes with a random sign, exponent field uniform in [6, 15] (values
+    2^-1 .. 448, the upper range an amax/448 group quantiser fills) and a
+    random mantissa; 4 FP32 group scales uniform in [0.004, 0.009]; 64 BF16
+    rope values N(0,1) (truncated to BF16); bytes 656..671 are 0xFF padding,
+    which no step may read."""
+
+    name: str
+    B: int
+    S1: int
+    NQ: int
+    topk: int
+    act: np.ndarray            # int32 [B] kv_act_seqs
+    max_blocks: int
+    num_blocks: int
+    block_table: np.ndarray    # int32 [B, max_blocks], -1 padded
+    seed: int
+    BS: int = 128
+    s2_tile: int = 128
+    frac_invalid: float = 0.0  # share of selected entries replaced by -1
+
+    def __post_init__(self):
+        self._q = None
+        self._topk = None
+
+    @property
+    def T(self) -> int:
+        return self.B * self.S1
+
+    @property
+    def softmax_scale(self) -> float:
+        return float(np.float32(1.0) / np.sqrt(np.float32(MLA_DN + MLA_DR)))
+
+    def cur(self) -> np.ndarray:
+        """int64 [T]: selected keys each query token attends to,
+        clamp(kv_act_seqs[b] - S1 + 1 + s, 0, topk)."""
+        t = np.arange(self.T)
+        c = self.act[t // self.S1].astype(np.int64) - self.S1 + 1 + t % self.S1
+        return np.clip(c, 0, self.topk)
+
+    def topk_indices(self) -> np.ndarray:
+        """int32 [T, topk]: for token (b, s) the first cur entries are distinct
+        positions of its visible prefix [0, kv_act_seqs[b] - S1 + 1 + s) in
+        random order (a share frac_invalid of them replaced by -1); the rest -1."""
+        if self._topk is None:
+            out = np.full((self.T, self.topk), -1, dtype=np.int32)
+            cur = self.cur()
+            for t in range(self.T):
+                n = int(cur[t])
+                if n == 0:
+                    continue
+                b, s = divmod(t, self.S1)
+                prefix = int(self.act[b]) - self.S1 + 1 + s
+                r = _rng(self.seed, 5, t)
+                sel = r.permutation(prefix)[:n] if prefix <= 4 * n else \
+                    r.choice(prefix, size=n, replace=False)
+                if self.frac_invalid > 0:
+                    sel = np.where(r.random(n) < self.frac_invalid, -1, sel)
+                out[t, :n] = sel
+            self._topk = out
+        return self._topk
+
+    def q_bf16(self):
+        """(q_nope, q_rope) BF16 torch CPU tensors [T, NQ, 512] / [T, NQ, 64],
+        N(0,1) rounded to BF16 by the library routine."""
+        import torch
+        if self._q is None:
+            r = _rng(self.seed, 1)
+            qn = r.standard_normal((self.T, self.NQ, MLA_DN), dtype=np.float32)
+            qr = r.standard_normal((self.T, self.NQ, MLA_DR), dtype=np.float32)
+            self._q = (torch.from_numpy(qn).to(torch.bfloat16),
+                       torch.from_numpy(qr).to(torch.bfloat16))
+        return self._q
+
+    def q_bits(self):
+        """(q_nope, q_rope) as uint16 BF16 bit patterns."""
+        import torch
+        qn, qr = self.q_bf16()
+        return (qn.view(torch.int16).numpy().view(np.uint16),
+                qr.view(torch.int16).numpy().view(np.uint16))
+
+    def physical_rows(self, idx: np.ndarray, b: np.ndarray) -> np.ndarray:
+        """int64 physical cache rows of sequence positions idx of batches b
+        (a -1 block is read as block 0)."""
+        blk = self.block_table[b, idx // self.BS].astype(np.int64)
+        return np.maximum(blk, 0) * self.BS + idx % self.BS
+
+    def rows_used(self) -> np.ndarray:
+        """Sorted unique physical rows that valid selected keys read."""
+        tk = self.topk_indices()
+        t = np.repeat(np.arange(self.T), self.topk)
+        idx = tk.reshape(-1).astype(np.int64)
+        b = t // self.S1
+        ok = (idx >= 0) & (idx < self.act[b])
+        return np.unique(self.physical_rows(idx[ok], b[ok]))
+
+    def row_bytes(self, rows: np.ndarray) -> np.ndarray:
+        """uint8 [len(rows), 672]: the packed cache rows with these ids."""
+        rows = np.asarray(rows, dtype=np.int64)
+        n = rows.size
+        out = np.full((n, MLA_ROW_BYTES), 0xFF, dtype=np.uint8)
+        w = _hashed_words(self.seed, rows, MLA_DN // 8, 0).view(np.uint8).reshape(n, MLA_DN)
+        sign = w & np.uint8(0x80)
+        e = (6 + (((w >> np.uint8(3)) & np.uint8(15)).astype(np.uint16) * 10 >> 4)).astype(np.uint8)
+        m = w & np.uint8(7)
+        m = np.where((e == 15) & (m == 7), np.uint8(6), m)
+        out[:, :MLA_DN] = sign | (e << np.uint8(3)) | m
+        u = _uniform01(_hashed_words(self.seed, rows, MLA_DR, 1))
+        v = _uniform01(_hashed_words(self.seed, rows, MLA_DR, 2))
+        rope = (np.sqrt(-2.0 * np.log(u)) * np.cos(2.0 * np.pi * v)).astype(np.float32)
+        out[:, MLA_DN:MLA_DN + 2 * MLA_DR] = (rope.view(np.uint32) >> np.uint32(16)).astype(
+            np.uint16).view(np.uint8).reshape(n, 2 * MLA_DR)
+        sc = (0.004 + 0.005 * _uniform01(_hashed_words(self.seed, rows, 4, 3))).astype(np.float32)
+        out[:, MLA_DN + 2 * MLA_DR:MLA_DN + 2 * MLA_DR + 16] = sc.view(np.uint8).reshape(n, 16)
+        return out
+
+    def cache(self, rows=None) -> np.ndarray:
+        """uint8 [num_blocks*BS, 672]: every row drawn (rows=None), or only the
+        listed rows drawn and the others zero."""
+        total = self.num_blocks * self.BS
+        if rows is None:
+            return self.row_bytes(np.arange(total))
+        c = np.zeros((total, MLA_ROW_BYTES), dtype=np.uint8)
+        c[rows] = self.row_bytes(rows)
+        return c
+
+    def flops(self) -> int:
+        """2 * NQ * (576 + 512) per valid selected key of every query token."""
+        tk = self.topk_indices()
+        t = np.repeat(np.arange(self.T), self.topk)
+        idx = tk.reshape(-1).astype(np.int64)
+        ok = (idx >= 0) & (idx < self.act[t // self.S1])
+        return int(ok.sum()) * 2 * self.NQ * (MLA_DN + MLA_DR + MLA_DN)
+
+
+def mla(name: str, B: int, S1: int, act, *, NQ: int = 128, topk: int = 2048, seed: int,
+        spare: float = 0.10, frac_invalid: float = 0.0, BS: int = 128) -> MlaCase:
+    act = np.asarray(act, dtype=np.int32)
+    need = [max(1, int(math.ceil(int(a) / BS))) for a in act]
+    max_blocks = max(need)
+    num_blocks = max(1, int(math.ceil(sum(need) * (1.0 + spare))))
+    perm = _rng(seed, 0).permutation(num_blocks).astype(np.int32)
+    bt = np.full((B, max_blocks), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        bt[b, :need[b]] = perm[pos:pos + need[b]]
+        pos += need[b]
+    return MlaCase(name=name, B=B, S1=S1, NQ=NQ, topk=topk, act=act, max_blocks=max_blocks,
+                   num_blocks=num_blocks, block_table=bt, seed=seed, BS=BS,
+                   frac_invalid=frac_invalid)
+
+
+def mla_page_ragged() -> MlaCase:
+    """The MLA page's first decode case: b=4, nq=128, n_kv=1, s_q=2, actual
+    sequence lengths [65536, 16381, 666, 15]."""
+    return mla("mla_ragged", 4, 2, [65536, 16381, 666, 15], seed=BASE_SEED + 200)
+
+
+def mla_page_b64() -> MlaCase:
+    """The MLA page's default decode case: b=64, nq=128, n_kv=1, s_q=2, every
+    sequence 65536 long."""
+    return mla("mla_b64", 64, 2, [65536] * 64, seed=BASE_SEED + 201)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "glm": glm,
