@@ -12,6 +12,7 @@ Functions take torch CUDA tensors and work in place (outputs are arguments):
   kv_compress_epilog(...)  BF16 rows to rope (BF16) + grouped E4M3 nope (modes 0/1)
   quantize_rows(...)       per-token E4M3 quantiser (Q, K)
   value_channel_scale(...) per-channel V dequant scale
+  mla_sparse_decode(...)   MLA sparse attention over a packed FP8 latent cache
 """
 from __future__ import annotations
 
@@ -93,6 +94,9 @@ def lib():
         L.pa_fp8_quantize_rows.restype = i32
         L.pa_fp8_value_channel_scale.argtypes = [P, i32, P, i32, i64, i32, i32, P, P]
         L.pa_fp8_value_channel_scale.restype = i32
+        L.pa_mla_sparse_decode.argtypes = [P, P, P, i64, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                           i64, i32, f32, i32, P, P]
+        L.pa_mla_sparse_decode.restype = i32
         _lib = L
         return L
 
@@ -363,3 +367,56 @@ __all__ = [
     "DecodeWorkspace", "cache_scatter", "cache_quant_scatter", "quantize_rows",
     "value_channel_scale",
 ]
+
+
+MLA_ROW_USED = 656
+
+
+class MlaStatus:
+    """A device int the MLA decode kernel ORs a bit into when one of its
+    bounded waits gives up (zeroed at creation)."""
+
+    def __init__(self, device=None):
+        torch = _torch()
+        self.buf = torch.zeros(1, dtype=torch.int32,
+                               device=device if device is not None else torch.cuda.current_device())
+
+    def value(self) -> int:
+        return int(self.buf.item())
+
+
+def mla_sparse_decode(q_nope, q_rope, nope_cache, topk_indices, block_table, kv_act_seqs, out, *,
+                      S1: int, status: MlaStatus, block_size: int = 128, softmax_scale=None,
+                      s2_tile: int = 128, stream=None):
+    """MLA sparse attention with FP8 anti-quantisation (decode), in place.
+
+    q_nope bfloat16 [B*S1, NQ, 512], q_rope bfloat16 [B*S1, NQ, 64];
+    nope_cache uint8 [num_blocks*block_size, row_bytes] packed rows (E4M3 kn |
+    BF16 kr | 4 FP32 scales, row_bytes >= 656); topk_indices int32
+    [B*S1, topk]; block_table int32 [B, max_blocks]; kv_act_seqs int32 [B];
+    out bfloat16 [B*S1, NQ, 512]."""
+    torch = _torch()
+    _need(q_nope, "q_nope", torch.bfloat16)
+    _need(q_rope, "q_rope", torch.bfloat16)
+    _need(nope_cache, "nope_cache", torch.uint8)
+    _need(topk_indices, "topk_indices", torch.int32)
+    _need(block_table, "block_table", torch.int32)
+    _need(kv_act_seqs, "kv_act_seqs", torch.int32)
+    _need(out, "out", torch.bfloat16)
+    T, NQ, dn = q_nope.shape
+    if dn != 512 or tuple(q_rope.shape) != (T, NQ, 64) or tuple(out.shape) != (T, NQ, 512):
+        raise ValueError("q_nope/out must be [T, NQ, 512] and q_rope [T, NQ, 64]")
+    B = kv_act_seqs.shape[0]
+    if T != B * S1 or topk_indices.shape[0] != T:
+        raise ValueError("B*S1 must equal the query token count of q_nope and topk_indices")
+    rows, row_bytes = nope_cache.shape
+    if rows % block_size:
+        raise ValueError("nope_cache rows must be a multiple of block_size")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(576.0)
+    st = lib().pa_mla_sparse_decode(_ptr(q_nope), _ptr(q_rope), _ptr(nope_cache), row_bytes,
+                                    _ptr(topk_indices), _ptr(block_table), _ptr(kv_act_seqs),
+                                    _ptr(out), B, S1, NQ, 1, topk_indices.shape[1], block_size,
+                                    rows // block_size, block_table.shape[1], float(softmax_scale),
+                                    s2_tile, _ptr(status.buf), _stream(stream))
+    _check(st, "pa_mla_sparse_decode")

@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(LIB_DIR, "libpa_fp8.so")
 
-SOURCES = ["status.cu", "cache.cu", "decode.cu"]
+SOURCES = ["status.cu", "cache.cu", "decode.cu", "mla.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I" + INCLUDE]

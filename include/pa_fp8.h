@@ -341,6 +341,64 @@ PA_API pa_status pa_fp8_value_channel_scale(const void* v, int in_dtype,
                                      int64_t total_tokens, int H, int D,
                                      float* v_scale, void* stream);
 
+/* ------------------------------------------------------------------------
+ * MLA sparse attention with FP8 anti-quantisation, decode ([MS] 核心参数与
+ * KV Cache 布局, API 签名与 Decode / Prefill 差异, 计算流程：5 层嵌套循环,
+ * 关键实现细节, 在线反量化与 Online Softmax 的实现细节). [MS] = the page
+ * "PyPTO-Gym 算子实战：DeepSeek V32 MLA 的 Sparse Attention FP8 反量化算子
+ * （Ascend 950PR）解析与验证".
+ *
+ * NQ query heads share one latent KV head (n_kv = 1) of 512 "nope" channels
+ * (kv_lora_rank) plus 64 rope channels. For query token t = b*S1 + s and head
+ * h, over the first cur = clamp(kv_act_seqs[b] - S1 + 1 + s, 0, topk)
+ * entries of topk_indices[t], walked in tiles of s2_tile entries:
+ *   idx  = topk_indices[t][j], a position in sequence b; the packed row
+ *          block_table[b][idx / block_size] * block_size + idx % block_size
+ *          of nope_cache is read (an entry outside [0, kv_act_seqs[b]) takes
+ *          no part; a block id of -1 or outside [0, num_blocks) reads block 0)
+ *   kn   = BF16(FP32(E4M3 code) * scale[channel / 128]), k = [kn, kr] (576)
+ *   S_j  = ([q_nope, q_rope] . k_j) * softmax_scale           (FP32)
+ *   per tile: m = max S_j, p_j = exp(S_j - m), l = sum p_j, P = BF16(p)
+ *             o = P . kn                                       (FP32, 512)
+ *   merge:    M' = max(M, m); O = O exp(M - M') + o exp(m - M');
+ *             L = L exp(M - M') + l exp(m - M')    (the first tile sets them)
+ *   out  = BF16(O / L); a token with no valid entry gets zeros.
+ *
+ * Arguments (device pointers):
+ *   q_nope        BF16 [B*S1, NQ, 512], row t*NQ + h.
+ *   q_rope        BF16 [B*S1, NQ, 64].
+ *   nope_cache    bytes [num_blocks*block_size, row_bytes]: per row 512 E4M3
+ *                 codes, 64 BF16 rope values, 4 FP32 scales (bytes 0..655);
+ *                 the rest of the row is padding and is not read. row_bytes
+ *                 >= 656 and a multiple of 16 ([MS] pads rows to 672).
+ *   topk_indices  int32 [B*S1, topk].
+ *   block_table   int32 [B, max_blocks_per_seq].
+ *   kv_act_seqs   int32 [B]; only the entries the visible count lets through
+ *                 are read, so the table needs no room past each sequence.
+ *   out           BF16 [B*S1, NQ, 512].
+ *   n_kv          1 (anything else is PA_ERR_UNSUPPORTED).
+ *   NQ            a multiple of 64 (PA_ERR_UNSUPPORTED otherwise).
+ *   s2_tile       128, the kernel's tile of selected entries (the tile is a
+ *                 tuning knob on the page; it decides which keys share one
+ *                 tile max, i.e. the BF16 rounding of P). Other values are
+ *                 PA_ERR_UNSUPPORTED.
+ *   status        device int, zeroed by the caller before the first call;
+ *                 a wait inside the kernel that gives up (about 2 s) ORs a
+ *                 non-zero bit into it and the output is undefined.
+ * Alignment: q_nope, q_rope, nope_cache, out 16-byte aligned; status 4-byte.
+ * B = 0 enqueues nothing. Nothing is allocated; the call is asynchronous on
+ * `stream`.
+ * ------------------------------------------------------------------------ */
+PA_API pa_status pa_mla_sparse_decode(const void* q_nope, const void* q_rope,
+                                      const void* nope_cache, int64_t row_bytes,
+                                      const int32_t* topk_indices,
+                                      const int32_t* block_table,
+                                      const int32_t* kv_act_seqs, void* out,
+                                      int B, int S1, int NQ, int n_kv, int topk,
+                                      int block_size, int64_t num_blocks,
+                                      int max_blocks_per_seq, float softmax_scale,
+                                      int s2_tile, int* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for need in ("pa_fp8_decode", "pa_fp8_decode_workspace_size", "pa_fp8_cache_scatter",
                  "pa_fp8_cache_quant_scatter", "pa_fp8_quantize_rows",
-                 "pa_fp8_value_channel_scale", "pa_fp8_kv_compress_epilog", "pa_status_string",
+                 "pa_fp8_value_channel_scale", "pa_fp8_kv_compress_epilog",
+                 "pa_mla_sparse_decode", "pa_status_string",
                  "pa_last_error"):
         assert need in names
 
@@ -147,3 +148,33 @@ def test_kv_compress_epilog_rejects_bad_arguments(L):
     assert b"323" in L.pa_last_error()
     assert f(fake, 8, 16, 16 * 326, 326, fake, 4, 256, fake, 0, 64, 0, 1, None) == 2   # mode 0: 352
     assert f(fake, 8, 16, 15 * 384, 384, fake, 4, 256, fake, 0, 64, 1, 1, None) == 2   # block stride
+
+
+def test_mla_sparse_decode_rejects_bad_arguments(L):
+    """Host validation of the MLA decode: every rejection happens before a
+    launch (no GPU is needed to reach these answers)."""
+    P = ctypes.c_void_p
+    fake = P(256)
+    f = L.pa_mla_sparse_decode
+    scale = ctypes.c_float(1.0 / 24.0)
+
+    def call(**kw):
+        a = dict(qn=fake, qr=fake, cache=fake, row_bytes=672, tk=fake, bt=fake, act=fake, out=fake,
+                 B=4, S1=2, NQ=128, n_kv=1, topk=2048, bs=128, nb=100, mb=512, s2=128, status=fake)
+        a.update(kw)
+        return f(a["qn"], a["qr"], a["cache"], a["row_bytes"], a["tk"], a["bt"], a["act"], a["out"],
+                 a["B"], a["S1"], a["NQ"], a["n_kv"], a["topk"], a["bs"], a["nb"], a["mb"], scale,
+                 a["s2"], a["status"], None)
+
+    assert call(cache=None) == 1
+    assert call(status=None) == 1
+    assert call(row_bytes=640) == 2          # the 656 used bytes do not fit
+    assert call(row_bytes=660) == 2          # not a multiple of 16
+    assert call(topk=0) == 2
+    assert call(S1=0) == 2
+    assert call(n_kv=2) == 5                 # one latent KV head
+    assert call(NQ=96) == 5                  # heads in groups of 64
+    assert call(s2=512) == 5
+    assert b"s2_tile" in L.pa_last_error()
+    assert call(out=P(258)) == 2             # alignment
+    assert call(B=0) == 0                    # nothing to do, nothing enqueued
