@@ -67,6 +67,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["glm45_step", "mla"], default="glm45_step",
+                    help="glm45_step: the GLM-4.5 append + decode step (default); mla: the "
+                         "MLA sparse FP8 decode at the DeepSeek-V3.2 page's b=64 case")
+    ap.add_argument("--mla-batch", type=int, default=64,
+                    help="sequences of the mla workload (64 = the page's case; smaller for "
+                         "profiling captures)")
     ap.add_argument("--copies", type=int, default=0, help="cache copies to rotate (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -310,6 +316,12 @@ def reference_arm(args, rank, world):
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.workload == "mla":
+        if args.impl == "reference":
+            mla_reference_arm(args, rank, world)
+        else:
+            mla_arm(args, rank, world, local)
+        return
     if args.impl == "reference":
         reference_arm(args, rank, world)
         return
@@ -547,6 +559,266 @@ def main():
             "clocks": clk,
             "cpu_baseline": cpu,
             "tokens_per_s": world * case.B * case.S1 * args.steps / (ms_total * 1e-3),
+        }
+        print(json.dumps(line), flush=True)
+    finish_ranks(world)
+
+
+# --------------------------------------------------------------------------
+# MLA sparse FP8 decode (DeepSeek-V3.2 shape)
+# --------------------------------------------------------------------------
+
+MLA_METRIC = ("MLA sparse FP8 decode: achieved BF16 tensor TFLOP/s (% of peak), µs/step at the "
+              "DeepSeek-V3.2 b=64 decode shape")
+MLA_UNIT = "TFLOP/s"
+MLA_WORKLOAD = ("mla_sparse_decode: b=%d s_q=2 nq=128 n_kv=1 topk=2048 kv_lora_rank=512 "
+                "qk_rope_dim=64 block_size=128 kv_act_seqs=65536 (all); 672-byte packed rows "
+                "(E4M3 nope, BF16 rope, 4 FP32 group scales); s2_tile=128")
+MLA_VARIANTS = 2          # top-k selections rotated between steps (each ~172 MB of rows)
+# DRAM traffic of one MLA decode launch on this workload from an ncu capture,
+# valid only for the kernel source it was taken with.
+# Captured on the 16-sequence case and scaled by the selected rows (x4): each
+# row is read from DRAM once, so the traffic grows in proportion.
+MLA_TRAFFIC = {"sources_sha1": "775a64bf2a5c52d0653a25b28b6338bdfddb12e1",
+               "bytes_per_launch": 4 * (54278912 + 303104)}
+
+
+def mla_sources_sha1() -> str:
+    with open(os.path.join(ROOT, "fp8_paged_kv_block_gb300", "csrc", "mla.cu"), "rb") as fh:
+        return hashlib.sha1(fh.read()).hexdigest()
+
+
+def measured_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def mla_host_cache(case, used, rb):
+    """The full packed cache on the host with only the used rows drawn (the
+    rest is never read and is never touched, so it costs no memory)."""
+    host = np.zeros((case.num_blocks * case.BS, workloads.MLA_ROW_BYTES), dtype=np.uint8)
+    host[used] = rb
+    return host
+
+
+def mla_oracle_sample(case, host, budget_s):
+    """Time the oracle on whole query tokens (all heads) until about budget_s
+    of CPU time: (TFLOP/s, tokens, seconds, flops)."""
+    import oracle
+    qn, qr = case.q_bits()
+    tk = case.topk_indices(0)
+    cur = case.cur()
+    NQ = case.NQ
+    done, flops, t0 = 0, 0, time.perf_counter()
+    toks = np.random.default_rng(5).permutation(case.T)
+    for t in toks:
+        rows = np.arange(int(t) * NQ, (int(t) + 1) * NQ, dtype=np.int64)
+        oracle.mla_sparse_decode(qn, qr, host, tk, case.block_table, case.act, S1=case.S1,
+                                 block_size=case.BS, s2_tile=case.s2_tile,
+                                 softmax_scale=case.softmax_scale, rows=rows)
+        b = int(t) // case.S1
+        sel = tk[int(t), :int(cur[t])]
+        nvalid = int(((sel >= 0) & (sel < case.act[b])).sum())
+        flops += nvalid * 2 * NQ * (512 + 64 + 512)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, done, dt, flops
+
+
+def mla_reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    case = workloads.mla_page_b64(args.mla_batch)
+    used = case.rows_used((0,))
+    host = mla_host_cache(case, used, case.row_bytes(used))
+    total_steps = args.steps + args.warmup
+    budget = max(args.cpu_seconds / max(total_steps, 1), 0.5)
+    for _ in range(args.warmup):
+        mla_oracle_sample(case, host, budget)
+    vals = []
+    tok = 0
+    for _ in range(args.steps):
+        v, tok, _, _ = mla_oracle_sample(case, host, budget)
+        vals.append(v)
+    value = statistics.median(vals) if vals else 0.0
+    line = {
+        "impl": "reference", "metric": MLA_METRIC, "value": value, "unit": MLA_UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": case.flops() / (value * 1e12) * 1e3 if value else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
+        "data": "synthetic", "config": {"workload": MLA_WORKLOAD % case.B, "sample_tokens": tok},
+        "cpu_baseline": {"value": value, "unit": MLA_UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d query tokens (all 128 heads) per step; ms_per_step "
+                                   "extrapolated to the 128-token decode by flops" % tok},
+        "e2e": {"value": value, "unit": MLA_UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def mla_arm(args, rank, world, local):
+    import torch
+    import fp8_paged_kv_block_gb300 as pa
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_ranks(world, "nccl", dev)
+    pa.build()
+    pa.lib()
+
+    case = workloads.mla_page_b64(args.mla_batch)
+    V = MLA_VARIANTS
+    used = case.rows_used(range(V))
+    rb = case.row_bytes(used)
+    nrows = case.num_blocks * case.BS
+    cache = torch.zeros((nrows, workloads.MLA_ROW_BYTES), dtype=torch.uint8, device=dev)
+    cache[torch.from_numpy(used).to(dev)] = torch.from_numpy(rb).to(dev)
+    qn_h, qr_h = case.q_bf16()
+    qn, qr = qn_h.to(dev), qr_h.to(dev)
+    tks = [torch.from_numpy(case.topk_indices(v)).to(dev) for v in range(V)]
+    bt = torch.from_numpy(case.block_table).to(dev)
+    act = torch.from_numpy(case.act).to(dev)
+    out = torch.empty((case.T, case.NQ, 512), dtype=torch.bfloat16, device=dev)
+    status = pa.MlaStatus(dev)
+    flops_v = [case.flops(v) for v in range(V)]
+    bytes_v = [case.algorithmic_bytes(v) for v in range(V)]
+
+    def launch(i, q=(qn, qr), tk=None, o=out):
+        pa.mla_sparse_decode(q[0], q[1], cache, tks[i % V] if tk is None else tk, bt, act, o,
+                             S1=case.S1, status=status, block_size=case.BS,
+                             softmax_scale=case.softmax_scale)
+
+    cyc = V * 6
+
+    def capture(fn, n):
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(min(n, V)):
+                fn(i)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                fn(i)
+        return g
+
+    counts = (max(args.warmup, 3), args.steps)
+    graphs = (capture(launch, cyc), {n % cyc: capture(launch, n % cyc) for n in counts if n % cyc})
+
+    def run_steps(gr, n):
+        full, tails = gr
+        for _ in range(n // cyc):
+            full.replay()
+        if n % cyc:
+            tails[n % cyc].replay()
+
+    def timed(gr, n):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200000)
+        e0.record()
+        run_steps(gr, n)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    run_steps(graphs, max(args.warmup, 3))
+    torch.cuda.synchronize()
+    assert status.value() == 0, "MLA decode kernel reported a wait timeout"
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_start = time.perf_counter()
+    ms = timed(graphs, args.steps)
+    while time.perf_counter() - t_start < 1.0:
+        run_steps(graphs, cyc * 4)
+        torch.cuda.synchronize()
+
+    # ---- end to end: queries and selections in from pinned host memory, the
+    # output back, around every launch (one CUDA graph per step) ----
+    h_q = [qn_h.pin_memory(), qr_h.pin_memory()]
+    h_tk = [torch.from_numpy(case.topk_indices(v)).pin_memory() for v in range(V)]
+    d_q = [torch.empty_like(qn), torch.empty_like(qr)]
+    d_tk = torch.empty_like(tks[0])
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_q) + h_tk[0].numel() * 4
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step(i):
+        d_q[0].copy_(h_q[0], non_blocking=True)
+        d_q[1].copy_(h_q[1], non_blocking=True)
+        d_tk.copy_(h_tk[i % V], non_blocking=True)
+        launch(i, q=d_q, tk=d_tk)
+        h_out.copy_(out, non_blocking=True)
+
+    g_e2e = (capture(e2e_step, cyc), {n % cyc: capture(e2e_step, n % cyc) for n in counts if n % cyc})
+    run_steps(g_e2e, max(args.warmup, 3))
+    n_e2e = args.steps
+    ms_e2e = timed(g_e2e, n_e2e)
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    assert status.value() == 0, "MLA decode kernel reported a wait timeout"
+
+    flops_run = sum(flops_v[i % V] for i in range(args.steps))
+    bytes_run = sum(bytes_v[i % V] for i in range(args.steps))
+    us_launch = ms / args.steps * 1e3
+    tflops = flops_run / (ms * 1e-3) / 1e12
+    value = world * tflops
+    peak, peak_src = measured_bf16_peak()
+    hbm_peak, _ = measured_hbm_peak()
+    gbs = bytes_run / (ms * 1e-3) / 1e9
+    traffic = (MLA_TRAFFIC["bytes_per_launch"]
+               if MLA_TRAFFIC["sources_sha1"] == mla_sources_sha1() else None)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = mla_host_cache(case, used, rb)
+        v, tok, dt, _ = mla_oracle_sample(case, host, args.cpu_seconds)
+        cpu = {"value": v, "unit": MLA_UNIT, "cores": 1, "kind": "oracle",
+               "sample": "%d query tokens x 128 heads of the same workload (top-k selection 0), "
+                         "single-threaded C oracle, %.1f s" % (tok, dt)}
+    if rank == 0:
+        line = {
+            "metric": MLA_METRIC, "value": value, "unit": MLA_UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "us_per_step": us_launch, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16+e4m3", "data": "synthetic",
+            "config": {
+                "workload": MLA_WORKLOAD % case.B, "query_tokens": case.T,
+                "keys_per_step": case.keys_read(0),
+                "flops_per_step": flops_v[0], "bytes_per_step": bytes_v[0],
+                "l2": "inputs larger than L2: %d top-k selections rotated (%.0f MB of rows each "
+                      "> %.0f MB L2)" % (V, case.keys_read(0) * 656 / 1e6,
+                                         torch.cuda.get_device_properties(dev).L2_cache_size / 1e6),
+                "timing": "CUDA graphs replayed on one stream, CUDA events over the K steps",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+            },
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "kernel": "pa_mla_sparse_decode", "achieved": tflops,
+                         "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "traffic": traffic, "peak_source": peak_src,
+                         "us_per_launch": us_launch,
+                         "algorithmic_flops_per_launch": flops_v[0],
+                         "hbm": {"achieved_gbs": gbs, "peak_gbs": hbm_peak, "frac": gbs / hbm_peak,
+                                 "algorithmic_bytes_per_launch": bytes_v[0]}},
+            "e2e": {"value": world * flops_run / (ms_e2e * 1e-3) / 1e12, "unit": MLA_UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "us_per_step": ms_e2e / n_e2e * 1e3,
+                    "issue": "pinned H2D copies of the queries and the step's top-k selection, "
+                             "the decode, the D2H copy of the output: one CUDA graph per step"},
+            "clocks": clk,
+            "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     finish_ranks(world)

@@ -337,6 +337,20 @@ def _hashed_words(seed: int, rows: np.ndarray, nwords: int, lane: int) -> np.nda
         return _mix64(ctr ^ key)
 
 
+def _code_of_byte() -> np.ndarray:
+    """Random byte -> E4M3 code: its sign bit, exponent field 6 + (bits 3..6
+    scaled to 0..9), its low 3 bits as mantissa; the NaN pattern becomes the
+    largest finite magnitude's neighbour."""
+    b = np.arange(256, dtype=np.int64)
+    e = 6 + (((b >> 3) & 15) * 10 >> 4)
+    m = b & 7
+    m = np.where((e == 15) & (m == 7), 6, m)
+    return ((b & 0x80) | (e << 3) | m).astype(np.uint8)
+
+
+_CODE_OF_BYTE = _code_of_byte()
+
+
 def _uniform01(words: np.ndarray) -> np.ndarray:
     """float64 in (0, 1) from the top 53 bits."""
     return ((words >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / (1 << 53))
@@ -367,7 +381,7 @@ class MlaCase:
 
     def __post_init__(self):
         self._q = None
-        self._topk = None
+        self._topk = {}
 
     @property
     def T(self) -> int:
@@ -384,11 +398,12 @@ class MlaCase:
         c = self.act[t // self.S1].astype(np.int64) - self.S1 + 1 + t % self.S1
         return np.clip(c, 0, self.topk)
 
-    def topk_indices(self) -> np.ndarray:
+    def topk_indices(self, variant: int = 0) -> np.ndarray:
         """int32 [T, topk]: for token (b, s) the first cur entries are distinct
         positions of its visible prefix [0, kv_act_seqs[b] - S1 + 1 + s) in
-        random order (a share frac_invalid of them replaced by -1); the rest -1."""
-        if self._topk is None:
+        random order (a share frac_invalid of them replaced by -1); the rest -1.
+        Each variant is an independent draw (a different selection)."""
+        if variant not in self._topk:
             out = np.full((self.T, self.topk), -1, dtype=np.int32)
             cur = self.cur()
             for t in range(self.T):
@@ -397,14 +412,14 @@ class MlaCase:
                     continue
                 b, s = divmod(t, self.S1)
                 prefix = int(self.act[b]) - self.S1 + 1 + s
-                r = _rng(self.seed, 5, t)
+                r = _rng(self.seed, 5, t) if variant == 0 else _rng(self.seed, 5, t, variant)
                 sel = r.permutation(prefix)[:n] if prefix <= 4 * n else \
                     r.choice(prefix, size=n, replace=False)
                 if self.frac_invalid > 0:
                     sel = np.where(r.random(n) < self.frac_invalid, -1, sel)
                 out[t, :n] = sel
-            self._topk = out
-        return self._topk
+            self._topk[variant] = out
+        return self._topk[variant]
 
     def q_bf16(self):
         """(q_nope, q_rope) BF16 torch CPU tensors [T, NQ, 512] / [T, NQ, 64],
@@ -431,33 +446,44 @@ class MlaCase:
         blk = self.block_table[b, idx // self.BS].astype(np.int64)
         return np.maximum(blk, 0) * self.BS + idx % self.BS
 
-    def rows_used(self) -> np.ndarray:
-        """Sorted unique physical rows that valid selected keys read."""
-        tk = self.topk_indices()
+    def _valid(self, variant: int):
+        """(flat positions, batch of each) of the valid visible selected entries."""
+        tk = self.topk_indices(variant)
+        cur = self.cur()
         t = np.repeat(np.arange(self.T), self.topk)
+        j = np.tile(np.arange(self.topk), self.T)
         idx = tk.reshape(-1).astype(np.int64)
         b = t // self.S1
-        ok = (idx >= 0) & (idx < self.act[b])
-        return np.unique(self.physical_rows(idx[ok], b[ok]))
+        ok = (j < cur[t]) & (idx >= 0) & (idx < self.act[b])
+        return idx[ok], b[ok]
+
+    def rows_used(self, variants=(0,)) -> np.ndarray:
+        """Sorted unique physical rows that valid selected keys read."""
+        parts = [self.physical_rows(*self._valid(v)) for v in variants]
+        return np.unique(np.concatenate(parts))
+
+    def keys_read(self, variant: int = 0) -> int:
+        """Valid selected (token, key) pairs: the packed rows one decode reads."""
+        return int(self._valid(variant)[0].size)
 
     def row_bytes(self, rows: np.ndarray) -> np.ndarray:
         """uint8 [len(rows), 672]: the packed cache rows with these ids."""
         rows = np.asarray(rows, dtype=np.int64)
         n = rows.size
-        out = np.full((n, MLA_ROW_BYTES), 0xFF, dtype=np.uint8)
+        out = np.empty((n, MLA_ROW_BYTES), dtype=np.uint8)
+        out[:, 656:] = 0xFF
         w = _hashed_words(self.seed, rows, MLA_DN // 8, 0).view(np.uint8).reshape(n, MLA_DN)
-        sign = w & np.uint8(0x80)
-        e = (6 + (((w >> np.uint8(3)) & np.uint8(15)).astype(np.uint16) * 10 >> 4)).astype(np.uint8)
-        m = w & np.uint8(7)
-        m = np.where((e == 15) & (m == 7), np.uint8(6), m)
-        out[:, :MLA_DN] = sign | (e << np.uint8(3)) | m
-        u = _uniform01(_hashed_words(self.seed, rows, MLA_DR, 1))
-        v = _uniform01(_hashed_words(self.seed, rows, MLA_DR, 2))
-        rope = (np.sqrt(-2.0 * np.log(u)) * np.cos(2.0 * np.pi * v)).astype(np.float32)
+        out[:, :MLA_DN] = _CODE_OF_BYTE[w]
+        h = _hashed_words(self.seed, rows, MLA_DR, 1)
+        u = ((h & np.uint64(0xFFFFFFFF)).astype(np.float32) + 0.5) * np.float32(2.0 ** -32)
+        v = ((h >> np.uint64(32)).astype(np.float32) + 0.5) * np.float32(2.0 ** -32)
+        rope = np.sqrt(np.float32(-2.0) * np.log(u)) * np.cos(np.float32(2.0 * np.pi) * v)
         out[:, MLA_DN:MLA_DN + 2 * MLA_DR] = (rope.view(np.uint32) >> np.uint32(16)).astype(
             np.uint16).view(np.uint8).reshape(n, 2 * MLA_DR)
-        sc = (0.004 + 0.005 * _uniform01(_hashed_words(self.seed, rows, 4, 3))).astype(np.float32)
-        out[:, MLA_DN + 2 * MLA_DR:MLA_DN + 2 * MLA_DR + 16] = sc.view(np.uint8).reshape(n, 16)
+        h = _hashed_words(self.seed, rows, 2, 2)
+        s4 = np.stack([h & np.uint64(0xFFFFFFFF), h >> np.uint64(32)], axis=-1).reshape(n, 4)
+        sc = (np.float32(0.004) + np.float32(0.005 * 2.0 ** -32) * s4.astype(np.float32))
+        out[:, MLA_DN + 2 * MLA_DR:656] = sc.astype(np.float32).view(np.uint8).reshape(n, 16)
         return out
 
     def cache(self, rows=None) -> np.ndarray:
@@ -470,13 +496,17 @@ class MlaCase:
         c[rows] = self.row_bytes(rows)
         return c
 
-    def flops(self) -> int:
-        """2 * NQ * (576 + 512) per valid selected key of every query token."""
-        tk = self.topk_indices()
-        t = np.repeat(np.arange(self.T), self.topk)
-        idx = tk.reshape(-1).astype(np.int64)
-        ok = (idx >= 0) & (idx < self.act[t // self.S1])
-        return int(ok.sum()) * 2 * self.NQ * (MLA_DN + MLA_DR + MLA_DN)
+    def flops(self, variant: int = 0) -> int:
+        """2 * NQ * (576 + 512) per valid selected key of every query token:
+        the two contractions."""
+        return self.keys_read(variant) * 2 * self.NQ * (MLA_DN + MLA_DR + MLA_DN)
+
+    def algorithmic_bytes(self, variant: int = 0) -> int:
+        """Bytes one decode must move at minimum: the 656 used bytes of every
+        selected row, the BF16 queries and output, the selected indices, the
+        lengths (block-table reads are not counted)."""
+        return (self.keys_read(variant) * 656 + self.T * self.NQ * (MLA_DN + MLA_DR) * 2
+                + self.T * self.NQ * MLA_DN * 2 + int(self.cur().sum()) * 4 + self.B * 4)
 
 
 def mla(name: str, B: int, S1: int, act, *, NQ: int = 128, topk: int = 2048, seed: int,
@@ -502,10 +532,11 @@ def mla_page_ragged() -> MlaCase:
     return mla("mla_ragged", 4, 2, [65536, 16381, 666, 15], seed=BASE_SEED + 200)
 
 
-def mla_page_b64() -> MlaCase:
+def mla_page_b64(B: int = 64) -> MlaCase:
     """The MLA page's default decode case: b=64, nq=128, n_kv=1, s_q=2, every
-    sequence 65536 long."""
-    return mla("mla_b64", 64, 2, [65536] * 64, seed=BASE_SEED + 201)
+    sequence 65536 long (B other than 64: the same case with fewer or more
+    sequences)."""
+    return mla("mla_b%d" % B, B, 2, [65536] * B, seed=BASE_SEED + 201)
 
 
 WORKLOADS = {
