@@ -62,7 +62,10 @@ struct MlaSmem {
     uint8_t qt[kNC][kQChunk];         // the 64 heads' queries
     float red[2][4][kHG];             // per lane quarter: column max / column sum
     float wrow[kConsWarps][32];       // per consumer warp: one broadcast row
-    uint64_t q_full, k_full, k_empty, s_full[2], s_empty[2], p_full, o_done, drain;
+    // k_full[i] (i < 4): chunks 2i, 2i+1 of the tile written; k_full[4]: the rope
+    // chunk. k_empty[g]: C2's channel group g (chunks 2g, 2g+1) done; after
+    // group 3 P^T in chunk 8 is free too.
+    uint64_t q_full, k_full[5], k_empty[4], s_full[2], s_empty[2], p_full, o_done, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -216,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, kProdWarps);
-        mbar_init(&sm.k_full, kProdWarps);
-        mbar_init(&sm.k_empty, 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&sm.k_full[i], kProdWarps);
+        for (int i = 0; i < 4; ++i) mbar_init(&sm.k_empty[i], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.s_empty[i], kConsWarps);
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
         const int rr = lane >> 3, cu = lane & 7;
         for (int t = 0; t < ntiles; ++t) {
             uint4 kn[kGroupsPerProd][4], sc[kGroupsPerProd];
-            int64_t ro[kGroupsPerProd];
+            int64_t ro[kGroupsPerProd];   // byte offset of the row, -1 for an entry that takes no part
 #pragma unroll
             for (int gi = 0; gi < kGroupsPerProd; ++gi) {
                 const int rg = pw + kProdWarps * gi;
@@ -291,14 +294,46 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
 #pragma unroll
                     for (int i = 0; i < 4; ++i) kn[gi][i] = ldg_nc16(src + 16 * (cu + 8 * i));
                     sc[gi] = ldg_nc16(src + kDn + 2 * kDr);
+                    // the rope bytes are copied once chunk 8 is free: bring them to L2 now
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kDn + 16 * cu));
                 } else {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) kn[gi][i] = make_uint4(0, 0, 0, 0);
                     sc[gi] = make_uint4(0, 0, 0, 0);
                 }
             }
-            // the previous tile's C2 has read the key chunks and P^T
-            if (t > 0) mbar_wait(&sm.k_empty, static_cast<uint32_t>(t - 1) & 1u, p.err, 2, &sm.abort);
+            // chunk pair i (channels 128i..128i+127) as soon as the previous
+            // tile's C2 has read it
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (t > 0) mbar_wait(&sm.k_empty[i], static_cast<uint32_t>(t - 1) & 1u, p.err, 2, &sm.abort);
+                uint8_t* chunk = sm.kt[(cu >> 2) + 2 * i];
+                const int u0 = 2 * (cu & 3);
+#pragma unroll
+                for (int gi = 0; gi < kGroupsPerProd; ++gi) {
+                    const int rg = pw + kProdWarps * gi;
+                    if (rg >= kRowGroups) continue;
+                    const int k = 4 * rg + rr;
+                    const uint4 c8 = kn[gi][i];
+                    const float f = __uint_as_float(i == 0 ? sc[gi].x : i == 1 ? sc[gi].y : i == 2 ? sc[gi].z : sc[gi].w);
+                    uint4 lo, hi;
+                    lo.x = dq2(c8.x & 0xFFFFu, f);
+                    lo.y = dq2(c8.x >> 16, f);
+                    lo.z = dq2(c8.y & 0xFFFFu, f);
+                    lo.w = dq2(c8.y >> 16, f);
+                    hi.x = dq2(c8.z & 0xFFFFu, f);
+                    hi.y = dq2(c8.z >> 16, f);
+                    hi.z = dq2(c8.w & 0xFFFFu, f);
+                    hi.w = dq2(c8.w >> 16, f);
+                    *reinterpret_cast<uint4*>(chunk + sw128(k, u0)) = lo;
+                    *reinterpret_cast<uint4*>(chunk + sw128(k, u0 + 1)) = hi;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.k_full[i]);
+            }
+            // the rope chunk (free once the previous C2's last group is done,
+            // which the wait of pair 3 covered)
 #pragma unroll
             for (int gi = 0; gi < kGroupsPerProd; ++gi) {
                 const int rg = pw + kProdWarps * gi;
@@ -311,36 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
                         *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
                 }
             }
-#pragma unroll
-            for (int gi = 0; gi < kGroupsPerProd; ++gi) {
-                const int rg = pw + kProdWarps * gi;
-                if (rg >= kRowGroups) continue;
-                const int k = 4 * rg + rr;
-                const float s4[4] = {__uint_as_float(sc[gi].x), __uint_as_float(sc[gi].y),
-                                     __uint_as_float(sc[gi].z), __uint_as_float(sc[gi].w)};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 c8 = kn[gi][i];
-                    const float f = s4[i];
-                    uint4 lo, hi;
-                    lo.x = dq2(c8.x & 0xFFFFu, f);
-                    lo.y = dq2(c8.x >> 16, f);
-                    lo.z = dq2(c8.y & 0xFFFFu, f);
-                    lo.w = dq2(c8.y >> 16, f);
-                    hi.x = dq2(c8.z & 0xFFFFu, f);
-                    hi.y = dq2(c8.z >> 16, f);
-                    hi.z = dq2(c8.w & 0xFFFFu, f);
-                    hi.w = dq2(c8.w >> 16, f);
-                    uint8_t* chunk = sm.kt[(cu >> 2) + 2 * i];
-                    const int u0 = 2 * (cu & 3);
-                    *reinterpret_cast<uint4*>(chunk + sw128(k, u0)) = lo;
-                    *reinterpret_cast<uint4*>(chunk + sw128(k, u0 + 1)) = hi;
-                }
-            }
             cp_async_wait_all();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.k_full);
+            if (lane == 0) mbar_arrive(&sm.k_full[4]);
         }
     } else if (warp == kMmaWarp) {
         // ================================ MMA issue ================================
@@ -349,11 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
             constexpr uint32_t kIdescO = idesc_bf16(128, kHG, 1, 1);   // MN-major V^T and P^T
             mbar_wait(&sm.q_full, 0, p.err, 1, &sm.abort);
             for (int t = 0; t < ntiles; ++t) {
-                mbar_wait(&sm.k_full, static_cast<uint32_t>(t) & 1u, p.err, 16, &sm.abort);
                 mbar_wait(&sm.s_empty[t & 1], (static_cast<uint32_t>(t >> 1) & 1u) ^ 1u, p.err, 32, &sm.abort);
-                tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>((t & 1) * kHG);
                 for (int c = 0; c < kNC; ++c) {
+                    if ((c & 1) == 0) {   // chunks 2i, 2i+1 (and the rope chunk 8) as they land
+                        mbar_wait(&sm.k_full[c >> 1], static_cast<uint32_t>(t) & 1u, p.err, 16, &sm.abort);
+                        tc_fence_after();
+                    }
                     const uint64_t ad = smem_desc(smem_u32(sm.kt[c]), 16, 1024, kSmem128BSwizzle);
                     const uint64_t bd = smem_desc(smem_u32(sm.qt[c]), 16, 1024, kSmem128BSwizzle);
 #pragma unroll
@@ -373,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
                                                       kSmem128BSwizzle);
                         umma_bf16(tmem + kOCol + 64 * g, ad, bd, kIdescO, (t > 0 || ks > 0) ? 1u : 0u);
                     }
+                    umma_commit(&sm.k_empty[g]);
                 }
-                umma_commit(&sm.k_empty);
                 umma_commit(&sm.o_done);
             }
             umma_commit(&sm.drain);
@@ -561,6 +572,8 @@ extern "C" pa_status pa_mla_sparse_decode(const void* q_nope, const void* q_rope
                "pa_mla_sparse_decode: row_bytes %lld must be >= 656 and a multiple of 16",
                static_cast<long long>(row_bytes));
     PA_REQUIRE(std::isfinite(softmax_scale), PA_ERR_INVALID, "pa_mla_sparse_decode: softmax_scale not finite");
+    PA_REQUIRE(num_blocks * block_size <= 0x7FFFFFFF, PA_ERR_UNSUPPORTED,
+               "pa_mla_sparse_decode: more than 2^31 - 1 cache rows");
     PA_REQUIRE(n_kv == 1, PA_ERR_UNSUPPORTED, "pa_mla_sparse_decode: n_kv %d (one latent KV head is built)", n_kv);
     PA_REQUIRE(NQ % kHG == 0, PA_ERR_UNSUPPORTED, "pa_mla_sparse_decode: NQ %d (a multiple of 64 is built)", NQ);
     PA_REQUIRE(s2_tile == kNK, PA_ERR_UNSUPPORTED, "pa_mla_sparse_decode: s2_tile %d (128 is built)", s2_tile);

@@ -370,7 +370,9 @@ PA_API pa_status pa_fp8_value_channel_scale(const void* v, int in_dtype,
  *   nope_cache    bytes [num_blocks*block_size, row_bytes]: per row 512 E4M3
  *                 codes, 64 BF16 rope values, 4 FP32 scales (bytes 0..655);
  *                 the rest of the row is padding and is not read. row_bytes
- *                 >= 656 and a multiple of 16 ([MS] pads rows to 672).
+ *                 >= 656 and a multiple of 16 ([MS] pads rows to 672); at
+ *                 most 2^31 - 1 rows (PA_ERR_UNSUPPORTED otherwise). E4M3
+ *                 NaN codes are out of contract.
  *   topk_indices  int32 [B*S1, topk].
  *   block_table   int32 [B, max_blocks_per_seq].
  *   kv_act_seqs   int32 [B]; only the entries the visible count lets through

@@ -151,10 +151,11 @@ def test_mla_page_ragged_case_full(pa):
     gpu = run_gpu(pa, case, cache)
     _, ref = run_oracle(case, cache)
     d = check_close(gpu, ref, abs_weighted(case, cache))
-    # most outputs round to the very same BF16 value
+    # most outputs round to the very same BF16 value, and the mean error is
+    # within half a BF16 step (2^-8 relative) of the mean magnitude
     same = (gpu == oracle.bf16_from_float(ref.reshape(-1)).reshape(gpu.shape)).mean()
     assert same > 0.95, same
-    assert d.mean() < 1e-4
+    assert d.mean() <= 2.0 ** -8 * np.abs(ref).mean(), (d.mean(), np.abs(ref).mean())
 
 
 def test_mla_row_pitch_and_block_size(pa):
