@@ -6,11 +6,12 @@
 //
 // One CTA per (query token, group of 64 query heads). The token's selected
 // keys are walked in tiles of 128:
-//   producers (7 warps)  gather each selected row (top-k index -> block table
-//                        -> 656-byte packed row), dequantise the E4M3 nope part
-//                        by its 128-channel group scale to BF16 and write the
-//                        576-wide BF16 key rows into shared memory as nine
-//                        64-channel chunks in the 128-byte-swizzled layout;
+//   producers (7 warps)  gather half of the selected rows (top-k index -> block
+//                        table -> 656-byte packed row), dequantise the E4M3 nope
+//                        part by its 128-channel group scale to BF16 and write
+//                        the 576-wide BF16 key rows into shared memory as nine
+//                        64-channel chunks in the 128-byte-swizzled layout (the
+//                        consumers do the other half between their softmax steps);
 //   MMA warp (1 thread)  C1: S^T[key][head] = K[key][576] . Q[head][576]^T
 //                        (tcgen05 kind::f16, M = 128 keys, N = 64 heads, FP32 in
 //                        tensor memory); C2: O^T[chan][head] += V^T[chan][key] .
@@ -45,8 +46,13 @@ constexpr int kKChunk = kNK * 128;  // bytes per key chunk (128 rows x 128 B)
 constexpr int kQChunk = kHG * 128;
 constexpr int kConsWarps = 8;
 constexpr int kProdWarps = 7;       // 16 warps in all: 4 per SM sub-partition, 128 registers each
-constexpr int kRowGroups = kNK / 4;                                   // 4 key rows per group
-constexpr int kGroupsPerProd = (kRowGroups + kProdWarps - 1) / kProdWarps;
+constexpr int kRowGroups = kNK / 4;   // 4 key rows per group
+// Row groups 0..15 of a tile are dequantised by the 7 producer warps (group
+// rg by warp rg % 7, up to 3 each), 16..31 by the 8 consumer warps (group rg
+// by consumer warp (rg - 16) % 8, 2 each) once they have handed P^T to C2.
+constexpr int kProdGroups = kRowGroups / 2;
+constexpr int kGroupsPerProd = (kProdGroups + kProdWarps - 1) / kProdWarps;
+constexpr int kGroupsPerCons = (kRowGroups - kProdGroups) / kConsWarps;
 constexpr int kProdWarp0 = kConsWarps;
 constexpr int kMmaWarp = kConsWarps + kProdWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
@@ -195,6 +201,121 @@ __device__ __forceinline__ float col_reduce(float (&v)[32], int lane)
     return v[0];
 }
 
+// ---- key rows: a warp handles row groups rg = rg0 + step * gi (gi < NG, rg <
+// lim); lane (rr, cu) handles row 4 rg + rr and its 16-byte units cu + 8 i:
+// unit U holds channels 16U..16U+15, i.e. chunk U / 4 and scale group i ----
+
+// Byte offset of each row in the cache, -1 for an entry that takes no part
+// (past the visible count, -1, or past the sequence end).
+template <int NG>
+__device__ __forceinline__ void rows_locate(const MlaParams& p, int t, int cur, int act, int b, int64_t tk_base,
+                                            int rg0, int step, int lim, int rr, int64_t (&ro)[NG])
+{
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+        const int rg = rg0 + step * gi;
+        ro[gi] = -1;
+        if (rg < lim) {
+            const int j = t * kNK + 4 * rg + rr;
+            const int idx = j < cur ? __ldg(p.topk_idx + tk_base + j) : -1;
+            if (idx >= 0 && idx < act) {
+                const int bi = idx / p.BS;   // past the table's width: out of contract, block 0
+                int blk = bi < p.max_blocks ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + bi)
+                                            : 0;
+                if (blk < 0 || blk >= p.num_blocks) blk = 0;
+                ro[gi] = (static_cast<int64_t>(blk) * p.BS + idx % p.BS) * p.row_bytes;
+            }
+        }
+    }
+}
+
+// The codes and the scale unit of each row into registers (zeros for rows
+// that take no part); the rope bytes are brought to L2 for the later copy.
+template <int NG>
+__device__ __forceinline__ void rows_load(const MlaParams& p, const int64_t (&ro)[NG], int cu, uint4 (&kn)[NG][4],
+                                          uint4 (&sc)[NG])
+{
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+        if (ro[gi] >= 0) {
+            const uint8_t* src = p.cache + ro[gi];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) kn[gi][i] = ldg_nc16(src + 16 * (cu + 8 * i));
+            sc[gi] = ldg_nc16(src + kDn + 2 * kDr);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kDn + 16 * cu));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) kn[gi][i] = make_uint4(0, 0, 0, 0);
+            sc[gi] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// Whole rows (656 bytes, at most six 128-byte lines) to L2 ahead of time.
+template <int NG>
+__device__ __forceinline__ void rows_prefetch_l2(const MlaParams& p, const int64_t (&ro)[NG], int cu)
+{
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi)
+        if (ro[gi] >= 0 && cu < 6) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.cache + ro[gi] + 128 * cu));
+}
+
+// Dequantise the rows' unit i (channels 128 i + 16 cu .. + 15 of each row's
+// group i) into chunk pair i, and the rope chunk; each step is announced on
+// k_full once the previous tile's C2 has released the chunks.
+template <int NG>
+__device__ __forceinline__ void rows_produce(MlaSmem& sm, const MlaParams& p, int t, const int64_t (&ro)[NG],
+                                             const uint4 (&kn)[NG][4], const uint4 (&sc)[NG], int rg0, int step,
+                                             int lim, int rr, int cu, int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (t > 0) mbar_wait(&sm.k_empty[i], static_cast<uint32_t>(t - 1) & 1u, p.err, 2, &sm.abort);
+        uint8_t* chunk = sm.kt[(cu >> 2) + 2 * i];
+        const int u0 = 2 * (cu & 3);
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            const int rg = rg0 + step * gi;
+            if (rg >= lim) continue;
+            const int k = 4 * rg + rr;
+            const uint4 c8 = kn[gi][i];
+            const float f = __uint_as_float(i == 0 ? sc[gi].x : i == 1 ? sc[gi].y : i == 2 ? sc[gi].z : sc[gi].w);
+            uint4 lo, hi;
+            lo.x = dq2(c8.x & 0xFFFFu, f);
+            lo.y = dq2(c8.x >> 16, f);
+            lo.z = dq2(c8.y & 0xFFFFu, f);
+            lo.w = dq2(c8.y >> 16, f);
+            hi.x = dq2(c8.z & 0xFFFFu, f);
+            hi.y = dq2(c8.z >> 16, f);
+            hi.z = dq2(c8.w & 0xFFFFu, f);
+            hi.w = dq2(c8.w >> 16, f);
+            *reinterpret_cast<uint4*>(chunk + sw128(k, u0)) = lo;
+            *reinterpret_cast<uint4*>(chunk + sw128(k, u0 + 1)) = hi;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.k_full[i]);
+    }
+    // the rope chunk: free once the previous C2's last group is done, which
+    // the wait for pair 3 covered
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+        const int rg = rg0 + step * gi;
+        if (rg < lim) {
+            const int k = 4 * rg + rr;
+            uint8_t* dst = sm.kt[8] + sw128(k, cu);
+            if (ro[gi] >= 0)
+                cp_async16(dst, p.cache + ro[gi] + kDn + 16 * cu, 16);
+            else
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.k_full[4]);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -219,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, kProdWarps);
-        for (int i = 0; i < 5; ++i) mbar_init(&sm.k_full[i], kProdWarps);
+        for (int i = 0; i < 5; ++i) mbar_init(&sm.k_full[i], kProdWarps + kConsWarps);
         for (int i = 0; i < 4; ++i) mbar_init(&sm.k_empty[i], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
@@ -263,93 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.q_full);
         }
-        // Row group rg (key rows 4 rg .. 4 rg + 3) goes to producer warp rg % 7.
-        // Lane (rr, cu) handles row 4 rg + rr and its 16-byte units cu + 8 i:
-        // unit U holds channels 16U..16U+15, i.e. chunk U / 4 and scale group i.
         const int rr = lane >> 3, cu = lane & 7;
         for (int t = 0; t < ntiles; ++t) {
+            int64_t ro[kGroupsPerProd];
             uint4 kn[kGroupsPerProd][4], sc[kGroupsPerProd];
-            int64_t ro[kGroupsPerProd];   // byte offset of the row, -1 for an entry that takes no part
-#pragma unroll
-            for (int gi = 0; gi < kGroupsPerProd; ++gi) {
-                const int rg = pw + kProdWarps * gi;
-                ro[gi] = -1;
-                if (rg < kRowGroups) {
-                    const int j = t * kNK + 4 * rg + rr;
-                    const int idx = j < cur ? __ldg(p.topk_idx + tk_base + j) : -1;
-                    if (idx >= 0 && idx < act) {
-                        const int bi = idx / p.BS;   // past the table's width: out of contract, block 0
-                        int blk = bi < p.max_blocks
-                                      ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + bi)
-                                      : 0;
-                        if (blk < 0 || blk >= p.num_blocks) blk = 0;
-                        ro[gi] = (static_cast<int64_t>(blk) * p.BS + idx % p.BS) * p.row_bytes;
-                    }
-                }
-            }
-#pragma unroll
-            for (int gi = 0; gi < kGroupsPerProd; ++gi) {
-                if (ro[gi] >= 0) {
-                    const uint8_t* src = p.cache + ro[gi];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) kn[gi][i] = ldg_nc16(src + 16 * (cu + 8 * i));
-                    sc[gi] = ldg_nc16(src + kDn + 2 * kDr);
-                    // the rope bytes are copied once chunk 8 is free: bring them to L2 now
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kDn + 16 * cu));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) kn[gi][i] = make_uint4(0, 0, 0, 0);
-                    sc[gi] = make_uint4(0, 0, 0, 0);
-                }
-            }
-            // chunk pair i (channels 128i..128i+127) as soon as the previous
-            // tile's C2 has read it
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (t > 0) mbar_wait(&sm.k_empty[i], static_cast<uint32_t>(t - 1) & 1u, p.err, 2, &sm.abort);
-                uint8_t* chunk = sm.kt[(cu >> 2) + 2 * i];
-                const int u0 = 2 * (cu & 3);
-#pragma unroll
-                for (int gi = 0; gi < kGroupsPerProd; ++gi) {
-                    const int rg = pw + kProdWarps * gi;
-                    if (rg >= kRowGroups) continue;
-                    const int k = 4 * rg + rr;
-                    const uint4 c8 = kn[gi][i];
-                    const float f = __uint_as_float(i == 0 ? sc[gi].x : i == 1 ? sc[gi].y : i == 2 ? sc[gi].z : sc[gi].w);
-                    uint4 lo, hi;
-                    lo.x = dq2(c8.x & 0xFFFFu, f);
-                    lo.y = dq2(c8.x >> 16, f);
-                    lo.z = dq2(c8.y & 0xFFFFu, f);
-                    lo.w = dq2(c8.y >> 16, f);
-                    hi.x = dq2(c8.z & 0xFFFFu, f);
-                    hi.y = dq2(c8.z >> 16, f);
-                    hi.z = dq2(c8.w & 0xFFFFu, f);
-                    hi.w = dq2(c8.w >> 16, f);
-                    *reinterpret_cast<uint4*>(chunk + sw128(k, u0)) = lo;
-                    *reinterpret_cast<uint4*>(chunk + sw128(k, u0 + 1)) = hi;
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.k_full[i]);
-            }
-            // the rope chunk (free once the previous C2's last group is done,
-            // which the wait of pair 3 covered)
-#pragma unroll
-            for (int gi = 0; gi < kGroupsPerProd; ++gi) {
-                const int rg = pw + kProdWarps * gi;
-                if (rg < kRowGroups) {
-                    const int k = 4 * rg + rr;
-                    uint8_t* dst = sm.kt[8] + sw128(k, cu);
-                    if (ro[gi] >= 0)
-                        cp_async16(dst, p.cache + ro[gi] + kDn + 16 * cu, 16);
-                    else
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-                }
-            }
-            cp_async_wait_all();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.k_full[4]);
+            rows_locate<kGroupsPerProd>(p, t, cur, act, b, tk_base, pw, kProdWarps, kProdGroups, rr, ro);
+            rows_load<kGroupsPerProd>(p, ro, cu, kn, sc);
+            rows_produce<kGroupsPerProd>(sm, p, t, ro, kn, sc, pw, kProdWarps, kProdGroups, rr, cu, lane);
         }
     } else if (warp == kMmaWarp) {
         // ================================ MMA issue ================================
@@ -396,6 +437,21 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
         // ================================ consumers ================================
         const int q4 = warp & 3, hf = warp >> 2;
         const int key = 32 * q4 + lane;                 // tensor memory lane of S^T / O^T
+        // this warp's share of the key rows (row groups 16 + warp, 24 + warp):
+        // tile 0 now, tile t+1 once P^T of tile t is handed to C2
+        const int rr = lane >> 3, cu = lane & 7;
+        const int crg0 = kProdGroups + warp;
+        int64_t cro[kGroupsPerCons];
+        rows_locate<kGroupsPerCons>(p, 0, cur, act, b, tk_base, crg0, kConsWarps, kRowGroups, rr, cro);
+        {
+            uint4 kn[kGroupsPerCons][4], sc[kGroupsPerCons];
+            rows_load<kGroupsPerCons>(p, cro, cu, kn, sc);
+            rows_produce<kGroupsPerCons>(sm, p, 0, cro, kn, sc, crg0, kConsWarps, kRowGroups, rr, cu, lane);
+        }
+        if (ntiles > 1) {
+            rows_locate<kGroupsPerCons>(p, 1, cur, act, b, tk_base, crg0, kConsWarps, kRowGroups, rr, cro);
+            rows_prefetch_l2<kGroupsPerCons>(p, cro, cu);
+        }
         const uint32_t lanes = static_cast<uint32_t>(32 * q4) << 16;
         float Mrun = -INFINITY, Lrun = 0.f, sig = 1.f;   // head hf*32 + lane (log2 units)
         bool any = false;
@@ -507,6 +563,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.p_full);
+            if (t + 1 < ntiles) {
+                {
+                    uint4 kn[kGroupsPerCons][4], sc[kGroupsPerCons];
+                    rows_load<kGroupsPerCons>(p, cro, cu, kn, sc);
+                    rows_produce<kGroupsPerCons>(sm, p, t + 1, cro, kn, sc, crg0, kConsWarps, kRowGroups, rr, cu,
+                                                 lane);
+                }
+                if (t + 2 < ntiles) {
+                    rows_locate<kGroupsPerCons>(p, t + 2, cur, act, b, tk_base, crg0, kConsWarps, kRowGroups, rr,
+                                                cro);
+                    rows_prefetch_l2<kGroupsPerCons>(p, cro, cu);
+                }
+            }
         }
         // ---- out = BF16(O / L) = BF16(O^T * sig / L) ----
         mbar_wait(&sm.o_done, static_cast<uint32_t>(ntiles - 1) & 1u, p.err, 8, &sm.abort);
@@ -546,6 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
 
 static_assert(offsetof(MlaSmem, kt) % 1024 == 0 && offsetof(MlaSmem, qt) % 1024 == 0, "operand alignment");
 static_assert(offsetof(MlaSmem, wrow) % 16 == 0, "broadcast row alignment");
+static_assert(kProdGroups <= kGroupsPerProd * kProdWarps && kGroupsPerCons * kConsWarps + kProdGroups == kRowGroups,
+              "every row group has one warp");
 static_assert(sizeof(MlaSmem) + 1024 <= 232448, "MLA decode shared memory over budget");
 
 inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
