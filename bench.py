@@ -579,8 +579,8 @@ MLA_VARIANTS = 2          # top-k selections rotated between steps (each ~172 MB
 # valid only for the kernel source it was taken with.
 # Captured on the 16-sequence case and scaled by the selected rows (x4): each
 # row is read from DRAM once, so the traffic grows in proportion.
-MLA_TRAFFIC = {"sources_sha1": "775a64bf2a5c52d0653a25b28b6338bdfddb12e1",
-               "bytes_per_launch": 4 * (54278912 + 303104)}
+MLA_TRAFFIC = {"sources_sha1": "e64f58dd8d660d7dd8317b13d8c1881435cca30c",
+               "bytes_per_launch": 4 * (54290432 + 355328)}
 
 
 def mla_sources_sha1() -> str:

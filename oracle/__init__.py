@@ -28,18 +28,24 @@ LAYOUT_BSND = 0
 LAYOUT_BNBD = 1
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compile one C source of the oracle into the shared library ``out``
+    (gcc, C11, -O2, no fast-math, no FMA contraction)."""
+    tmp = out + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off",
+           "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile pa_oracle.c into _build/liboracle.so (gcc, -O2, no fast-math)."""
     os.makedirs(_BUILD, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
-    tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
-    cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off",
-           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
 
 
 def _load():
@@ -47,7 +53,10 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # PA_ORACLE_LIB names another compiled copy of the oracle: the
+        # planted-mistake tests load mutated copies this way, each in a
+        # process of its own.
+        lib = ctypes.CDLL(os.environ.get("PA_ORACLE_LIB") or build())
         P = ctypes.c_void_p
         i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
         lib.or_e4m3_decode.argtypes = [ctypes.c_uint8]
