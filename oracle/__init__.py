@@ -91,7 +91,7 @@ def _load():
                                      i32, i64, i32, i32, i32, f32, P, i64]
         lib.or_pa_decode.restype = ctypes.c_int
         lib.or_mla_sparse_decode.argtypes = [P, P, P, i64, P, i32, P, P, P, P, i32, i32, i32,
-                                             i32, i64, i32, i32, f32, P, i64]
+                                             i32, i64, i32, i32, f32, P, i64, i32]
         lib.or_mla_sparse_decode.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -309,14 +309,19 @@ MLA_DR = 64
 MLA_ROW_USED = 656
 
 
+MLA_FORMAT_PAGE = 0        # [MS]: E4M3 kn | BF16 kr | 4 FP32 scales (per 128 channels)
+MLA_FORMAT_KVC_BF16 = 1    # [KC] quant mode 0: BF16 kr | E4M3 kn | 8 BF16 scales (per 64)
+MLA_FORMAT_KVC_E8M0 = 2    # [KC] quant mode 1: BF16 kr | E4M3 kn | 8 E8M0 scales (per 64)
+
+
 def mla_sparse_decode(q_nope, q_rope, cache, topk_indices, block_table, kv_act_seqs, *, S1,
                       block_size=128, s2_tile=128, softmax_scale=None, rows=None,
-                      want_f32=False):
+                      want_f32=False, row_format=MLA_FORMAT_PAGE):
     """MLA sparse FP8 decode (the steps are listed in ``pa_oracle.c``).
 
     q_nope uint16 (BF16 bits) [T, NQ, 512], q_rope uint16 [T, NQ, 64] with
     T = B*S1; cache uint8 [num_blocks*block_size, row_bytes >= 656] packed rows
-    (E4M3 kn | BF16 kr | 4 FP32 scales); topk_indices int32 [T, topk];
+    in the layout ``row_format`` names (MLA_FORMAT_*); topk_indices int32 [T, topk];
     block_table int32 [B, max_blocks]; kv_act_seqs int32 [B]. Returns BF16 bits
     uint16 [T, NQ, 512] (and the float32 values before the cast when
     ``want_f32``). ``rows`` restricts the work to the flat rows ``t*NQ + h``;
@@ -345,7 +350,7 @@ def mla_sparse_decode(q_nope, q_rope, cache, topk_indices, block_table, kv_act_s
     rc = lib.or_mla_sparse_decode(_ptr(qn), _ptr(qr), _ptr(kv), row_bytes, _ptr(tk),
                                   tk.shape[1], _ptr(bt), _ptr(act), _ptr(out), _ptr(out32), B,
                                   S1, NQ, block_size, num_blocks, bt.shape[1], s2_tile,
-                                  softmax_scale, _ptr(r), nrows)
+                                  softmax_scale, _ptr(r), nrows, row_format)
     if rc != 0:
         raise ValueError("or_mla_sparse_decode rejected its arguments")
     return (out, out32) if want_f32 else out

@@ -553,10 +553,19 @@ int or_pa_decode(const uint8_t* q, const float* q_scale, const uint8_t* k_cache,
 /*                                                                         */
 /* Fixed sizes: kv_lora_rank 512 (the "nope" part), qk_rope_dim 64, so a   */
 /* query/key head is 576 wide; one KV head shared by all NQ query heads.   */
-/* Cache row (row_bytes >= 656 bytes apart, [MS] pads them to 672):        */
+/* Cache row (row_bytes >= 656 bytes apart, [MS] pads them to 672), by    */
+/* row_format:                                                             */
+/*  0 ([MS] 核心参数与 KV Cache 布局):                                      */
 /*   [0, 512)    kn, E4M3 codes;                                            */
 /*   [512, 640)  kr, 64 BF16 values (little-endian);                        */
 /*   [640, 656)  4 FP32 dequant scales, one per 128 channels of kn.         */
+/*  1, 2 (the row the KV compress epilog above writes for d = 576, [KC]    */
+/*  计算公式 场景 1 / 场景 2, read back by the same dequantisation):        */
+/*   [0, 128)    kr, 64 BF16 values;                                        */
+/*   [128, 640)  kn, E4M3 codes;                                            */
+/*   [640, ...)  one scale per 64 channels of kn: 8 BF16 values (format 1, */
+/*               quant mode 0) or 8 E8M0 bytes e for 2^(e - 127) (format 2, */
+/*               quant mode 1).                                            */
 /* q_nope [T*NQ][512], q_rope [T*NQ][64] BF16 bits, T = B*S1 query tokens, */
 /* token t = b*S1 + s. topk_indices [T][topk] int32: positions in the      */
 /* sequence of the selected keys. block_table [B][max_blocks] int32,       */
@@ -571,7 +580,7 @@ int or_pa_decode(const uint8_t* q, const float* q_scale, const uint8_t* k_cache,
 /*    id outside the pool, is read as block 0).                            */
 /*    An idx outside [0, kv_act_seqs[b]) takes no part (the pages only     */
 /*    produce valid positions; masking is the plain reading of "-1" pads). */
-/*  - dequant: kn_j[c] = BF16(FP32(E4M3(code)) * scale[c / 128]);          */
+/*  - dequant: kn_j[c] = BF16(FP32(E4M3(code)) * scale of c's group);      */
 /*    k_j = [kn_j, kr_j] (576), q = [q_nope, q_rope] (576).                */
 /*  - C1: s_j = q . k_j, FP32 result (products of BF16 are exact; summed   */
 /*    in double and rounded once); S_j = s_j * softmax_scale.              */
@@ -592,7 +601,7 @@ int or_mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const u
                          const int32_t* block_table, const int32_t* kv_act_seqs, uint16_t* out,
                          float* out_f32, int B, int S1, int NQ, int BS, int64_t num_blocks,
                          int max_blocks, int s2_tile, float softmax_scale, const int64_t* rows,
-                         int64_t nrows)
+                         int64_t nrows, int row_format)
 {
     enum { DN = 512, DR = 64, DK = 576 };
     float* kn;   /* [s2_tile][512] dequantised kn of the tile (BF16 values) */
@@ -604,7 +613,8 @@ int or_mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const u
     float O[DN];
     int64_t total = (int64_t)B * S1 * NQ, ri;
     if (B <= 0 || S1 <= 0 || NQ <= 0 || BS <= 0 || topk < 0 || s2_tile <= 0 ||
-        row_bytes < 656 || num_blocks <= 0 || max_blocks <= 0)
+        row_bytes < 656 || num_blocks <= 0 || max_blocks <= 0 || row_format < 0 ||
+        row_format > 2)
         return -1;
     kn = (float*)malloc(sizeof(float) * (size_t)s2_tile * DN);
     kr = (float*)malloc(sizeof(float) * (size_t)s2_tile * DR);
@@ -644,7 +654,9 @@ int or_mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const u
             for (j = 0; j < n; ++j) {
                 int idx = topk_indices[t * topk + j0 + j];
                 const uint8_t* kv;
-                float sc[4];
+                const uint8_t* code; /* the 512 kn codes of the row */
+                const uint8_t* rope; /* its 64 BF16 kr values       */
+                float sc[8];         /* the scale of each 64 channels */
                 int blk;
                 double acc = 0.0;
                 ok[j] = (uint8_t)(idx >= 0 && idx < act);
@@ -654,14 +666,29 @@ int or_mla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_rope, const u
                 if (blk < 0 || blk >= num_blocks)
                     blk = 0;
                 kv = cache + ((int64_t)blk * BS + idx % BS) * row_bytes;
-                memcpy(sc, kv + 640, sizeof(sc));
+                if (row_format == 0) {
+                    float s4[4];
+                    memcpy(s4, kv + 640, sizeof(s4));
+                    for (c = 0; c < 8; ++c)
+                        sc[c] = s4[c / 2]; /* one FP32 scale per 128 channels */
+                    code = kv;
+                    rope = kv + DN;
+                } else {
+                    for (c = 0; c < 8; ++c)
+                        sc[c] = row_format == 1
+                                    ? or_bf16_to_float((uint16_t)(kv[640 + 2 * c] |
+                                                                  (kv[640 + 2 * c + 1] << 8)))
+                                    : (float)ldexp(1.0, (int)kv[640 + c] - 127);
+                    code = kv + 2 * DR;
+                    rope = kv;
+                }
                 for (c = 0; c < DN; ++c) {
-                    float f = (float)or_e4m3_decode(kv[c]) * sc[c / 128];
+                    float f = (float)or_e4m3_decode(code[c]) * sc[c / 64];
                     kn[(int64_t)j * DN + c] = or_bf16_to_float(or_bf16_from_float(f));
                 }
                 for (c = 0; c < DR; ++c)
                     kr[(int64_t)j * DR + c] =
-                        or_bf16_to_float((uint16_t)(kv[DN + 2 * c] | (kv[DN + 2 * c + 1] << 8)));
+                        or_bf16_to_float((uint16_t)(rope[2 * c] | (rope[2 * c + 1] << 8)));
                 for (c = 0; c < DN; ++c)
                     acc += q[c] * (double)kn[(int64_t)j * DN + c];
                 for (c = 0; c < DR; ++c)

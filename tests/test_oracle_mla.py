@@ -299,3 +299,136 @@ def test_mla_page_cases_shapes():
         assert (tk[t, n:] == -1).all()
     c64 = workloads.mla_page_b64()
     assert (c64.B, c64.S1, int(c64.act.min()), int(c64.act.max())) == (64, 2, 65536, 65536)
+
+
+# ---- rows written by the KV compress epilog (quant modes 0 and 1) ----------------------
+# The CANN aclnnKvCompressEpilog page's row for d = 576: the rope part first as BF16, the nope
+# part as E4M3 in groups of 64 channels, one scale per group (BF16 in quant mode 0, an E8M0
+# power of two in quant mode 1). The decode dequantises it with the MLA page's rule
+# (BF16(FP32(code) * scale)), each group by its own scale.
+
+KVC_FORMATS = [workloads.MLA_FORMAT_KVC_BF16, workloads.MLA_FORMAT_KVC_E8M0]
+
+
+def run_fmt(case, cache, fmt, want_f32=True, s2_tile=None):
+    qn, qr = case.q_bits()
+    return oracle.mla_sparse_decode(qn, qr, cache, case.topk_indices(), case.block_table,
+                                    case.act, S1=case.S1, block_size=case.BS,
+                                    s2_tile=case.s2_tile if s2_tile is None else s2_tile,
+                                    softmax_scale=case.softmax_scale, want_f32=want_f32,
+                                    row_format=fmt)
+
+
+def kvc_rows_from_page_rows(page, fmt):
+    """The same keys moved into the KV compress row: rope bytes first, then the codes, then
+    each 128-channel FP32 scale twice as two 64-channel scales (BF16 bits, or the E8M0 byte
+    of a power of two). Only scales that the KV compress format holds exactly are allowed."""
+    out = np.full_like(page, 0xFF)
+    out[:, :2 * DR] = page[:, DN:DN + 2 * DR]
+    out[:, 2 * DR:2 * DR + DN] = page[:, :DN]
+    s4 = page[:, 640:656].copy().view(np.float32)
+    s8 = np.repeat(s4, 2, axis=1)
+    if fmt == workloads.MLA_FORMAT_KVC_BF16:
+        bits = s8.view(np.uint32)
+        assert not (bits & 0xFFFF).any(), "scale not exact in BF16"
+        out[:, 640:656] = (bits >> 16).astype(np.uint16).view(np.uint8).reshape(-1, 16)
+    else:
+        m, e = np.frexp(s8.astype(np.float64))
+        assert (m == 0.5).all(), "scale not a power of two"
+        out[:, 640:648] = (e - 1 + 127).astype(np.uint8)
+    return out
+
+
+@pytest.mark.parametrize("fmt", KVC_FORMATS)
+def test_mla_kvc_row_equals_the_page_row_holding_the_same_keys(fmt):
+    """Page-format rows whose scales the KV compress row can hold exactly (BF16 values; powers
+    of two) are moved byte by byte into the KV compress layout: the outputs are bit-identical,
+    so the new layout is read as the same keys through the pinned page-format path."""
+    case = small_case(frac_invalid=0.1, act=(300, 141))
+    page = case.cache()
+    s4 = page[:, 640:656].copy().view(np.uint32)
+    if fmt == workloads.MLA_FORMAT_KVC_BF16:
+        s4 &= np.uint32(0xFFFF0000)
+    else:
+        k = np.random.default_rng(2).integers(-9, -6, size=s4.shape)
+        s4[:] = (np.ldexp(1.0, k).astype(np.float32)).view(np.uint32)
+    page[:, 640:656] = s4.view(np.uint8).reshape(-1, 16)
+    kvc = kvc_rows_from_page_rows(page, fmt)
+    a, a32 = run(case, cache=page)
+    b, b32 = run_fmt(case, kvc, fmt)
+    assert np.array_equal(a, b) and np.array_equal(a32, b32)
+    assert np.abs(a32).max() > 0.1
+
+
+@pytest.mark.parametrize("fmt", KVC_FORMATS)
+def test_mla_kvc_single_key_gives_its_dequantised_row(fmt):
+    """One visible key: every head outputs that key's nope row dequantised with torch (E4M3
+    codes at bytes 128..639 to float32, times the scale of each 64 channels, to BF16), bit for
+    bit."""
+    case = small_case(act=(1, 1), S1=1, B=2, topk=8)
+    cache = case.cache(fmt=fmt)
+    out = run_fmt(case, cache, fmt, want_f32=False)
+    for t in range(case.T):
+        rows = selected(case, t)
+        assert rows.size == 1
+        r = torch.from_numpy(cache[rows].copy())
+        codes = r[:, 2 * DR:2 * DR + DN].contiguous().view(torch.float8_e4m3fn).to(torch.float32)
+        if fmt == workloads.MLA_FORMAT_KVC_BF16:
+            sc = r[:, 640:656].contiguous().view(torch.bfloat16).to(torch.float32)
+        else:
+            sc = torch.pow(2.0, r[:, 640:648].to(torch.float32) - 127.0)
+        kn = (codes * sc.repeat_interleave(64, dim=1)).to(torch.bfloat16)
+        want = kn[0].view(torch.int16).numpy().view(np.uint16)
+        for h in range(case.NQ):
+            assert np.array_equal(out[t, h], want)
+
+
+@pytest.mark.parametrize("fmt", KVC_FORMATS)
+def test_mla_kvc_padding_after_the_scales_is_not_used(fmt):
+    case = small_case(act=(300, 41))
+    cache = case.cache(fmt=fmt)
+    end = 656 if fmt == workloads.MLA_FORMAT_KVC_BF16 else 648
+    other = cache.copy()
+    other[:, end:] = np.random.default_rng(4).integers(0, 256, size=other[:, end:].shape,
+                                                       dtype=np.uint8)
+    a, a32 = run_fmt(case, cache, fmt)
+    b, b32 = run_fmt(case, other, fmt)
+    assert np.array_equal(a, b) and np.array_equal(a32, b32)
+
+
+@pytest.mark.parametrize("mode,round_scale", [(0, False), (1, True)])
+def test_mla_kvc_reads_what_the_compress_epilog_wrote(mode, round_scale):
+    """The append-then-attend chain on the CPU: BF16 key rows x = [nope 512 | rope 64] go
+    through the KV compress epilog oracle into a paged cache, and the decode over that cache
+    matches FP64 softmax attention over x itself (keys [nope, rope], values the nope part)
+    within the quantisation error: E4M3 codes carry up to 2^-4 relative error per channel
+    (an E8M0 scale rounded up doubles it), BF16 keys and P 2^-9; measured worst 0.031 (mode
+    0) and 0.039 (mode 1), a layout or scale mistake gives errors of order 1. Quant mode 1
+    without roundScale is left out: its power of two at or below max|x|/448 saturates the
+    group's largest values at 448 by design (pinned with the epilog oracle itself)."""
+    case = small_case(B=2, S1=2, NQ=4, act=(300, 141), topk=96, frac_invalid=0.1)
+    rows = case.rows_used()
+    x = torch.from_numpy(np.random.default_rng(9).standard_normal(
+        (rows.size, DN + DR)).astype(np.float32)).to(torch.bfloat16)
+    cache = np.zeros((case.num_blocks * case.BS, workloads.MLA_ROW_BYTES), dtype=np.uint8)
+    oracle.kv_compress_epilog(x.float().numpy(), cache.reshape(case.num_blocks, -1),
+                              case.num_blocks, case.BS, case.BS * workloads.MLA_ROW_BYTES,
+                              workloads.MLA_ROW_BYTES, rows.astype(np.int64), quant_mode=mode,
+                              round_scale=round_scale)
+    fmt = workloads.MLA_FORMAT_KVC_BF16 if mode == 0 else workloads.MLA_FORMAT_KVC_E8M0
+    _, out32 = run_fmt(case, cache, fmt)
+    key_of_row = {int(r): i for i, r in enumerate(rows)}
+    xd = x.double().numpy()
+    worst = 0.0
+    for t in range(case.T):
+        sel = selected(case, t)
+        for h in range(case.NQ):
+            if sel.size == 0:
+                assert not out32[t, h].any()
+                continue
+            k = xd[[key_of_row[int(r)] for r in sel]]
+            s = (k @ torch_query(case, t, h)) * case.softmax_scale
+            w = np.exp(s - s.max())
+            ref = (w / w.sum()) @ k[:, :DN]
+            worst = max(worst, float(np.abs(out32[t, h] - ref).max()))
+    assert worst < 0.1, worst

@@ -68,7 +68,7 @@ MUTANTS = [
     ("mla: tile sum merged without its factor", MLA_PINS,
      [("L = any ? L * a + l * bb : l;", "L = any ? L * a + l : l;")]),
     ("mla: scale groups of 64 channels instead of 128", MLA_PINS,
-     [("* sc[c / 128];", "* sc[(c / 64) % 4];")]),
+     [("sc[c] = s4[c / 2];", "sc[c] = s4[c % 4];")]),
     ("mla: visible count off by one", MLA_PINS,
      [("cur = act - S1 + 1 + s;", "cur = act - S1 + s;")]),
     ("mla: dequantised keys not rounded to BF16", MLA_PINS,
@@ -81,6 +81,19 @@ MUTANTS = [
        "ok[j] = (uint8_t)(idx >= 0 && idx < max_blocks * BS);")]),
     ("mla: softmax scale dropped", MLA_PINS,
      [("S[j] = (float)acc * softmax_scale;", "S[j] = (float)acc;")]),
+    # MLA decode of rows written by the KV compress epilog ([KC] 计算公式 场景 1 / 场景 2)
+    ("mla kvc: group scales per 128 channels instead of 64", MLA_PINS,
+     [("float f = (float)or_e4m3_decode(code[c]) * sc[c / 64];",
+       "float f = (float)or_e4m3_decode(code[c]) * sc[row_format == 0 ? c / 64 : c / 128];")]),
+    ("mla kvc: E8M0 exponent bias 128 instead of 127", MLA_PINS,
+     [("(int)kv[640 + c] - 127)", "(int)kv[640 + c] - 128)")]),
+    ("mla kvc: BF16 scale bytes read big-endian", MLA_PINS,
+     [("(kv[640 + 2 * c] |\n", "(kv[640 + 2 * c + 1] |\n"),
+      ("(kv[640 + 2 * c + 1] << 8)))", "(kv[640 + 2 * c] << 8)))")]),
+    ("mla kvc: rope read where the page row keeps it", MLA_PINS,
+     [("rope = kv;", "rope = kv + DN;")]),
+    ("mla kvc: codes read from the row start", MLA_PINS,
+     [("code = kv + 2 * DR;", "code = kv;")]),
 ]
 
 

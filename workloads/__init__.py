@@ -318,6 +318,12 @@ def append(frac_skip: float = 0.05, B: int = 64, lo: int = 512, hi: int = 8192) 
 MLA_DN = 512
 MLA_DR = 64
 MLA_ROW_BYTES = 672     # 656 used bytes padded to 672
+# Cache row formats the MLA decode reads: the MLA page's packed row, and the
+# KV compress epilog's row for d = 576 (rope first; 64-channel group scales,
+# BF16 for its quant mode 0, E8M0 for quant mode 1).
+MLA_FORMAT_PAGE = 0
+MLA_FORMAT_KVC_BF16 = 1
+MLA_FORMAT_KVC_E8M0 = 2
 
 
 def _mix64(x: np.ndarray) -> np.ndarray:
@@ -361,9 +367,11 @@ class MlaCase:
     """One MLA sparse decode workload. Cache rows are drawn as raw bytes:
     E4M3 codes with a random sign, exponent field uniform in [6, 15] (values
     2^-1 .. 448, the upper range an amax/448 group quantiser fills) and a
-    random mantissa; 4 FP32 group scales uniform in [0.004, 0.009]; 64 BF16
-    rope values N(0,1) (truncated to BF16); bytes 656..671 are 0xFF padding,
-    which no step may read."""
+    random mantissa; 64 BF16 rope values N(0,1) (truncated to BF16); group
+    scales: 4 FP32 uniform in [0.004, 0.009] (page format), 8 BF16 of the
+    same range truncated to BF16 (KV compress quant mode 0), or 8 E8M0 bytes
+    for 2^-8 or 2^-7 (quant mode 1). The bytes after the scales are 0xFF
+    padding, which no step may use."""
 
     name: str
     B: int
@@ -466,34 +474,53 @@ class MlaCase:
         """Valid selected (token, key) pairs: the packed rows one decode reads."""
         return int(self._valid(variant)[0].size)
 
-    def row_bytes(self, rows: np.ndarray) -> np.ndarray:
-        """uint8 [len(rows), 672]: the packed cache rows with these ids."""
+    def row_bytes(self, rows: np.ndarray, fmt: int = MLA_FORMAT_PAGE) -> np.ndarray:
+        """uint8 [len(rows), 672]: the cache rows with these ids in row format
+        fmt (MLA_FORMAT_*). The codes and rope values of a row are the same
+        draw in every format; only their places and the scales differ."""
         rows = np.asarray(rows, dtype=np.int64)
         n = rows.size
+        code_at, rope_at = (0, MLA_DN) if fmt == MLA_FORMAT_PAGE else (2 * MLA_DR, 0)
         out = np.empty((n, MLA_ROW_BYTES), dtype=np.uint8)
-        out[:, 656:] = 0xFF
         w = _hashed_words(self.seed, rows, MLA_DN // 8, 0).view(np.uint8).reshape(n, MLA_DN)
-        out[:, :MLA_DN] = _CODE_OF_BYTE[w]
+        out[:, code_at:code_at + MLA_DN] = _CODE_OF_BYTE[w]
         h = _hashed_words(self.seed, rows, MLA_DR, 1)
         u = ((h & np.uint64(0xFFFFFFFF)).astype(np.float32) + 0.5) * np.float32(2.0 ** -32)
         v = ((h >> np.uint64(32)).astype(np.float32) + 0.5) * np.float32(2.0 ** -32)
         rope = np.sqrt(np.float32(-2.0) * np.log(u)) * np.cos(np.float32(2.0 * np.pi) * v)
-        out[:, MLA_DN:MLA_DN + 2 * MLA_DR] = (rope.view(np.uint32) >> np.uint32(16)).astype(
+        out[:, rope_at:rope_at + 2 * MLA_DR] = (rope.view(np.uint32) >> np.uint32(16)).astype(
             np.uint16).view(np.uint8).reshape(n, 2 * MLA_DR)
-        h = _hashed_words(self.seed, rows, 2, 2)
-        s4 = np.stack([h & np.uint64(0xFFFFFFFF), h >> np.uint64(32)], axis=-1).reshape(n, 4)
-        sc = (np.float32(0.004) + np.float32(0.005 * 2.0 ** -32) * s4.astype(np.float32))
-        out[:, MLA_DN + 2 * MLA_DR:656] = sc.astype(np.float32).view(np.uint8).reshape(n, 16)
+        s0 = MLA_DN + 2 * MLA_DR
+        if fmt == MLA_FORMAT_PAGE:
+            h = _hashed_words(self.seed, rows, 2, 2)
+            s4 = np.stack([h & np.uint64(0xFFFFFFFF), h >> np.uint64(32)], axis=-1).reshape(n, 4)
+            sc = (np.float32(0.004) + np.float32(0.005 * 2.0 ** -32) * s4.astype(np.float32))
+            out[:, s0:s0 + 16] = sc.astype(np.float32).view(np.uint8).reshape(n, 16)
+            end = s0 + 16
+        elif fmt == MLA_FORMAT_KVC_BF16:
+            h = _hashed_words(self.seed, rows, 4, 3)
+            s8 = np.stack([h & np.uint64(0xFFFFFFFF), h >> np.uint64(32)], axis=-1).reshape(n, 8)
+            sc = (np.float32(0.004) + np.float32(0.005 * 2.0 ** -32) * s8.astype(np.float32))
+            out[:, s0:s0 + 16] = (sc.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(
+                np.uint16).view(np.uint8).reshape(n, 16)
+            end = s0 + 16
+        elif fmt == MLA_FORMAT_KVC_E8M0:
+            h = _hashed_words(self.seed, rows, 1, 4).view(np.uint8).reshape(n, 8)
+            out[:, s0:s0 + 8] = (np.uint8(119) + (h & np.uint8(1))).astype(np.uint8)
+            end = s0 + 8
+        else:
+            raise ValueError("unknown MLA row format %r" % (fmt,))
+        out[:, end:] = 0xFF
         return out
 
-    def cache(self, rows=None) -> np.ndarray:
+    def cache(self, rows=None, fmt: int = MLA_FORMAT_PAGE) -> np.ndarray:
         """uint8 [num_blocks*BS, 672]: every row drawn (rows=None), or only the
         listed rows drawn and the others zero."""
         total = self.num_blocks * self.BS
         if rows is None:
-            return self.row_bytes(np.arange(total))
+            return self.row_bytes(np.arange(total), fmt)
         c = np.zeros((total, MLA_ROW_BYTES), dtype=np.uint8)
-        c[rows] = self.row_bytes(rows)
+        c[rows] = self.row_bytes(rows, fmt)
         return c
 
     def flops(self, variant: int = 0) -> int:
