@@ -70,6 +70,10 @@ def parse_args():
     ap.add_argument("--workload", choices=["glm45_step", "mla"], default="glm45_step",
                     help="glm45_step: the GLM-4.5 append + decode step (default); mla: the "
                          "MLA sparse FP8 decode at the DeepSeek-V3.2 page's b=64 case")
+    ap.add_argument("--mla-format", choices=["page", "kvc0", "kvc1"], default="page",
+                    help="MLA cache rows: the MLA page's packed row, or the KV compress "
+                         "epilog's row for d=576 with quant mode 0 (BF16 group scales) or 1 "
+                         "(E8M0 group scales)")
     ap.add_argument("--mla-batch", type=int, default=64,
                     help="sequences of the mla workload (64 = the page's case; smaller for "
                          "profiling captures)")
@@ -571,16 +575,28 @@ def main():
 MLA_METRIC = ("MLA sparse FP8 decode: achieved BF16 tensor TFLOP/s (% of peak), µs/step at the "
               "DeepSeek-V3.2 b=64 decode shape")
 MLA_UNIT = "TFLOP/s"
-MLA_WORKLOAD = ("mla_sparse_decode: b=%d s_q=2 nq=128 n_kv=1 topk=2048 kv_lora_rank=512 "
-                "qk_rope_dim=64 block_size=128 kv_act_seqs=65536 (all); 672-byte packed rows "
-                "(E4M3 nope, BF16 rope, 4 FP32 group scales); s2_tile=128")
+MLA_WORKLOAD = ("%s: b=%d s_q=2 nq=128 n_kv=1 topk=2048 kv_lora_rank=512 "
+                "qk_rope_dim=64 block_size=128 kv_act_seqs=65536 (all); 672-byte %s; s2_tile=128")
+MLA_FORMATS = {  # --mla-format: (row format, KV compress quant mode, entry point, rows)
+    "page": (workloads.MLA_FORMAT_PAGE, None, "mla_sparse_decode",
+             "packed rows (E4M3 nope, BF16 rope, 4 FP32 group scales)"),
+    "kvc0": (workloads.MLA_FORMAT_KVC_BF16, 0, "mla_sparse_decode_kvc",
+             "KV compress epilog rows, quant mode 0 (BF16 rope, E4M3 nope, 8 BF16 group scales)"),
+    "kvc1": (workloads.MLA_FORMAT_KVC_E8M0, 1, "mla_sparse_decode_kvc",
+             "KV compress epilog rows, quant mode 1 (BF16 rope, E4M3 nope, 8 E8M0 group scales)"),
+}
+
+
+def mla_workload_name(args, B):
+    _, _, entry, rows = MLA_FORMATS[args.mla_format]
+    return MLA_WORKLOAD % (entry, B, rows)
 MLA_VARIANTS = 2          # top-k selections rotated between steps (each ~172 MB of rows)
 # DRAM traffic of one MLA decode launch on this workload from an ncu capture,
 # valid only for the kernel source it was taken with.
 # Captured on the 16-sequence case and scaled by the selected rows (x4): each
 # row is read from DRAM once, so the traffic grows in proportion.
-MLA_TRAFFIC = {"sources_sha1": "e64f58dd8d660d7dd8317b13d8c1881435cca30c",
-               "bytes_per_launch": 4 * (54290432 + 355328)}
+MLA_TRAFFIC = {"sources_sha1": "495ff6dfa6d80de79b093600199b93ebcefad886", "format": "page",
+               "bytes_per_launch": 4 * (54291200 + 381952)}
 
 
 def mla_sources_sha1() -> str:
@@ -605,7 +621,7 @@ def mla_host_cache(case, used, rb):
     return host
 
 
-def mla_oracle_sample(case, host, budget_s):
+def mla_oracle_sample(case, host, budget_s, row_format=workloads.MLA_FORMAT_PAGE):
     """Time the oracle on whole query tokens (all heads) until about budget_s
     of CPU time: (TFLOP/s, tokens, seconds, flops)."""
     import oracle
@@ -619,7 +635,8 @@ def mla_oracle_sample(case, host, budget_s):
         rows = np.arange(int(t) * NQ, (int(t) + 1) * NQ, dtype=np.int64)
         oracle.mla_sparse_decode(qn, qr, host, tk, case.block_table, case.act, S1=case.S1,
                                  block_size=case.BS, s2_tile=case.s2_tile,
-                                 softmax_scale=case.softmax_scale, rows=rows)
+                                 softmax_scale=case.softmax_scale, rows=rows,
+                                 row_format=row_format)
         b = int(t) // case.S1
         sel = tk[int(t), :int(cur[t])]
         nvalid = int(((sel >= 0) & (sel < case.act[b])).sum())
@@ -635,16 +652,17 @@ def mla_reference_arm(args, rank, world):
     if rank != 0:
         return
     case = workloads.mla_page_b64(args.mla_batch)
+    fmt = MLA_FORMATS[args.mla_format][0]
     used = case.rows_used((0,))
-    host = mla_host_cache(case, used, case.row_bytes(used))
+    host = mla_host_cache(case, used, case.row_bytes(used, fmt))
     total_steps = args.steps + args.warmup
     budget = max(args.cpu_seconds / max(total_steps, 1), 0.5)
     for _ in range(args.warmup):
-        mla_oracle_sample(case, host, budget)
+        mla_oracle_sample(case, host, budget, fmt)
     vals = []
     tok = 0
     for _ in range(args.steps):
-        v, tok, _, _ = mla_oracle_sample(case, host, budget)
+        v, tok, _, _ = mla_oracle_sample(case, host, budget, fmt)
         vals.append(v)
     value = statistics.median(vals) if vals else 0.0
     line = {
@@ -652,7 +670,8 @@ def mla_reference_arm(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": case.flops() / (value * 1e12) * 1e3 if value else None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
-        "data": "synthetic", "config": {"workload": MLA_WORKLOAD % case.B, "sample_tokens": tok},
+        "data": "synthetic", "config": {"workload": mla_workload_name(args, case.B),
+                                        "sample_tokens": tok},
         "cpu_baseline": {"value": value, "unit": MLA_UNIT, "cores": 1, "kind": "oracle",
                          "sample": "%d query tokens (all 128 heads) per step; ms_per_step "
                                    "extrapolated to the 128-token decode by flops" % tok},
@@ -675,9 +694,10 @@ def mla_arm(args, rank, world, local):
     pa.lib()
 
     case = workloads.mla_page_b64(args.mla_batch)
+    fmt, quant_mode, entry, _ = MLA_FORMATS[args.mla_format]
     V = MLA_VARIANTS
     used = case.rows_used(range(V))
-    rb = case.row_bytes(used)
+    rb = case.row_bytes(used, fmt)
     nrows = case.num_blocks * case.BS
     cache = torch.zeros((nrows, workloads.MLA_ROW_BYTES), dtype=torch.uint8, device=dev)
     cache[torch.from_numpy(used).to(dev)] = torch.from_numpy(rb).to(dev)
@@ -692,9 +712,14 @@ def mla_arm(args, rank, world, local):
     bytes_v = [case.algorithmic_bytes(v) for v in range(V)]
 
     def launch(i, q=(qn, qr), tk=None, o=out):
-        pa.mla_sparse_decode(q[0], q[1], cache, tks[i % V] if tk is None else tk, bt, act, o,
-                             S1=case.S1, status=status, block_size=case.BS,
-                             softmax_scale=case.softmax_scale)
+        if quant_mode is None:
+            pa.mla_sparse_decode(q[0], q[1], cache, tks[i % V] if tk is None else tk, bt, act, o,
+                                 S1=case.S1, status=status, block_size=case.BS,
+                                 softmax_scale=case.softmax_scale)
+        else:
+            pa.mla_sparse_decode_kvc(q[0], q[1], cache, tks[i % V] if tk is None else tk, bt,
+                                     act, o, quant_mode=quant_mode, S1=case.S1, status=status,
+                                     block_size=case.BS, softmax_scale=case.softmax_scale)
 
     cyc = V * 6
 
@@ -779,12 +804,13 @@ def mla_arm(args, rank, world, local):
     hbm_peak, _ = measured_hbm_peak()
     gbs = bytes_run / (ms * 1e-3) / 1e9
     traffic = (MLA_TRAFFIC["bytes_per_launch"]
-               if MLA_TRAFFIC["sources_sha1"] == mla_sources_sha1() else None)
+               if MLA_TRAFFIC["sources_sha1"] == mla_sources_sha1()
+               and MLA_TRAFFIC["format"] == args.mla_format else None)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = mla_host_cache(case, used, rb)
-        v, tok, dt, _ = mla_oracle_sample(case, host, args.cpu_seconds)
+        v, tok, dt, _ = mla_oracle_sample(case, host, args.cpu_seconds, fmt)
         cpu = {"value": v, "unit": MLA_UNIT, "cores": 1, "kind": "oracle",
                "sample": "%d query tokens x 128 heads of the same workload (top-k selection 0), "
                          "single-threaded C oracle, %.1f s" % (tok, dt)}
@@ -795,7 +821,7 @@ def mla_arm(args, rank, world, local):
             "us_per_step": us_launch, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16+e4m3", "data": "synthetic",
             "config": {
-                "workload": MLA_WORKLOAD % case.B, "query_tokens": case.T,
+                "workload": mla_workload_name(args, case.B), "query_tokens": case.T,
                 "keys_per_step": case.keys_read(0),
                 "flops_per_step": flops_v[0], "bytes_per_step": bytes_v[0],
                 "l2": "inputs larger than L2: %d top-k selections rotated (%.0f MB of rows each "
@@ -805,7 +831,7 @@ def mla_arm(args, rank, world, local):
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
             "gpu_launches": args.steps,
-            "roofline": {"bound": "tensor", "kernel": "pa_mla_sparse_decode", "achieved": tflops,
+            "roofline": {"bound": "tensor", "kernel": "pa_" + entry, "achieved": tflops,
                          "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                          "traffic": traffic, "peak_source": peak_src,
                          "us_per_launch": us_launch,

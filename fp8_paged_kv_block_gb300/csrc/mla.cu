@@ -25,6 +25,12 @@
 // own max and cast to BF16, and tiles are merged with exp(m_old - m_new) and
 // exp(m_tile - m_new). O^T is kept as O / beta, beta being the last merged
 // tile's exp(m_tile - m_new), so that C2 can accumulate into it directly.
+//
+// The same kernel also reads the rows that the KV compress epilog ("CANN
+// ops-transformer aclnnKvCompressEpilog 算子详解", 计算公式 场景 1 / 场景 2)
+// writes for d = 576: rope first, the nope codes in groups of 64 channels,
+// one BF16 or E8M0 scale per group. Only where the producers find the codes,
+// the rope bytes and the scale of a group differs (a template parameter).
 #include "common.cuh"
 
 #include <cuda_fp8.h>
@@ -39,6 +45,19 @@ namespace {
 constexpr int kDn = 512;            // kv_lora_rank: the nope part, also V
 constexpr int kDr = 64;             // rope part
 constexpr int kRowUsed = 656;       // kn 512 B | kr 128 B | 4 FP32 scales
+// Row formats. Page: the MLA page's packed row (E4M3 kn at byte 0, BF16 kr at
+// 512, four FP32 scales, one per 128 channels, at 640). KvcBf16 / KvcE8m0: the
+// KV compress epilog's row for d = 576 with quant mode 0 / 1 (BF16 kr at 0,
+// E4M3 kn at 128, at 640 one scale per 64 channels: 8 BF16 values / 8 E8M0
+// bytes e for 2^(e - 127)). Every format lies within bytes [0, 656).
+constexpr int kFmtPage = 0;
+constexpr int kFmtKvcBf16 = 1;
+constexpr int kFmtKvcE8m0 = 2;
+constexpr int kScaleOff = kDn + 2 * kDr;
+template <int F>
+constexpr int kCodeOff = F == kFmtPage ? 0 : 2 * kDr;
+template <int F>
+constexpr int kRopeOff = F == kFmtPage ? kDn : 0;
 constexpr int kHG = 64;             // query heads per CTA (N of C1 and C2)
 constexpr int kNK = 128;            // keys per tile (M of C1)
 constexpr int kNC = 9;              // 64-channel chunks of a 576-wide row
@@ -231,7 +250,7 @@ __device__ __forceinline__ void rows_locate(const MlaParams& p, int t, int cur, 
 
 // The codes and the scale unit of each row into registers (zeros for rows
 // that take no part); the rope bytes are brought to L2 for the later copy.
-template <int NG>
+template <int F, int NG>
 __device__ __forceinline__ void rows_load(const MlaParams& p, const int64_t (&ro)[NG], int cu, uint4 (&kn)[NG][4],
                                           uint4 (&sc)[NG])
 {
@@ -240,9 +259,9 @@ __device__ __forceinline__ void rows_load(const MlaParams& p, const int64_t (&ro
         if (ro[gi] >= 0) {
             const uint8_t* src = p.cache + ro[gi];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) kn[gi][i] = ldg_nc16(src + 16 * (cu + 8 * i));
-            sc[gi] = ldg_nc16(src + kDn + 2 * kDr);
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kDn + 16 * cu));
+            for (int i = 0; i < 4; ++i) kn[gi][i] = ldg_nc16(src + kCodeOff<F> + 16 * (cu + 8 * i));
+            sc[gi] = ldg_nc16(src + kScaleOff);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(src + kRopeOff<F> + 16 * cu));
         } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i) kn[gi][i] = make_uint4(0, 0, 0, 0);
@@ -260,10 +279,31 @@ __device__ __forceinline__ void rows_prefetch_l2(const MlaParams& p, const int64
         if (ro[gi] >= 0 && cu < 6) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.cache + ro[gi] + 128 * cu));
 }
 
-// Dequantise the rows' unit i (channels 128 i + 16 cu .. + 15 of each row's
-// group i) into chunk pair i, and the rope chunk; each step is announced on
-// k_full once the previous tile's C2 has released the chunks.
-template <int NG>
+// Dequant scale of a lane's code unit i (channels 128 i + 16 cu .. + 15) from
+// the row's 16-byte scale unit: the page row's FP32 scale of 128 channels i,
+// or the KV compress row's scale of 64 channels 2 i + cu / 4.
+template <int F>
+__device__ __forceinline__ float unit_scale(const uint4& s, int i, int cu)
+{
+    const uint32_t w = i == 0 ? s.x : i == 1 ? s.y : i == 2 ? s.z : s.w;
+    if constexpr (F == kFmtPage) {
+        return __uint_as_float(w);
+    } else if constexpr (F == kFmtKvcBf16) {
+        // BF16 scale 2 i + cu / 4: half cu / 4 of word i (little-endian)
+        return __uint_as_float(cu < 4 ? w << 16 : w & 0xFFFF0000u);
+    } else {
+        // E8M0 byte 2 i + cu / 4 of the first 8 bytes: 2^(e - 127), e = 0
+        // being the FP32 subnormal 2^-127
+        const uint32_t w8 = i < 2 ? s.x : s.y;
+        const uint32_t e = (w8 >> (8 * (2 * (i & 1) + (cu >> 2)))) & 0xFFu;
+        return __uint_as_float(e != 0 ? e << 23 : 0x00400000u);
+    }
+}
+
+// Dequantise the rows' unit i (channels 128 i + 16 cu .. + 15 of each row)
+// into chunk pair i, and the rope chunk; each step is announced on k_full
+// once the previous tile's C2 has released the chunks.
+template <int F, int NG>
 __device__ __forceinline__ void rows_produce(MlaSmem& sm, const MlaParams& p, int t, const int64_t (&ro)[NG],
                                              const uint4 (&kn)[NG][4], const uint4 (&sc)[NG], int rg0, int step,
                                              int lim, int rr, int cu, int lane)
@@ -279,7 +319,7 @@ __device__ __forceinline__ void rows_produce(MlaSmem& sm, const MlaParams& p, in
             if (rg >= lim) continue;
             const int k = 4 * rg + rr;
             const uint4 c8 = kn[gi][i];
-            const float f = __uint_as_float(i == 0 ? sc[gi].x : i == 1 ? sc[gi].y : i == 2 ? sc[gi].z : sc[gi].w);
+            const float f = unit_scale<F>(sc[gi], i, cu);
             uint4 lo, hi;
             lo.x = dq2(c8.x & 0xFFFFu, f);
             lo.y = dq2(c8.x >> 16, f);
@@ -305,7 +345,7 @@ __device__ __forceinline__ void rows_produce(MlaSmem& sm, const MlaParams& p, in
             const int k = 4 * rg + rr;
             uint8_t* dst = sm.kt[8] + sw128(k, cu);
             if (ro[gi] >= 0)
-                cp_async16(dst, p.cache + ro[gi] + kDn + 16 * cu, 16);
+                cp_async16(dst, p.cache + ro[gi] + kRopeOff<F> + 16 * cu, 16);
             else
                 *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
         }
@@ -316,6 +356,7 @@ __device__ __forceinline__ void rows_produce(MlaSmem& sm, const MlaParams& p, in
     if (lane == 0) mbar_arrive(&sm.k_full[4]);
 }
 
+template <int F>
 __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -389,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
             int64_t ro[kGroupsPerProd];
             uint4 kn[kGroupsPerProd][4], sc[kGroupsPerProd];
             rows_locate<kGroupsPerProd>(p, t, cur, act, b, tk_base, pw, kProdWarps, kProdGroups, rr, ro);
-            rows_load<kGroupsPerProd>(p, ro, cu, kn, sc);
-            rows_produce<kGroupsPerProd>(sm, p, t, ro, kn, sc, pw, kProdWarps, kProdGroups, rr, cu, lane);
+            rows_load<F, kGroupsPerProd>(p, ro, cu, kn, sc);
+            rows_produce<F, kGroupsPerProd>(sm, p, t, ro, kn, sc, pw, kProdWarps, kProdGroups, rr, cu, lane);
         }
     } else if (warp == kMmaWarp) {
         // ================================ MMA issue ================================
@@ -445,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
         rows_locate<kGroupsPerCons>(p, 0, cur, act, b, tk_base, crg0, kConsWarps, kRowGroups, rr, cro);
         {
             uint4 kn[kGroupsPerCons][4], sc[kGroupsPerCons];
-            rows_load<kGroupsPerCons>(p, cro, cu, kn, sc);
-            rows_produce<kGroupsPerCons>(sm, p, 0, cro, kn, sc, crg0, kConsWarps, kRowGroups, rr, cu, lane);
+            rows_load<F, kGroupsPerCons>(p, cro, cu, kn, sc);
+            rows_produce<F, kGroupsPerCons>(sm, p, 0, cro, kn, sc, crg0, kConsWarps, kRowGroups, rr, cu, lane);
         }
         if (ntiles > 1) {
             rows_locate<kGroupsPerCons>(p, 1, cur, act, b, tk_base, crg0, kConsWarps, kRowGroups, rr, cro);
@@ -566,9 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
             if (t + 1 < ntiles) {
                 {
                     uint4 kn[kGroupsPerCons][4], sc[kGroupsPerCons];
-                    rows_load<kGroupsPerCons>(p, cro, cu, kn, sc);
-                    rows_produce<kGroupsPerCons>(sm, p, t + 1, cro, kn, sc, crg0, kConsWarps, kRowGroups, rr, cu,
-                                                 lane);
+                    rows_load<F, kGroupsPerCons>(p, cro, cu, kn, sc);
+                    rows_produce<F, kGroupsPerCons>(sm, p, t + 1, cro, kn, sc, crg0, kConsWarps, kRowGroups, rr,
+                                                    cu, lane);
                 }
                 if (t + 2 < ntiles) {
                     rows_locate<kGroupsPerCons>(p, t + 2, cur, act, b, tk_base, crg0, kConsWarps, kRowGroups, rr,
@@ -621,44 +662,37 @@ static_assert(sizeof(MlaSmem) + 1024 <= 232448, "MLA decode shared memory over b
 
 inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-}  // namespace
-}  // namespace pa
-
-using namespace pa;
-
-extern "C" pa_status pa_mla_sparse_decode(const void* q_nope, const void* q_rope, const void* nope_cache,
-                                          int64_t row_bytes, const int32_t* topk_indices,
-                                          const int32_t* block_table, const int32_t* kv_act_seqs, void* out,
-                                          int B, int S1, int NQ, int n_kv, int topk, int block_size,
-                                          int64_t num_blocks, int max_blocks_per_seq, float softmax_scale,
-                                          int s2_tile, int* status, void* stream)
+// Validation and launch shared by the entry points; F is the row format.
+template <int F>
+pa_status mla_launch(const char* name, const void* q_nope, const void* q_rope, const void* cache, int64_t row_bytes,
+                     const int32_t* topk_indices, const int32_t* block_table, const int32_t* kv_act_seqs, void* out,
+                     int B, int S1, int NQ, int n_kv, int topk, int block_size, int64_t num_blocks,
+                     int max_blocks_per_seq, float softmax_scale, int s2_tile, int* status, void* stream)
 {
-    PA_REQUIRE(q_nope && q_rope && nope_cache && topk_indices && block_table && kv_act_seqs && out && status,
-               PA_ERR_NULLPTR, "pa_mla_sparse_decode: null pointer argument");
+    PA_REQUIRE(q_nope && q_rope && cache && topk_indices && block_table && kv_act_seqs && out && status,
+               PA_ERR_NULLPTR, "%s: null pointer argument", name);
     PA_REQUIRE(B >= 0 && S1 >= 1 && NQ >= 1 && topk >= 1 && block_size >= 1 && num_blocks >= 1 &&
                    max_blocks_per_seq >= 1,
-               PA_ERR_INVALID, "pa_mla_sparse_decode: bad sizes (B=%d S1=%d NQ=%d topk=%d block_size=%d)", B, S1,
-               NQ, topk, block_size);
+               PA_ERR_INVALID, "%s: bad sizes (B=%d S1=%d NQ=%d topk=%d block_size=%d)", name, B, S1, NQ, topk,
+               block_size);
     PA_REQUIRE(row_bytes >= kRowUsed && row_bytes % 16 == 0, PA_ERR_INVALID,
-               "pa_mla_sparse_decode: row_bytes %lld must be >= 656 and a multiple of 16",
-               static_cast<long long>(row_bytes));
-    PA_REQUIRE(std::isfinite(softmax_scale), PA_ERR_INVALID, "pa_mla_sparse_decode: softmax_scale not finite");
-    PA_REQUIRE(num_blocks * block_size <= 0x7FFFFFFF, PA_ERR_UNSUPPORTED,
-               "pa_mla_sparse_decode: more than 2^31 - 1 cache rows");
-    PA_REQUIRE(n_kv == 1, PA_ERR_UNSUPPORTED, "pa_mla_sparse_decode: n_kv %d (one latent KV head is built)", n_kv);
-    PA_REQUIRE(NQ % kHG == 0, PA_ERR_UNSUPPORTED, "pa_mla_sparse_decode: NQ %d (a multiple of 64 is built)", NQ);
-    PA_REQUIRE(s2_tile == kNK, PA_ERR_UNSUPPORTED, "pa_mla_sparse_decode: s2_tile %d (128 is built)", s2_tile);
-    PA_REQUIRE(aligned16(q_nope) && aligned16(q_rope) && aligned16(nope_cache) && aligned16(out) &&
+               "%s: row_bytes %lld must be >= 656 and a multiple of 16", name, static_cast<long long>(row_bytes));
+    PA_REQUIRE(std::isfinite(softmax_scale), PA_ERR_INVALID, "%s: softmax_scale not finite", name);
+    PA_REQUIRE(num_blocks * block_size <= 0x7FFFFFFF, PA_ERR_UNSUPPORTED, "%s: more than 2^31 - 1 cache rows", name);
+    PA_REQUIRE(n_kv == 1, PA_ERR_UNSUPPORTED, "%s: n_kv %d (one latent KV head is built)", name, n_kv);
+    PA_REQUIRE(NQ % kHG == 0, PA_ERR_UNSUPPORTED, "%s: NQ %d (a multiple of 64 is built)", name, NQ);
+    PA_REQUIRE(s2_tile == kNK, PA_ERR_UNSUPPORTED, "%s: s2_tile %d (128 is built)", name, s2_tile);
+    PA_REQUIRE(aligned16(q_nope) && aligned16(q_rope) && aligned16(cache) && aligned16(out) &&
                    (reinterpret_cast<uintptr_t>(status) & 3u) == 0,
-               PA_ERR_INVALID, "pa_mla_sparse_decode: q_nope, q_rope, nope_cache and out must be 16-byte aligned");
+               PA_ERR_INVALID, "%s: q_nope, q_rope, the cache and out must be 16-byte aligned", name);
     const int64_t grid = static_cast<int64_t>(B) * S1 * (NQ / kHG);
-    PA_REQUIRE(grid <= 0x7FFFFFFF, PA_ERR_INVALID, "pa_mla_sparse_decode: too many CTAs");
+    PA_REQUIRE(grid <= 0x7FFFFFFF, PA_ERR_INVALID, "%s: too many CTAs", name);
     if (grid == 0) return PA_OK;
 
     MlaParams prm;
     prm.q_nope = static_cast<const uint16_t*>(q_nope);
     prm.q_rope = static_cast<const uint16_t*>(q_rope);
-    prm.cache = static_cast<const uint8_t*>(nope_cache);
+    prm.cache = static_cast<const uint8_t*>(cache);
     prm.topk_idx = topk_indices;
     prm.block_table = block_table;
     prm.act = kv_act_seqs;
@@ -677,11 +711,48 @@ extern "C" pa_status pa_mla_sparse_decode(const void* q_nope, const void* q_rope
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [&] {
-        attr = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr = cudaFuncSetAttribute(mla_decode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem));
     });
-    PA_REQUIRE(attr == cudaSuccess, PA_ERR_CUDA, "pa_mla_sparse_decode: smem attribute: %s",
-               cudaGetErrorString(attr));
-    mla_decode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, static_cast<cudaStream_t>(stream)>>>(prm);
-    return check_launch("pa_mla_sparse_decode");
+    PA_REQUIRE(attr == cudaSuccess, PA_ERR_CUDA, "%s: smem attribute: %s", name, cudaGetErrorString(attr));
+    mla_decode_kernel<F><<<static_cast<unsigned>(grid), kThreads, smem, static_cast<cudaStream_t>(stream)>>>(prm);
+    return check_launch(name);
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_mla_sparse_decode(const void* q_nope, const void* q_rope, const void* nope_cache,
+                                          int64_t row_bytes, const int32_t* topk_indices,
+                                          const int32_t* block_table, const int32_t* kv_act_seqs, void* out,
+                                          int B, int S1, int NQ, int n_kv, int topk, int block_size,
+                                          int64_t num_blocks, int max_blocks_per_seq, float softmax_scale,
+                                          int s2_tile, int* status, void* stream)
+{
+    return mla_launch<kFmtPage>("pa_mla_sparse_decode", q_nope, q_rope, nope_cache, row_bytes, topk_indices,
+                                block_table, kv_act_seqs, out, B, S1, NQ, n_kv, topk, block_size, num_blocks,
+                                max_blocks_per_seq, softmax_scale, s2_tile, status, stream);
+}
+
+extern "C" pa_status pa_mla_sparse_decode_kvc(const void* q_nope, const void* q_rope, const void* kv_cache,
+                                              int64_t row_bytes, int quant_mode, const int32_t* topk_indices,
+                                              const int32_t* block_table, const int32_t* kv_act_seqs, void* out,
+                                              int B, int S1, int NQ, int n_kv, int topk, int block_size,
+                                              int64_t num_blocks, int max_blocks_per_seq, float softmax_scale,
+                                              int s2_tile, int* status, void* stream)
+{
+    PA_REQUIRE(quant_mode != 2, PA_ERR_UNSUPPORTED,
+               "pa_mla_sparse_decode_kvc: quant_mode 2 (HiFloat8 / FP4 rows) is not built");
+    PA_REQUIRE(quant_mode == 0 || quant_mode == 1, PA_ERR_INVALID, "pa_mla_sparse_decode_kvc: quant_mode %d",
+               quant_mode);
+    if (quant_mode == 0)
+        return mla_launch<kFmtKvcBf16>("pa_mla_sparse_decode_kvc", q_nope, q_rope, kv_cache, row_bytes,
+                                       topk_indices, block_table, kv_act_seqs, out, B, S1, NQ, n_kv, topk,
+                                       block_size, num_blocks, max_blocks_per_seq, softmax_scale, s2_tile, status,
+                                       stream);
+    return mla_launch<kFmtKvcE8m0>("pa_mla_sparse_decode_kvc", q_nope, q_rope, kv_cache, row_bytes, topk_indices,
+                                   block_table, kv_act_seqs, out, B, S1, NQ, n_kv, topk, block_size, num_blocks,
+                                   max_blocks_per_seq, softmax_scale, s2_tile, status, stream);
 }

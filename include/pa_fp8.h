@@ -401,6 +401,42 @@ PA_API pa_status pa_mla_sparse_decode(const void* q_nope, const void* q_rope,
                                       int max_blocks_per_seq, float softmax_scale,
                                       int s2_tile, int* status, void* stream);
 
+/* ------------------------------------------------------------------------
+ * The MLA sparse decode above over cache rows that pa_fp8_kv_compress_epilog
+ * wrote with d = 576 (nope 512, rope 64): the decode side of the KV compress
+ * epilog ("CANN ops-transformer aclnnKvCompressEpilog 算子详解", 计算公式
+ * 场景 1 / 场景 2) read with [MS]'s dequantisation rule (在线反量化:
+ * BF16(FP32(code) * scale)), each 64-channel group by its own scale.
+ *
+ * Row layout (bytes; the rest of the row is not used):
+ *   [0, 128)    kr, 64 BF16 values;
+ *   [128, 640)  kn, 512 E4M3 codes;
+ *   quant_mode 0: [640, 656) eight BF16 scales s_g, one per 64 channels;
+ *   quant_mode 1: [640, 648) eight E8M0 bytes e_g for s_g = 2^(e_g - 127)
+ *                 (byte 255 is out of contract; the epilog writes <= 254).
+ * kn[c] = BF16(FP32(E4M3 code c) * s_{c / 64}); everything else (gather,
+ * visible count, masking, C1, tile-local softmax, BF16 P, C2, merge, output)
+ * is the same as pa_mla_sparse_decode.
+ *
+ * Arguments: as pa_mla_sparse_decode, with
+ *   kv_cache      bytes [num_blocks*block_size, row_bytes], blocks contiguous
+ *                 (the epilog's block_stride = block_size * head_dim); row_bytes
+ *                 = the epilog's head_dim, >= 656 and a multiple of 16 (mode 1
+ *                 rows of the minimum 648 bytes do not qualify: pad to 656).
+ *   quant_mode    0 or 1 as given to the epilog; 2 (HiFloat8 rope, FP4 nope)
+ *                 returns PA_ERR_UNSUPPORTED, anything else PA_ERR_INVALID.
+ * Nothing is allocated; the call is asynchronous on `stream`.
+ * ------------------------------------------------------------------------ */
+PA_API pa_status pa_mla_sparse_decode_kvc(const void* q_nope, const void* q_rope,
+                                          const void* kv_cache, int64_t row_bytes,
+                                          int quant_mode, const int32_t* topk_indices,
+                                          const int32_t* block_table,
+                                          const int32_t* kv_act_seqs, void* out,
+                                          int B, int S1, int NQ, int n_kv, int topk,
+                                          int block_size, int64_t num_blocks,
+                                          int max_blocks_per_seq, float softmax_scale,
+                                          int s2_tile, int* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -178,3 +178,35 @@ def test_mla_sparse_decode_rejects_bad_arguments(L):
     assert b"s2_tile" in L.pa_last_error()
     assert call(out=P(258)) == 2             # alignment
     assert call(B=0) == 0                    # nothing to do, nothing enqueued
+
+
+def test_mla_sparse_decode_kvc_rejects_bad_arguments(L):
+    """Host validation of the MLA decode over KV compress epilog rows: the
+    shared checks, plus the quant mode (0 and 1 are built, 2 is HiFloat8)."""
+    P = ctypes.c_void_p
+    fake = P(256)
+    f = L.pa_mla_sparse_decode_kvc
+    scale = ctypes.c_float(1.0 / 24.0)
+
+    def call(**kw):
+        a = dict(qn=fake, qr=fake, cache=fake, row_bytes=672, mode=0, tk=fake, bt=fake, act=fake,
+                 out=fake, B=4, S1=2, NQ=128, n_kv=1, topk=2048, bs=128, nb=100, mb=512, s2=128,
+                 status=fake)
+        a.update(kw)
+        return f(a["qn"], a["qr"], a["cache"], ctypes.c_int64(a["row_bytes"]), a["mode"], a["tk"],
+                 a["bt"], a["act"], a["out"], a["B"], a["S1"], a["NQ"], a["n_kv"], a["topk"],
+                 a["bs"], ctypes.c_int64(a["nb"]), a["mb"], scale, a["s2"], a["status"], None)
+
+    assert call(mode=2) == 5                 # HiFloat8 / FP4 rows
+    assert b"quant_mode" in L.pa_last_error()
+    assert call(mode=3) == 2
+    assert call(mode=-1) == 2
+    assert call(cache=None) == 1
+    assert call(row_bytes=648) == 2          # the minimum mode-1 row is not 16-byte aligned
+    assert call(mode=1, row_bytes=648) == 2
+    assert call(n_kv=2) == 5
+    assert call(NQ=96) == 5
+    assert call(s2=64) == 5
+    assert call(qn=P(264)) == 2              # alignment
+    assert call(B=0) == 0
+    assert call(mode=1, B=0) == 0

@@ -513,6 +513,21 @@ class MlaCase:
         out[:, end:] = 0xFF
         return out
 
+    def key_rows(self, rows: np.ndarray) -> np.ndarray:
+        """float32 [len(rows), 576] holding BF16 values: unquantised key rows
+        [nope 512 | rope 64] of these physical rows, N(0,1) truncated to BF16,
+        for an append step (the KV compress epilog) to write into the cache.
+        A row's values depend on its id alone."""
+        rows = np.asarray(rows, dtype=np.int64)
+        n = rows.size
+        h = _hashed_words(self.seed, rows, (MLA_DN + MLA_DR) // 2, 5)
+        u = ((h & np.uint64(0xFFFFFFFF)).astype(np.float32) + 0.5) * np.float32(2.0 ** -32)
+        v = ((h >> np.uint64(32)).astype(np.float32) + 0.5) * np.float32(2.0 ** -32)
+        r = np.sqrt(np.float32(-2.0) * np.log(u))
+        x = np.concatenate([r * np.cos(np.float32(2.0 * np.pi) * v),
+                            r * np.sin(np.float32(2.0 * np.pi) * v)], axis=1).astype(np.float32)
+        return (x.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).reshape(n, -1)
+
     def cache(self, rows=None, fmt: int = MLA_FORMAT_PAGE) -> np.ndarray:
         """uint8 [num_blocks*BS, 672]: every row drawn (rows=None), or only the
         listed rows drawn and the others zero."""
