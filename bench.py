@@ -18,6 +18,7 @@ pages) on a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -57,8 +58,8 @@ FALLBACK_HBM_GBS = 6800.0
 OVERLAP_DECODE = 2
 OVERLAP_APPEND = True
 
-DECODE_TRAFFIC = {"sources_sha1": "7a0f808934febb1bf199e314f196c867adb2dfdb",
-                  "bytes_per_launch": 57871616 + 131328}
+DECODE_TRAFFIC = {"sources_sha1": "f2c5a5a43f9dc2eb1c0f2c1fbccdc9e4a25a999c",
+                  "bytes_per_launch": 57871104 + 107008}
 
 
 def parse_args():
@@ -67,7 +68,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["glm45_step", "mla"], default="glm45_step",
+    ap.add_argument("--workload", choices=["glm45_step", "mla", "configs"], default="glm45_step",
                     help="glm45_step: the GLM-4.5 append + decode step (default); mla: the "
                          "MLA sparse FP8 decode at the DeepSeek-V3.2 page's b=64 case")
     ap.add_argument("--mla-format", choices=["page", "kvc0", "kvc1"], default="page",
@@ -320,6 +321,14 @@ def reference_arm(args, rank, world):
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.workload == "configs":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the configs sweep has no "
+                                  "reference arm; the oracle is timed on the default workload"}))
+            return
+        configs_arm(args, rank, world, local)
+        return
     if args.workload == "mla":
         if args.impl == "reference":
             mla_reference_arm(args, rank, world)
@@ -569,6 +578,163 @@ def main():
 
 
 # --------------------------------------------------------------------------
+# Every decode configuration (--workload configs): one JSON line each
+# --------------------------------------------------------------------------
+
+CONFIGS = [  # (name, workload, description)
+    ("tiny", workloads.tiny, "B=2 S1=1 NQ=4 NKV=1 kv {37,300} s2_tile=512 PA_BSND"),
+    ("glm45", workloads.glm, "B=16 S1=1 NQ=96 NKV=8 kv~U[1,4096] s2_tile=512 PA_BSND"),
+    ("long", workloads.long_ctx, "B=4 S1=1 NQ=96 NKV=8 kv~U[32768,131072], every 64th K row x8 "
+                                 "before quantisation, s2_tile=512 PA_BSND"),
+    ("ragged", workloads.ragged, "B=256 S1=2 NQ=96 NKV=8 kv~lognormal(median 1024, sigma 1) "
+                                 "clipped to [1,16384] s2_tile=512 PA_BSND"),
+    ("append", workloads.append, "64 new BF16 K/V rows (5% of slots -1) into contexts "
+                                 "U[512,8192], NQ=96 NKV=8 BNBD, then decode over the updated cache"),
+]
+
+
+def configs_arm(args, rank, world, local):
+    """Decode time per launch for each configuration, inputs built on the
+    device with the library's own kernels (as the parity tests build them);
+    append + decode step for the append configuration."""
+    import torch
+    import fp8_paged_kv_block_gb300 as pa
+    from fp8_paged_kv_block_gb300 import paged
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_ranks(world, "nccl", dev)
+    pa.build()
+    pa.lib()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, peak_src = measured_hbm_peak()
+
+    def timed(fn, n, reps):
+        """ms per call of fn(i): a graph of reps calls replayed n // reps times."""
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(reps):
+                fn(i)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                fn(i)
+        for _ in range(max(args.warmup, 3)):
+            g.replay()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200000)
+        e0.record()
+        for _ in range(max(1, n // reps)):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1), world, dev) / (max(1, n // reps) * reps)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    lines = []
+    for name, make, desc in CONFIGS:
+        made = make()
+        app = made if name == "append" else None
+        case = app.ctx if app is not None else made
+        act_after = app.act_after if app is not None else case.act
+        dcase = dataclasses.replace(case, act=act_after)
+        dec_bytes = dcase.algorithmic_bytes()
+        q8, qs = paged.quantize_queries(torch.from_numpy(case.q()).to(dev))
+        k32, v32 = case.kv()
+        base = paged.build_cache(torch.from_numpy(k32).to(dev), torch.from_numpy(v32).to(dev),
+                                 torch.from_numpy(case.cu_seqlens).to(dev),
+                                 torch.from_numpy(case.slots).to(dev),
+                                 torch.from_numpy(case.token_batch).to(dev), case.num_blocks,
+                                 case.layout)
+        del k32, v32
+        case.drop()
+        cache_bytes = 2 * base.k_cache.numel() + 4 * base.k_scale.numel()
+        copies = max(1, math.ceil(3 * l2 / cache_bytes))
+        caches = [base] + [paged.PagedFP8(base.k_cache.clone(), base.v_cache.clone(),
+                                          base.k_scale.clone(), base.v_scale.clone(), base.layout)
+                           for _ in range(copies - 1)]
+        bt = torch.from_numpy(case.block_table).to(dev)
+        act_d = torch.from_numpy(act_after).to(dev)
+        out = torch.empty((case.B * case.S1, case.NQ, case.D), dtype=torch.bfloat16, device=dev)
+        ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile,
+                                device=dev)
+
+        def attend(i, overlap=OVERLAP_DECODE):
+            c = caches[i % copies]
+            pa.decode(q8, qs, c.k_cache, c.k_scale, c.v_cache, c.v_scale, bt, act_d, out,
+                      S1=case.S1, layout=case.layout, s2_tile=case.s2_tile,
+                      softmax_scale=case.softmax_scale, workspace=ws, overlap_prologue=overlap)
+
+        est_us = max(5.0, dec_bytes / (peak * 1e3) * 2.0)
+        n = max(50, min(args.steps, int(100000 / est_us)))
+        reps = copies * max(1, math.ceil(16 / copies))
+        ms_dec = timed(attend, n, reps)
+        ms_dec0 = timed(lambda i: attend(i, 0), n, reps)
+        extra = {}
+        if app is not None:
+            kb, vb = app.new_kv_bf16()
+            kn_d, vn_d = kb.to(dev), vb.to(dev)
+            slot_d = torch.from_numpy(app.slot_mapping).to(dev)
+            tb_d = torch.from_numpy(app.token_batch).to(dev)
+            app_bytes = (app.T * case.NKV * (2 * case.D * 2 + 2 * case.D + 4) + app.T * 8)
+
+            def append(i):
+                c = caches[i % copies]
+                pa.cache_quant_scatter(kn_d, vn_d, c.k_cache, c.v_cache, slot_d, c.k_scale,
+                                       c.v_scale, tb_d, layout=case.layout,
+                                       overlap_prologue=OVERLAP_APPEND)
+
+            def step(i):
+                append(i)
+                attend(i)
+
+            ms_app = timed(append, n, reps)
+            ms_step = timed(step, n, reps)
+            extra = {"append_us_per_launch": ms_app * 1e3, "append_bytes": app_bytes,
+                     "step_us": ms_step * 1e3,
+                     "step_gbs": world * (dec_bytes + app_bytes) / (ms_step * 1e-3) / 1e9}
+        assert ws.error_flags() == 0, "decode kernel reported a wait timeout"
+        gbs = dec_bytes / (ms_dec * 1e-3) / 1e9
+        lines.append({
+            "metric": METRIC, "value": world * gbs, "unit": UNIT, "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": ms_dec,
+            "us_per_step": ms_dec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3+f32", "data": "synthetic",
+            "config": {"workload": name + ": " + desc, "B": case.B, "S1": case.S1,
+                       "kv_tokens": int(act_after.sum()), "decode_bytes": dec_bytes,
+                       "l2": ("inputs larger than L2: %d cache copies rotated (%.0f MB, L2 %.0f MB)"
+                              % (copies, copies * cache_bytes / 1e6, l2 / 1e6)),
+                       "timing": "CUDA graph of back-to-back decode launches "
+                                 "(overlap_prologue=%d), CUDA events" % OVERLAP_DECODE},
+            "gpu_launches": n,
+            "roofline": {"bound": "hbm", "kernel": "pa_fp8_decode", "achieved": gbs, "peak": peak,
+                         "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                         "peak_source": peak_src, "frac_of_8tbs_nominal": gbs / 8000.0,
+                         "us_per_launch": ms_dec * 1e3,
+                         "us_per_launch_stream_order": ms_dec0 * 1e3},
+            "tokens_per_s": world * case.B * case.S1 / (ms_dec * 1e-3),
+            **extra,
+        })
+        del caches, base, out, ws
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    if rank == 0:
+        for line in lines:
+            line["clocks"] = clk
+            print(json.dumps(line), flush=True)
+    finish_ranks(world)
+
+
+# --------------------------------------------------------------------------
 # MLA sparse FP8 decode (DeepSeek-V3.2 shape)
 # --------------------------------------------------------------------------
 
@@ -595,8 +761,8 @@ MLA_VARIANTS = 2          # top-k selections rotated between steps (each ~172 MB
 # valid only for the kernel source it was taken with.
 # Captured on the 16-sequence case and scaled by the selected rows (x4): each
 # row is read from DRAM once, so the traffic grows in proportion.
-MLA_TRAFFIC = {"sources_sha1": "495ff6dfa6d80de79b093600199b93ebcefad886", "format": "page",
-               "bytes_per_launch": 4 * (54291200 + 381952)}
+MLA_TRAFFIC = {"sources_sha1": "f10072f4bc2b9234db2c028594393e1055ae42f1", "format": "page",
+               "bytes_per_launch": 4 * (54290176 + 382720)}
 
 
 def mla_sources_sha1() -> str:

@@ -98,8 +98,8 @@ def lib():
         L.pa_mla_sparse_decode.argtypes = [P, P, P, i64, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                            i64, i32, f32, i32, P, P]
         L.pa_mla_sparse_decode.restype = i32
-        L.pa_mla_sparse_decode_kvc.argtypes = [P, P, P, i64, i32, P, P, P, P, i32, i32, i32, i32,
-                                               i32, i32, i64, i32, f32, i32, P, P]
+        L.pa_mla_sparse_decode_kvc.argtypes = [P, P, P, i64, i64, i32, P, P, P, P, i32, i32, i32,
+                                               i32, i32, i32, i64, i32, f32, i32, P, P]
         L.pa_mla_sparse_decode_kvc.restype = i32
         _lib = L
         return L
@@ -389,12 +389,10 @@ class MlaStatus:
         return int(self.buf.item())
 
 
-def _mla_args(q_nope, q_rope, cache, topk_indices, block_table, kv_act_seqs, out, S1,
-              block_size, softmax_scale):
+def _mla_args(q_nope, q_rope, topk_indices, block_table, kv_act_seqs, out, S1, softmax_scale):
     torch = _torch()
     _need(q_nope, "q_nope", torch.bfloat16)
     _need(q_rope, "q_rope", torch.bfloat16)
-    _need(cache, "cache", torch.uint8)
     _need(topk_indices, "topk_indices", torch.int32)
     _need(block_table, "block_table", torch.int32)
     _need(kv_act_seqs, "kv_act_seqs", torch.int32)
@@ -405,12 +403,9 @@ def _mla_args(q_nope, q_rope, cache, topk_indices, block_table, kv_act_seqs, out
     B = kv_act_seqs.shape[0]
     if T != B * S1 or topk_indices.shape[0] != T:
         raise ValueError("B*S1 must equal the query token count of q_nope and topk_indices")
-    rows, row_bytes = cache.shape
-    if rows % block_size:
-        raise ValueError("cache rows must be a multiple of block_size")
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(576.0)
-    return B, NQ, rows, row_bytes, float(softmax_scale)
+    return B, NQ, float(softmax_scale)
 
 
 def mla_sparse_decode(q_nope, q_rope, nope_cache, topk_indices, block_table, kv_act_seqs, out, *,
@@ -423,8 +418,13 @@ def mla_sparse_decode(q_nope, q_rope, nope_cache, topk_indices, block_table, kv_
     BF16 kr | 4 FP32 scales, row_bytes >= 656); topk_indices int32
     [B*S1, topk]; block_table int32 [B, max_blocks]; kv_act_seqs int32 [B];
     out bfloat16 [B*S1, NQ, 512]."""
-    B, NQ, rows, row_bytes, sc = _mla_args(q_nope, q_rope, nope_cache, topk_indices, block_table,
-                                           kv_act_seqs, out, S1, block_size, softmax_scale)
+    torch = _torch()
+    B, NQ, sc = _mla_args(q_nope, q_rope, topk_indices, block_table, kv_act_seqs, out, S1,
+                          softmax_scale)
+    _need(nope_cache, "nope_cache", torch.uint8)
+    rows, row_bytes = nope_cache.shape
+    if rows % block_size:
+        raise ValueError("nope_cache rows must be a multiple of block_size")
     st = lib().pa_mla_sparse_decode(_ptr(q_nope), _ptr(q_rope), _ptr(nope_cache), row_bytes,
                                     _ptr(topk_indices), _ptr(block_table), _ptr(kv_act_seqs),
                                     _ptr(out), B, S1, NQ, 1, topk_indices.shape[1], block_size,
@@ -438,15 +438,32 @@ def mla_sparse_decode_kvc(q_nope, q_rope, kv_cache, topk_indices, block_table, k
                           softmax_scale=None, s2_tile: int = 128, stream=None):
     """The MLA sparse decode of ``mla_sparse_decode`` over cache rows written by
     ``kv_compress_epilog`` with d = 576 and the given quant_mode (0: BF16 group
-    scales, 1: E8M0 group scales): kv_cache uint8 [num_blocks*block_size,
-    row_bytes] with row_bytes the epilog's head_dim (>= 656, a multiple of 16)
-    and contiguous blocks (block_stride = block_size * row_bytes)."""
-    B, NQ, rows, row_bytes, sc = _mla_args(q_nope, q_rope, kv_cache, topk_indices, block_table,
-                                           kv_act_seqs, out, S1, block_size, softmax_scale)
+    scales, 1: E8M0 group scales). kv_cache is the epilog's cache, uint8
+    [block_num, block_size, 1, head_dim] (blocks may be strided, rows within a
+    block contiguous), or [block_num * block_size, head_dim]; head_dim >= 656
+    and a multiple of 16."""
+    torch = _torch()
+    B, NQ, sc = _mla_args(q_nope, q_rope, topk_indices, block_table, kv_act_seqs, out, S1,
+                          softmax_scale)
+    _need(kv_cache, "kv_cache", torch.uint8, contiguous=False)
+    if kv_cache.dim() == 4:
+        nb, bs, one, row_bytes = kv_cache.shape
+        if one != 1 or bs != block_size or kv_cache.stride(3) != 1 or kv_cache.stride(1) != row_bytes:
+            raise ValueError("kv_cache must be [block_num, block_size, 1, head_dim] with "
+                             "contiguous rows inside a block")
+        stride = kv_cache.stride(0)
+    elif kv_cache.dim() == 2 and kv_cache.is_contiguous():
+        rows, row_bytes = kv_cache.shape
+        if rows % block_size:
+            raise ValueError("kv_cache rows must be a multiple of block_size")
+        nb, stride = rows // block_size, block_size * row_bytes
+    else:
+        raise ValueError("kv_cache must be [block_num, block_size, 1, head_dim] or a contiguous "
+                         "[block_num * block_size, head_dim]")
     st = lib().pa_mla_sparse_decode_kvc(_ptr(q_nope), _ptr(q_rope), _ptr(kv_cache), row_bytes,
-                                        int(quant_mode), _ptr(topk_indices), _ptr(block_table),
-                                        _ptr(kv_act_seqs), _ptr(out), B, S1, NQ, 1,
-                                        topk_indices.shape[1], block_size, rows // block_size,
+                                        stride, int(quant_mode), _ptr(topk_indices),
+                                        _ptr(block_table), _ptr(kv_act_seqs), _ptr(out), B, S1,
+                                        NQ, 1, topk_indices.shape[1], block_size, nb,
                                         block_table.shape[1], sc, s2_tile, _ptr(status.buf),
                                         _stream(stream))
     _check(st, "pa_mla_sparse_decode_kvc")

@@ -880,42 +880,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!pos_eq(x2, end)) x2 = advance(x2, len2, len2);
 
         // ---- S^T of this warp's blocks and their key scales ----
+        // With 32 query rows and two blocks per warp, the scores of both blocks
+        // do not fit in registers next to the rest of the state (they spill):
+        // each block is read from tensor memory twice instead, once for the
+        // row maxima and once for P, and the S^T buffer is released after the
+        // second read.
+        constexpr bool kReload = NR == 32 && MBW > 1;
+        constexpr int SVB = kReload ? 1 : MBW;
         mbar_wait(&sm.s_full[sb], (tcount / NSB) & 1, p.err, 256, &sm.abort);
         tc_fence_after();
-        float sv[MBW][NR];
+        float sv[SVB][NR];
+        if constexpr (!kReload) {
 #pragma unroll
-        for (int jj = 0; jj < MBW; ++jj) {
-            const int mb = hh * MBW + jj;
-            if (mb < nb) tmem_ld_cols<NR>(tl + sb * SC + mb * NR, sv[jj]);
+            for (int jj = 0; jj < MBW; ++jj) {
+                const int mb = hh * MBW + jj;
+                if (mb < nb) tmem_ld_cols<NR>(tl + sb * SC + mb * NR, sv[jj]);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
         }
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
 
         // ---- scores x = S * q_scale * scale * log2(e) * k_scale; tile row maxima ----
-        float qsc[NR];
-#pragma unroll
-        for (int r4 = 0; r4 < NR / 4; ++r4) {
-            const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
-            qsc[4 * r4 + 0] = q4v.x;
-            qsc[4 * r4 + 1] = q4v.y;
-            qsc[4 * r4 + 2] = q4v.z;
-            qsc[4 * r4 + 3] = q4v.w;
-        }
         float mloc[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) mloc[r] = -INFINITY;
+        if constexpr (!kReload) {
+            float qsc[NR];
 #pragma unroll
-        for (int jj = 0; jj < MBW; ++jj) {
-            const int mb = hh * MBW + jj;
-            if (mb < nb) {
-                const bool ok = mb * kBS + 32 * q4 + lane < valid;
+            for (int r4 = 0; r4 < NR / 4; ++r4) {
+                const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
+                qsc[4 * r4 + 0] = q4v.x;
+                qsc[4 * r4 + 1] = q4v.y;
+                qsc[4 * r4 + 2] = q4v.z;
+                qsc[4 * r4 + 3] = q4v.w;
+            }
 #pragma unroll
-                for (int r = 0; r < NR; ++r) {
-                    const float xv = ok ? (sv[jj][r] * qsc[r]) * ksv[jj] : -INFINITY;
-                    sv[jj][r] = xv;
-                    mloc[r] = fmaxf(mloc[r], xv);
+            for (int jj = 0; jj < MBW; ++jj) {
+                const int mb = hh * MBW + jj;
+                if (mb < nb) {
+                    const bool ok = mb * kBS + 32 * q4 + lane < valid;
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) {
+                        const float xv = ok ? (sv[jj][r] * qsc[r]) * ksv[jj] : -INFINITY;
+                        sv[jj][r] = xv;
+                        mloc[r] = fmaxf(mloc[r], xv);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int jj = 0; jj < MBW; ++jj) {
+                const int mb = hh * MBW + jj;
+                if (mb < nb) {
+                    tmem_ld_cols<NR>(tl + sb * SC + mb * NR, sv[0]);
+                    tmem_wait_ld();
+                    const bool ok = mb * kBS + 32 * q4 + lane < valid;
+#pragma unroll
+                    for (int r4 = 0; r4 < NR / 4; ++r4) {
+                        const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
+                        const float qv[4] = {q4v.x, q4v.y, q4v.z, q4v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r = 4 * r4 + e;
+                            const float xv = ok ? (sv[0][r] * qv[e]) * ksv[jj] : -INFINITY;
+                            mloc[r] = fmaxf(mloc[r], xv);
+                        }
+                    }
                 }
             }
         }
@@ -952,14 +984,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int mb = hh * MBW + jj;
             if (mb < nb) {
                 const int tok = mb * kBS + 32 * q4 + lane;
+                float* x = sv[kReload ? 0 : jj];
+                if constexpr (kReload) {
+                    // the same scores as in the first pass, bit for bit
+                    tmem_ld_cols<NR>(tl + sb * SC + mb * NR, x);
+                    tmem_wait_ld();
+                    const bool ok = tok < valid;
+#pragma unroll
+                    for (int r4 = 0; r4 < NR / 4; ++r4) {
+                        const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
+                        x[4 * r4 + 0] = ok ? (x[4 * r4 + 0] * q4v.x) * ksv[jj] : -INFINITY;
+                        x[4 * r4 + 1] = ok ? (x[4 * r4 + 1] * q4v.y) * ksv[jj] : -INFINITY;
+                        x[4 * r4 + 2] = ok ? (x[4 * r4 + 2] * q4v.z) * ksv[jj] : -INFINITY;
+                        x[4 * r4 + 3] = ok ? (x[4 * r4 + 3] * q4v.w) * ksv[jj] : -INFINITY;
+                    }
+                }
                 uint32_t pk[NR / 4];
 #pragma unroll
                 for (int r4 = 0; r4 < NR / 4; ++r4) {
                     const float4 m4 = *reinterpret_cast<const float4*>(&sm.wst[warp][0][4 * r4]);
-                    const float e0 = ex2(sv[jj][4 * r4 + 0] - m4.x);
-                    const float e1 = ex2(sv[jj][4 * r4 + 1] - m4.y);
-                    const float e2 = ex2(sv[jj][4 * r4 + 2] - m4.z);
-                    const float e3 = ex2(sv[jj][4 * r4 + 3] - m4.w);
+                    const float e0 = ex2(x[4 * r4 + 0] - m4.x);
+                    const float e1 = ex2(x[4 * r4 + 1] - m4.y);
+                    const float e2 = ex2(x[4 * r4 + 2] - m4.z);
+                    const float e3 = ex2(x[4 * r4 + 3] - m4.w);
                     ls[4 * r4 + 0] += e0;
                     ls[4 * r4 + 1] += e1;
                     ls[4 * r4 + 2] += e2;
@@ -972,6 +1019,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4*>(dst + a * 128) =
                         make_uint4(pk[4 * a], pk[4 * a + 1], pk[4 * a + 2], pk[4 * a + 3]);
             }
+        }
+        if constexpr (kReload) {
+            // both reads of this tile's S^T are done: MM1 may reuse the buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
         }
         // ---- this warp's share of MM2: the k-step of its 32 tokens in each of
         // its blocks, O^T[chan][row] += V^T[chan][tok] . P8^T[tok][row] (O^T

@@ -105,6 +105,7 @@ struct MlaParams {
     uint16_t* out;
     int* err;
     int64_t row_bytes;
+    int64_t block_stride;             // bytes from one block to the next (>= BS * row_bytes)
     int64_t num_blocks;
     int S1, NQ, topk, BS, max_blocks;
     float scale_log2;                 // softmax_scale * log2(e)
@@ -242,7 +243,7 @@ __device__ __forceinline__ void rows_locate(const MlaParams& p, int t, int cur, 
                 int blk = bi < p.max_blocks ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + bi)
                                             : 0;
                 if (blk < 0 || blk >= p.num_blocks) blk = 0;
-                ro[gi] = (static_cast<int64_t>(blk) * p.BS + idx % p.BS) * p.row_bytes;
+                ro[gi] = static_cast<int64_t>(blk) * p.block_stride + static_cast<int64_t>(idx % p.BS) * p.row_bytes;
             }
         }
     }
@@ -665,7 +666,7 @@ inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr
 // Validation and launch shared by the entry points; F is the row format.
 template <int F>
 pa_status mla_launch(const char* name, const void* q_nope, const void* q_rope, const void* cache, int64_t row_bytes,
-                     const int32_t* topk_indices, const int32_t* block_table, const int32_t* kv_act_seqs, void* out,
+                     int64_t block_stride, const int32_t* topk_indices, const int32_t* block_table, const int32_t* kv_act_seqs, void* out,
                      int B, int S1, int NQ, int n_kv, int topk, int block_size, int64_t num_blocks,
                      int max_blocks_per_seq, float softmax_scale, int s2_tile, int* status, void* stream)
 {
@@ -677,6 +678,9 @@ pa_status mla_launch(const char* name, const void* q_nope, const void* q_rope, c
                block_size);
     PA_REQUIRE(row_bytes >= kRowUsed && row_bytes % 16 == 0, PA_ERR_INVALID,
                "%s: row_bytes %lld must be >= 656 and a multiple of 16", name, static_cast<long long>(row_bytes));
+    PA_REQUIRE(block_stride >= block_size * row_bytes && block_stride % 16 == 0, PA_ERR_INVALID,
+               "%s: block_stride %lld must be >= block_size * row_bytes and a multiple of 16", name,
+               static_cast<long long>(block_stride));
     PA_REQUIRE(std::isfinite(softmax_scale), PA_ERR_INVALID, "%s: softmax_scale not finite", name);
     PA_REQUIRE(num_blocks * block_size <= 0x7FFFFFFF, PA_ERR_UNSUPPORTED, "%s: more than 2^31 - 1 cache rows", name);
     PA_REQUIRE(n_kv == 1, PA_ERR_UNSUPPORTED, "%s: n_kv %d (one latent KV head is built)", name, n_kv);
@@ -699,6 +703,7 @@ pa_status mla_launch(const char* name, const void* q_nope, const void* q_rope, c
     prm.out = static_cast<uint16_t*>(out);
     prm.err = status;
     prm.row_bytes = row_bytes;
+    prm.block_stride = block_stride;
     prm.num_blocks = num_blocks;
     prm.S1 = S1;
     prm.NQ = NQ;
@@ -731,28 +736,31 @@ extern "C" pa_status pa_mla_sparse_decode(const void* q_nope, const void* q_rope
                                           int64_t num_blocks, int max_blocks_per_seq, float softmax_scale,
                                           int s2_tile, int* status, void* stream)
 {
-    return mla_launch<kFmtPage>("pa_mla_sparse_decode", q_nope, q_rope, nope_cache, row_bytes, topk_indices,
-                                block_table, kv_act_seqs, out, B, S1, NQ, n_kv, topk, block_size, num_blocks,
-                                max_blocks_per_seq, softmax_scale, s2_tile, status, stream);
+    return mla_launch<kFmtPage>("pa_mla_sparse_decode", q_nope, q_rope, nope_cache, row_bytes,
+                                static_cast<int64_t>(block_size) * row_bytes, topk_indices, block_table,
+                                kv_act_seqs, out, B, S1, NQ, n_kv, topk, block_size, num_blocks, max_blocks_per_seq,
+                                softmax_scale, s2_tile, status, stream);
 }
 
 extern "C" pa_status pa_mla_sparse_decode_kvc(const void* q_nope, const void* q_rope, const void* kv_cache,
-                                              int64_t row_bytes, int quant_mode, const int32_t* topk_indices,
-                                              const int32_t* block_table, const int32_t* kv_act_seqs, void* out,
-                                              int B, int S1, int NQ, int n_kv, int topk, int block_size,
-                                              int64_t num_blocks, int max_blocks_per_seq, float softmax_scale,
-                                              int s2_tile, int* status, void* stream)
+                                              int64_t row_bytes, int64_t block_stride, int quant_mode,
+                                              const int32_t* topk_indices, const int32_t* block_table,
+                                              const int32_t* kv_act_seqs, void* out, int B, int S1, int NQ,
+                                              int n_kv, int topk, int block_size, int64_t num_blocks,
+                                              int max_blocks_per_seq, float softmax_scale, int s2_tile,
+                                              int* status, void* stream)
 {
     PA_REQUIRE(quant_mode != 2, PA_ERR_UNSUPPORTED,
                "pa_mla_sparse_decode_kvc: quant_mode 2 (HiFloat8 / FP4 rows) is not built");
     PA_REQUIRE(quant_mode == 0 || quant_mode == 1, PA_ERR_INVALID, "pa_mla_sparse_decode_kvc: quant_mode %d",
                quant_mode);
+    if (block_stride == 0) block_stride = static_cast<int64_t>(block_size) * row_bytes;
     if (quant_mode == 0)
         return mla_launch<kFmtKvcBf16>("pa_mla_sparse_decode_kvc", q_nope, q_rope, kv_cache, row_bytes,
-                                       topk_indices, block_table, kv_act_seqs, out, B, S1, NQ, n_kv, topk,
-                                       block_size, num_blocks, max_blocks_per_seq, softmax_scale, s2_tile, status,
-                                       stream);
-    return mla_launch<kFmtKvcE8m0>("pa_mla_sparse_decode_kvc", q_nope, q_rope, kv_cache, row_bytes, topk_indices,
-                                   block_table, kv_act_seqs, out, B, S1, NQ, n_kv, topk, block_size, num_blocks,
-                                   max_blocks_per_seq, softmax_scale, s2_tile, status, stream);
+                                       block_stride, topk_indices, block_table, kv_act_seqs, out, B, S1, NQ,
+                                       n_kv, topk, block_size, num_blocks, max_blocks_per_seq, softmax_scale,
+                                       s2_tile, status, stream);
+    return mla_launch<kFmtKvcE8m0>("pa_mla_sparse_decode_kvc", q_nope, q_rope, kv_cache, row_bytes, block_stride,
+                                   topk_indices, block_table, kv_act_seqs, out, B, S1, NQ, n_kv, topk, block_size,
+                                   num_blocks, max_blocks_per_seq, softmax_scale, s2_tile, status, stream);
 }

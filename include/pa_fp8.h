@@ -419,17 +419,22 @@ PA_API pa_status pa_mla_sparse_decode(const void* q_nope, const void* q_rope,
  * is the same as pa_mla_sparse_decode.
  *
  * Arguments: as pa_mla_sparse_decode, with
- *   kv_cache      bytes [num_blocks*block_size, row_bytes], blocks contiguous
- *                 (the epilog's block_stride = block_size * head_dim); row_bytes
- *                 = the epilog's head_dim, >= 656 and a multiple of 16 (mode 1
+ *   kv_cache      bytes: num_blocks blocks of block_stride bytes, row r of a
+ *                 block at r * row_bytes (the epilog's cache, block_stride and
+ *                 head_dim); position idx of sequence b is row idx % block_size
+ *                 of block block_table[b][idx / block_size].
+ *   row_bytes     the epilog's head_dim, >= 656 and a multiple of 16 (mode 1
  *                 rows of the minimum 648 bytes do not qualify: pad to 656).
+ *   block_stride  >= block_size * row_bytes and a multiple of 16; 0 means
+ *                 block_size * row_bytes (contiguous blocks).
  *   quant_mode    0 or 1 as given to the epilog; 2 (HiFloat8 rope, FP4 nope)
  *                 returns PA_ERR_UNSUPPORTED, anything else PA_ERR_INVALID.
  * Nothing is allocated; the call is asynchronous on `stream`.
  * ------------------------------------------------------------------------ */
 PA_API pa_status pa_mla_sparse_decode_kvc(const void* q_nope, const void* q_rope,
                                           const void* kv_cache, int64_t row_bytes,
-                                          int quant_mode, const int32_t* topk_indices,
+                                          int64_t block_stride, int quant_mode,
+                                          const int32_t* topk_indices,
                                           const int32_t* block_table,
                                           const int32_t* kv_act_seqs, void* out,
                                           int B, int S1, int NQ, int n_kv, int topk,

@@ -189,11 +189,12 @@ def test_mla_sparse_decode_kvc_rejects_bad_arguments(L):
     scale = ctypes.c_float(1.0 / 24.0)
 
     def call(**kw):
-        a = dict(qn=fake, qr=fake, cache=fake, row_bytes=672, mode=0, tk=fake, bt=fake, act=fake,
-                 out=fake, B=4, S1=2, NQ=128, n_kv=1, topk=2048, bs=128, nb=100, mb=512, s2=128,
-                 status=fake)
+        a = dict(qn=fake, qr=fake, cache=fake, row_bytes=672, stride=0, mode=0, tk=fake, bt=fake,
+                 act=fake, out=fake, B=4, S1=2, NQ=128, n_kv=1, topk=2048, bs=128, nb=100, mb=512,
+                 s2=128, status=fake)
         a.update(kw)
-        return f(a["qn"], a["qr"], a["cache"], ctypes.c_int64(a["row_bytes"]), a["mode"], a["tk"],
+        return f(a["qn"], a["qr"], a["cache"], ctypes.c_int64(a["row_bytes"]),
+                 ctypes.c_int64(a["stride"]), a["mode"], a["tk"],
                  a["bt"], a["act"], a["out"], a["B"], a["S1"], a["NQ"], a["n_kv"], a["topk"],
                  a["bs"], ctypes.c_int64(a["nb"]), a["mb"], scale, a["s2"], a["status"], None)
 
@@ -208,5 +209,9 @@ def test_mla_sparse_decode_kvc_rejects_bad_arguments(L):
     assert call(NQ=96) == 5
     assert call(s2=64) == 5
     assert call(qn=P(264)) == 2              # alignment
+    assert call(stride=128 * 672 - 16) == 2  # blocks overlap
+    assert b"block_stride" in L.pa_last_error()
+    assert call(stride=128 * 672 + 8) == 2   # not a multiple of 16
     assert call(B=0) == 0
     assert call(mode=1, B=0) == 0
+    assert call(B=0, stride=128 * 672 + 4096) == 0

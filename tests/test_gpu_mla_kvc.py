@@ -143,6 +143,31 @@ def test_mla_kvc_after_gpu_compress_epilog(pa, mode, round_scale):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
+def test_mla_kvc_strided_blocks(pa, mode):
+    """The epilog's cache with blocks 4 KB further apart than their rows need (block_stride
+    = block_size * head_dim + 4096): the GPU epilog writes it, the decode reads it, and the
+    output equals, bit for bit, the decode over the same rows in contiguous blocks, and the
+    oracle's within the criteria."""
+    case = small(B=2, S1=2, NQ=64, act=(700, 257), topk=384, seed=40 + mode, frac_invalid=0.05)
+    rows = case.rows_used()
+    x = torch.from_numpy(case.key_rows(rows)).to(torch.bfloat16).cuda()
+    slots = torch.from_numpy(rows.astype(np.int64)).cuda()
+    NB, BS, RB = case.num_blocks, case.BS, workloads.MLA_ROW_BYTES
+    pitch = BS * RB + 4096
+    big = torch.full((NB, pitch), 0x7F, dtype=torch.uint8, device="cuda")
+    strided = big.as_strided((NB, BS, 1, RB), (pitch, RB, RB, 1))
+    compact = torch.zeros((NB, BS, 1, RB), dtype=torch.uint8, device="cuda")
+    for c in (strided, compact):
+        pa.kv_compress_epilog(c, x, slots, quant_mode=mode, round_scale=True)
+    a = run_gpu(pa, case, strided, mode)
+    b = run_gpu(pa, case, compact, mode)
+    assert np.array_equal(a, b)
+    host = compact.cpu().numpy().reshape(NB * BS, RB)
+    _, ref = run_oracle(case, host, mode)
+    check_close(a, ref, abs_weighted(case, host, mode))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
 def test_mla_kvc_same_keys_as_the_page_format(pa, mode):
     """Page-format rows whose scales the KV compress row holds exactly (BF16 values, powers
     of two), moved byte by byte into the KV compress layout: the GPU gives the same output
