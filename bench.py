@@ -333,9 +333,26 @@ def reference_arm(args, rank, world):
     from concurrent.futures import ThreadPoolExecutor
     threads = host_threads()
     total_steps = args.steps + args.warmup
-    # about 150 s of oracle time on all cores over the whole run
-    budget = max(150.0 * threads / max(total_steps, 1), 1e-4)
-    rows, nbytes = oracle_sample(case, inp, budget, prt)
+    # about 150 s of wall time over the whole run: whole units in batch order
+    # while the busiest thread's estimated time per step stays within
+    # 150 s / steps (at least one unit)
+    wall = 150.0 / max(total_steps, 1)
+    G = case.group
+    load = [0.0] * threads
+    rows, nbytes = [], 0
+    for b in range(case.B):
+        a = int(case.act[b])
+        for n2 in range(case.NKV):
+            k = (len(rows) // G) % threads
+            t = prt * a * G
+            if rows and load[k] + t > wall:
+                break
+            load[k] += t
+            rows.extend(b * case.NQ + n2 * G + g for g in range(G))
+            nbytes += a * (2 * case.D + 4) + G * (case.D + 4) + case.D * 4 + G * case.D * 2
+        else:
+            continue
+        break
     chunks = deal_units(case, rows, threads)
     with ThreadPoolExecutor(max_workers=len(chunks)) as ex:
         def one_step():
