@@ -215,3 +215,43 @@ def test_mla_sparse_decode_kvc_rejects_bad_arguments(L):
     assert call(B=0) == 0
     assert call(mode=1, B=0) == 0
     assert call(B=0, stride=128 * 672 + 4096) == 0
+
+
+def _c_kind(param):
+    """The ctypes class a C parameter of the header needs."""
+    p = " ".join(param.split())
+    if "*" in p:
+        return "ptr"
+    base = p.rsplit(" ", 1)[0].replace("const ", "")
+    return {"int": "i32", "int32_t": "i32", "pa_status": "i32", "int64_t": "i64",
+            "size_t": "u64", "float": "f32"}[base]
+
+
+def _ctypes_kind(t):
+    if t is ctypes.c_void_p or t is ctypes.c_char_p or hasattr(t, "_type_") and \
+            isinstance(getattr(t, "_type_"), type):
+        return "ptr"
+    if t is ctypes.c_float:
+        return "f32"
+    if issubclass(t, ctypes._SimpleCData):
+        size, signed = ctypes.sizeof(t), t(-1).value == -1
+        return {(4, True): "i32", (8, True): "i64", (8, False): "u64"}[(size, signed)]
+    raise AssertionError(t)
+
+
+def test_binding_argtypes_match_the_header(L):
+    """Every entry point the Python binding declares to ctypes takes the
+    header's parameters in order, with the same widths (a mismatch would pass
+    garbage to the library without any error)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    checked = 0
+    for m in re.finditer(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(([^)]*)\)\s*;", text):
+        name, params = m.group(1), [p for p in m.group(2).split(",") if p.strip() != "void"]
+        argtypes = getattr(L, name).argtypes
+        if argtypes is None:          # not marshalled by the binding (called directly in tests)
+            continue
+        want = [_c_kind(p) for p in params]
+        got = [_ctypes_kind(t) for t in argtypes]
+        assert got == want, (name, got, want)
+        checked += 1
+    assert checked >= 11
