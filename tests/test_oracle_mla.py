@@ -433,3 +433,26 @@ def test_mla_kvc_reads_what_the_compress_epilog_wrote(mode, round_scale):
             ref = (w / w.sum()) @ k[:, :DN]
             worst = max(worst, float(np.abs(out32[t, h] - ref).max()))
     assert worst < 0.1, worst
+
+
+def test_mla_kvc_e8m0_extreme_exponents():
+    """E8M0 scale bytes at the ends of what the epilog writes: byte 0 is 2^-127 (an FP32
+    subnormal, kept, not flushed) and small bytes give subnormal products; one visible key
+    outputs its row dequantised with torch, bit for bit."""
+    case = small_case(act=(1, 1), S1=1, B=2, topk=8)
+    cache = case.cache(fmt=workloads.MLA_FORMAT_KVC_E8M0)
+    rows = [int(selected(case, t)[0]) for t in range(case.T)]
+    cache[rows[0], 640:648] = [0, 1, 2, 127, 0, 3, 1, 0]
+    cache[rows[1], 640:648] = [126, 127, 128, 130, 0, 0, 2, 1]
+    out = run_fmt(case, cache, workloads.MLA_FORMAT_KVC_E8M0, want_f32=False)
+    for t in range(case.T):
+        r = torch.from_numpy(cache[rows[t]:rows[t] + 1].copy())
+        codes = r[:, 2 * DR:2 * DR + DN].contiguous().view(torch.float8_e4m3fn).to(torch.float32)
+        sc = torch.tensor([np.ldexp(1.0, int(e) - 127) for e in cache[rows[t], 640:648]],
+                          dtype=torch.float64).to(torch.float32)
+        kn = (codes * sc.repeat_interleave(64)).to(torch.bfloat16)
+        want = kn[0].view(torch.int16).numpy().view(np.uint16)
+        if t == 0:
+            assert (want[:64] != 0).any() and (np.abs(kn[0, :64].float().numpy()) < 2.0 ** -126).any()
+        for h in range(case.NQ):
+            assert np.array_equal(out[t, h], want)
