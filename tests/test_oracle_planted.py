@@ -94,6 +94,9 @@ MUTANTS = [
      [("rope = kv;", "rope = kv + DN;")]),
     ("mla kvc: codes read from the row start", MLA_PINS,
      [("code = kv + 2 * DR;", "code = kv;")]),
+    ("mla kvc: E8M0 byte 0 read as a zero scale", MLA_PINS,
+     [("(float)ldexp(1.0, (int)kv[640 + c] - 127)",
+       "(kv[640 + c] ? (float)ldexp(1.0, (int)kv[640 + c] - 127) : 0.0f)")]),
 ]
 
 
