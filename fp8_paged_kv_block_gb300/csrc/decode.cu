@@ -21,27 +21,24 @@
 //  * Warp 8 (one thread) feeds the K ring: per 128-token block one 2-D TMA
 //    load (128 rows x 128 bytes, 128-byte swizzle); per unit the Q rows,
 //    q_scale and v_scale. Warp 9 (one thread) feeds the V ring the same way.
-//  * Warps 0-7 consume. Warp w owns tokens [w S2T/8, (w+1) S2T/8) of every
-//    tile (one block, or part of one). For those tokens it
-//      MM1  S[row][token] = Q_fp8 . K_fp8^T   warp-level mma.sync m16n8k32
-//           E4M3 x E4M3 -> F32, Q fragments held in registers for the unit,
-//           K fragments read with ldmatrix from the swizzled ring slot;
-//    scales by q_scale * k_scale, masks past kv_act_seqs, finds the tile's
-//    row maxima (in-thread, over the lane quad, then over the warps through
-//    shared memory), P = 2^(x - tile max), the row sums and the E4M3 codes
-//    P8 = 448 P, written as the MM2 operand; then one lane issues its
-//      MM2  O^T[chan][row] = V_blk^T (MN-major: the V ring slot)
-//                            x P8^T (K-major, 128-byte swizzle)
-//    on the tensor cores (tcgen05.mma kind::f8f6f4, accumulator in tensor
-//    memory, one accumulator per warp). A tcgen05.mma costs ~100 issue cycles
-//    whatever its N, so the group-sized MM1 (N = query rows) runs faster as
-//    warp MMAs next to the softmax; MM2 reads the V slot straight from the
-//    ring. The warps' accumulators are summed in a fixed order when a tile is
-//    folded into registers with the running-max rescale (double-buffered by
-//    tile parity), so results do not depend on the order MMAs complete in.
-//    Quantising against the tile's own maximum gives the same codes as
-//    quantising exp(S - running max) against its tile maximum (the ratio
-//    cancels the running max); the running max only weights whole tiles.
+//  * Warp 10 owns the tensor memory and issues MM1 from one thread
+//    (tcgen05.mma kind::f8f6f4, E4M3 x E4M3 -> F32, M = 128):
+//      MM1  S^T[token][row]   = K_blk (K-major, the ring slot as loaded)
+//                               x Q^T (K-major, 128-byte swizzled rows)
+//    S^T lives in tensor memory, up to 4 tiles ahead of the consumers.
+//  * Warps 0-7 consume: tcgen05.ld of S^T (a lane = a token, a column = a
+//    query row), scaling by q_scale * k_scale (each thread loads its token's
+//    key scales a tile ahead), masking past kv_act_seqs, the tile's row
+//    maxima (butterfly over lanes, then over warps through shared memory),
+//    P = 2^(x - tile max), the row sums, E4M3 P8 = 448 * P written as the
+//    MM2 operand; each warp then issues the MM2 k-step of its own tokens:
+//      MM2  O^T[chan][row]   += V_blk^T (MN-major: the V ring slot)
+//                               x P8^T (MN-major)
+//    O^T is double-buffered by tile parity and folded into registers with the
+//    running-max rescale while the next tile's maxima are found. Quantising
+//    against the tile's own maximum gives the same codes as quantising
+//    exp(S - running max) against its tile maximum (the ratio cancels the
+//    running max); the running max only weights whole tiles.
 //  * Masked tokens get S = -inf (selected, never multiplied) and P = 0; the
 //    V rows of a partial last block are zeroed in shared memory before MM2
 //    (a stale E4M3 NaN code times 0 is NaN).
@@ -59,19 +56,10 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBS = 128;
 constexpr int kNCW = 8;                      // consumer warps
-constexpr int kKProducerWarp = kNCW;        // K blocks and the per-unit header
+constexpr int kKProducerWarp = kNCW;        // K blocks, key scales, per-unit header
 constexpr int kVProducerWarp = kNCW + 1;    // V blocks
-// Three full warpgroups: the consumers' two and the producers' (warps 10 and
-// 11 only hand their registers over and exit), so that the register split
-// below is made per warpgroup.
-constexpr int kThreads = (kNCW + 4) * 32;
-// Registers per thread after the split: the launch gives every thread 168
-// (three warps share a sub-partition's register file); the producer
-// warpgroup gives back down to kProdRegs and the consumers take the rest:
-// 8 x kConsRegs + 4 x kProdRegs = 12 x 168.
-constexpr int kProdRegs = 72;
-constexpr int kConsRegs = 216;
-static_assert(kNCW * kConsRegs + 4 * kProdRegs <= (kThreads / 32) * 168, "register split over the launch budget");
+constexpr int kMmaWarp = kNCW + 2;          // tensor memory owner; issues MM1
+constexpr int kThreads = (kNCW + 3) * 32;
 constexpr int kKSlots = 4;                   // K ring (one s2 tile of 512); the V ring takes the other slots
 constexpr int kSlotBytes = kBS * kD;         // one 128-token block of one head
 constexpr int kMaxB = 1024;
@@ -90,56 +78,47 @@ __host__ __device__ constexpr uint32_t tmem_cols(int need)
     return c;
 }
 
-// How an s2 tile is shared by the consumer warps.
-template <int S2T>
-struct TileSplit {
-    static constexpr int NBT = S2T / kBS;                      // 128-token blocks per tile
-    static constexpr int TPW = S2T / kNCW;                     // tokens per consumer warp
-    static constexpr int NT = TPW / 8;                         // MM1 n-tiles (8 tokens) per warp
-    static constexpr bool PAIRS = TPW < 32;                    // two warps share one 32-token MM2 k-step
-    static constexpr int GT = PAIRS ? 32 : TPW;                // tokens per MM2 accumulator group
-    static constexpr int OCW = S2T / GT;                       // accumulator groups (MMA-issuing warps)
-    static constexpr int KW = kBS / TPW;                       // warps that read one block's K
-    static constexpr int VW = kBS / GT;                        // warps whose MMAs read one block's V
-    static constexpr int KSL = TPW >= 32 ? TPW / 32 : 1;       // key scales loaded per lane and tile
-    static constexpr int MMS = GT / 32;                        // MM2 k-steps per issuing warp
-    static_assert(TPW >= 16 && TPW <= kBS && TPW % 16 == 0, "tokens per warp");
-};
+// S^T buffers in tensor memory (MM1 may run that many tiles ahead of the
+// consumers): as many as fit next to O^T in the 512 columns, at most 4.
+__host__ __device__ constexpr int s_buffers(int sc, int nr)
+{
+    return (4 * sc + 2 * nr <= 512) ? 4 : ((3 * sc + 2 * nr <= 512) ? 3 : 2);
+}
 
 struct Pos {
     int b, i, t;
 };
 
-// NR: padded query rows per unit (16 or 32); S2T: s2 tile; NS: ring slots (as
-// many as fit): slots 0 .. NK-1 hold K blocks, the rest V blocks, each ring
-// with its own producer.
+// NR: padded query rows per unit (16 or 32, the MMA N); S2T: s2 tile; NS:
+// ring slots (as many as fit): slots 0 .. kKSlots-1 hold K blocks, the rest
+// V blocks, each ring with its own producer.
 template <int NR, int S2T, int NS>
 struct __align__(1024) DecodeSmemT {
     static constexpr int NSLOT = NS;
     alignas(1024) uint8_t ring[NS][kSlotBytes];
-    // P8 as the K-major MM2 operand, one 128-byte-swizzled atom per block:
-    // token t of block a, row r at a * NR * 128 + r * 128 + (((t / 16) ^ (r % 8)) * 16) + t % 16
+    // Q rows: bulk-copied as plain rows, then swizzled in place into the
+    // 128-byte-swizzled K-major operand layout
+    alignas(1024) uint8_t qb[2][NR][kD];
+    // P8^T, MN-major without swizzle: token t, row r at
+    // (t / 8) * 8 * NR + (r / 16) * 128 + (t % 8) * 16 + r % 16
     // (also the BF16 staging of a unit's output rows, NR x 128 x 2 bytes)
     alignas(1024) uint8_t pbuf[S2T * NR > NR * kD * 2 ? S2T * NR : NR * kD * 2];
-    alignas(16) uint8_t qb[2][NR][kD];    // the unit's Q rows (plain rows), by unit parity
+    // key scales of one tile's blocks, double-buffered by tile parity
     alignas(16) float vsc[2][kD];
     alignas(16) float qs[2][32];
-    alignas(16) float ks[kNCW][TileSplit<S2T>::TPW];   // key scales of each warp's tokens
-    alignas(16) float red[2][NR][kNCW];   // per-warp row maxima, double-buffered by tile
-    alignas(16) float redl[kNCW][32];     // per-warp row sums at unit end
-    alignas(16) float wst[kNCW][2][32];   // per-warp copies: [0] tile max, [1] q_scale or row sum
+    alignas(16) float red[2][32][kNCW];   // per-warp row maxima (row-major), double-buffered by tile
+    float redl[kNCW][32];       // per-warp row sums at unit end
+    alignas(16) float wst[kNCW][4][32];   // per-warp copies of row values
     alignas(16) float wfold[2][kNCW][2][32];   // per-warp fold weights c1, c2 by tile parity
     int scan[kThreads / 32];
     int bpre[kMaxB + 1];
     int slen[kMaxB];
-    // A slot's uses alternate between two full barriers (use u on bank u & 1,
-    // phase u / 2), so that a consumer waiting for a slot's second use within
-    // a tile cannot mistake the first use's phase for it: consumer warps wait
-    // for their own blocks in any order.
-    uint64_t full_bar[NS][2];
+    uint64_t full_bar[NS];
     uint64_t empty_bar[NS];
     uint64_t hdr_full[2];
     uint64_t hdr_empty[2];
+    uint64_t s_full[4];
+    uint64_t s_empty[4];
     uint64_t o_full;
     uint64_t done_bar;
     uint32_t tmem;
@@ -281,6 +260,34 @@ __device__ __forceinline__ void zero_rows(const DecodeParams& p, int b, int tid,
     for (int64_t k = tid; k < n16; k += nthreads) dst[k] = make_uint4(0, 0, 0, 0);
 }
 
+// Butterfly reduction over the 32 lanes of a warp of N per-lane values (one
+// per query row): on return lane L holds the reduction of row
+// (N == 16 ? L / 2 : L) over all lanes. `a` is clobbered.
+template <int N, bool kMax>
+__device__ __forceinline__ float lane_reduce(float (&a)[N], int lane)
+{
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        const int h = N >> (s + 1);
+        if (h == 0) break;
+        const int o = 16 >> s;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float keep = up ? a[i + h] : a[i];
+            const float send = up ? a[i] : a[i + h];
+            const float got = __shfl_xor_sync(0xffffffffu, send, o);
+            a[i] = kMax ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    float v = a[0];
+    if (N == 16) {
+        const float got = __shfl_xor_sync(0xffffffffu, v, 1);
+        v = kMax ? fmaxf(v, got) : v + got;
+    }
+    return v;
+}
+
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v)
 {
@@ -292,9 +299,40 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v)
     }
 }
 
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
+// Slot and phase parity of the j-th block (j < NBT) after (slot, ph) in a ring
+// of NSLOT; a ring that holds a tile wraps at most once.
+template <int NSLOT, int NBT>
+__device__ __forceinline__ int ring_slot(int slot, uint32_t ph, int j, uint32_t* par)
 {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+    if constexpr (NBT <= NSLOT) {
+        int s = slot + j;
+        *par = ph;
+        if (s >= NSLOT) {
+            s -= NSLOT;
+            *par ^= 1u;
+        }
+        return s;
+    } else {
+        const int k = slot + j;
+        *par = ph ^ static_cast<uint32_t>((k / NSLOT) & 1);
+        return k % NSLOT;
+    }
+}
+
+// Advance (slot, ph) by n <= NBT blocks in a ring of NSLOT.
+template <int NSLOT, int NBT>
+__device__ __forceinline__ void ring_advance(int& slot, uint32_t& ph, int n)
+{
+    slot += n;
+    if constexpr (NBT <= NSLOT) {
+        if (slot >= NSLOT) {
+            slot -= NSLOT;
+            ph ^= 1u;
+        }
+    } else {
+        ph ^= static_cast<uint32_t>((slot / NSLOT) & 1);
+        slot %= NSLOT;
+    }
 }
 
 template <int NR, int S2T>
@@ -302,20 +340,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
 {
-    using TS = TileSplit<S2T>;
-    constexpr int NBT = TS::NBT, TPW = TS::TPW, NT = TS::NT, GT = TS::GT, OCW = TS::OCW;
-    constexpr int KSL = TS::KSL, MMS = TS::MMS;
-    constexpr bool PAIRS = TS::PAIRS;
-    constexpr int MT = NR / 16;                  // MM1 m-tiles of 16 query rows
-    constexpr int HR = NR / 2;                   // O^T columns (query rows) per folding thread
-    constexpr uint32_t TCOLS = tmem_cols(2 * OCW * NR);   // two O^T buffers of OCW accumulators
+    constexpr int NBT = S2T / kBS;               // 128-token blocks (MMA M-blocks) per tile
+    constexpr int MBW = NBT >= 2 ? NBT / 2 : 1;  // blocks per consumer warp
+    constexpr int SC = NBT * NR;                 // tensor-memory columns of one S^T buffer
+    constexpr int NSB = s_buffers(SC, NR);       // S^T buffers
+    constexpr int OCOL = NSB * SC;               // first column of O^T (two buffers of NR columns)
+    constexpr uint32_t TCOLS = tmem_cols(NSB * SC + 2 * NR);
+    constexpr int HR = NR / 2;                   // O^T columns (query rows) per consumer warp
     constexpr int TC = S2T + kC0;
     constexpr int NSLOT = DecodeSmem<NR, S2T>::NSLOT;
-    // K ring of kKSlots (one tile up to s2 tile 512), the V ring the rest. A
-    // ring slot is used at most twice within one tile (two full-barrier banks)
-    constexpr int NK = kKSlots, NV = NSLOT - NK;
-    static_assert(NBT <= 2 * NK && NBT <= 2 * NV, "a ring slot would be used more than twice in a tile");
-    static_assert(2 * OCW * NR <= 512, "tensor memory columns");
+    // K ring: one tile up to s2 tile 512; with longer tiles the V ring takes a
+    // whole tile (MM2 needs every block of the tile) and K the rest
+    constexpr int NK = NBT <= kKSlots ? kKSlots : NSLOT - NBT, NV = NSLOT - NK;
+    static_assert(NV >= NBT, "the V ring must hold one tile");
+    static_assert(NK >= 1, "no K ring slot left");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -329,18 +367,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < NSLOT; ++i) {
-            mbar_init(&sm.full_bar[i][0], 1);
-            mbar_init(&sm.full_bar[i][1], 1);
-            // K blocks are released by every consumer warp that reads them,
-            // V blocks by the MM2 commits of the warps whose MMAs read them
-            mbar_init(&sm.empty_bar[i], i < NK ? TS::KW : TS::VW);
+            mbar_init(&sm.full_bar[i], 1);
+            // the MMAs reading the slot completed: K blocks are read by the MM1
+            // thread, V blocks by one MMA of each of the 4 consumer warps that
+            // hold the block's tokens
+            mbar_init(&sm.empty_bar[i], i < NK ? 1 : 4);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.hdr_full[i], 2);           // byte-counted copies + the q_scale cp.async
-            mbar_init(&sm.hdr_empty[i], kNCW);       // every consumer warp at the unit's end
+            mbar_init(&sm.hdr_empty[i], 1 + kNCW);   // last MM1 of the unit + every consumer warp
         }
-        mbar_init(&sm.o_full, OCW);                  // every accumulator group's MM2 share
-        mbar_init(&sm.done_bar, kNCW);               // every consumer warp's last MMAs
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.s_empty[i], kNCW);
+        }
+        mbar_init(&sm.o_full, kNCW);                 // every consumer warp's MM2 share
+        mbar_init(&sm.done_bar, 1);
         sm.abort = 0;
         sm.k_tiles = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -427,9 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.owner[lane] = own;
     }
 
-    // tensor memory (the MM2 accumulators): allocated by consumer warp 0,
-    // address published in shared memory
-    if (warp == 0) tmem_alloc(&sm.tmem, TCOLS);
+    // tensor memory: allocated by the MMA warp, address published in shared memory
+    if (warp == kMmaWarp) tmem_alloc(&sm.tmem, TCOLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -437,21 +478,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Pos start = sm.range[0];
     const Pos end = sm.range[1];
 
-    if (warp >= kNCW) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        if (warp > kVProducerWarp) return;
+    if (warp == kKProducerWarp || warp == kVProducerWarp) {
         // ============================== producers ==============================
-        // The K producer fills the K ring (plus the per-unit header), the V
-        // producer the V ring; each runs ahead of the consumers as far as its
-        // own ring allows, so V tiles waiting for their P never hold back the
-        // next tile's K.
+        // The K producer fills the K ring (plus key scales and the per-unit
+        // header), the V producer the V ring; each runs ahead of the MMAs as
+        // far as its own ring allows, so V tiles waiting for their P never
+        // hold back the next tile's K.
         if (lane != 0) return;
         const bool isK = warp == kKProducerWarp;
         const CUtensorMap* tm = isK ? &tmK : &tmV;
         asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
         const uint64_t pol = l2_evict_first_policy();
         const int base = isK ? 0 : NK, nring = isK ? NK : NV;
-        int hcount = 0, fills = 0, tcount = 0;   // fills: blocks issued into this ring so far
+        int slot = 0;
+        uint32_t ph = 0;
+        int hcount = 0, fills = 0, tcount = 0;
         bool first = true;
         // block ids, loaded two tiles ahead of their use
         int id0[NBT], id1[NBT], id2[NBT];
@@ -503,8 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool need_hdr = isK && (first || t == 0);
             bool hdr_done = false;
             // MM1 needs the header; when the K ring is shorter than a tile the
-            // tile's later K blocks wait for the consumers to read its first
-            // ones, so the header goes out before them
+            // tile's later K blocks wait for MM1 on its first ones, so the
+            // header goes out before them
             if (need_hdr && NK < NBT) {
                 issue_header(b, n2, rc);
                 hdr_done = true;
@@ -544,14 +585,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < NBT; ++j) {
                 if (j >= nb) break;
-                // slot and use of this ring's fills-th block
-                const int u = isK ? fills / NK : fills / NV;
-                const int sl = base + (isK ? fills % NK : fills % NV);
+                const int sl = base + slot;
                 if (!waited && t * S2T + (j + 1) * kBS > len - p.S1) {
                     grid_dependency_wait();
                     waited = true;
                 }
-                mbar_wait(&sm.empty_bar[sl], (static_cast<uint32_t>(u) & 1u) ^ 1u, p.err, 4, &sm.abort);
+                mbar_wait(&sm.empty_bar[sl], ph ^ 1, p.err, 4, &sm.abort);
                 int blk = id0[j];
                 if (blk < 0 || blk >= p.num_blocks) blk = 0;
                 int x0, y0;
@@ -562,9 +601,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     x0 = 0;
                     y0 = (blk * p.NKV + n2) * kBS;
                 }
-                mbar_arrive_expect_tx(&sm.full_bar[sl][u & 1], kSlotBytes);
-                tma_load_2d(sm.ring[sl], tm, x0, y0, &sm.full_bar[sl][u & 1], pol);
+                mbar_arrive_expect_tx(&sm.full_bar[sl], kSlotBytes);
+                tma_load_2d(sm.ring[sl], tm, x0, y0, &sm.full_bar[sl], pol);
                 ++fills;
+                if (++slot == nring) {
+                    slot = 0;
+                    ph ^= 1;
+                }
             }
 #pragma unroll
             for (int j = 0; j < NBT; ++j) {
@@ -584,9 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // every copy issued here lands before the CTA may exit
         for (int s = 0; s < nring; ++s) {
-            const int n = fills / nring + (s < fills % nring ? 1 : 0);   // uses of slot s
-            for (int u = n - 2 < 0 ? 0 : n - 2; u < n; ++u)
-                mbar_wait_drain(&sm.full_bar[base + s][u & 1], static_cast<uint32_t>(u >> 1) & 1u, p.err, 1024);
+            const int n = fills / nring + (s < fills % nring ? 1 : 0);
+            if (n > 0) mbar_wait_drain(&sm.full_bar[base + s], static_cast<uint32_t>(n - 1) & 1u, p.err, 1024);
         }
         if (isK) {
             for (int h = 0; h < 2; ++h) {
@@ -597,102 +639,171 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
+    if (warp == kMmaWarp) {
+        // ============================== MM1 issue ==============================
+        // One thread issues MM1 as soon as a K block lands (up to NSB tiles
+        // ahead of the consumers). MM2 is issued by the consumer warps.
+        constexpr uint32_t kIdescS = idesc_e4m3(128, NR, 0, 0);   // K-major K and Q
+        constexpr bool mm1 = true;
+        int slot = 0;
+        uint32_t ph = 0;
+        int hcount = 0, tcount = 0, hs = 0;
+        bool first = true;
+        for (Pos x = start; !pos_eq(x, end);) {
+            const Pos nx = pos_next<S2T>(sm.slen, sm.bpre, p.B, x, W);
+            const int rc = x.i - head_of(p, x.i) * p.NRC, t = x.t;
+            const int len = sm.slen[x.b];
+            const int valid = min(S2T, len - t * S2T);
+            const int nb = (valid + kBS - 1) / kBS;
+            if (mm1) {
+                if (first || t == 0) {
+                    hs = hcount & 1;
+                    mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
+                    // Q rows into the 128-byte-swizzled K-major layout (16-byte
+                    // chunk c of row r goes to position c ^ (r % 8)); rows past
+                    // the chunk's end become zeros
+                    if (lane < NR) {
+                        const int nrows = min(p.R - rc * NR, NR);
+                        uint4* row = reinterpret_cast<uint4*>(&sm.qb[hs][lane][0]);
+                        uint4 v[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) v[c] = lane < nrows ? row[c] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) row[c ^ (lane & 7)] = v[c];
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    ++hcount;
+                }
+                const int sb = tcount % NSB;
+                if (lane == 0) {
+                    // MM1: S^T[token][row] for each block of the tile
+                    mbar_wait(&sm.s_empty[sb], ((tcount / NSB) & 1) ^ 1, p.err, 64, &sm.abort);
+                    tc_fence_after();
+                    const uint64_t qd = smem_desc(smem_u32(&sm.qb[hs][0][0]), 16, 1024, kSmem128BSwizzle);
+                    for (int j = 0; j < nb; ++j) {
+                        uint32_t par;
+                        const int s = ring_slot<NK, NBT>(slot, ph, j, &par);
+                        mbar_wait(&sm.full_bar[s], par, p.err, 16, &sm.abort);
+                        tc_fence_after();
+                        const uint64_t kd = smem_desc(smem_u32(sm.ring[s]), 16, 1024, kSmem128BSwizzle);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)   // 32 bytes of head dim per MMA
+                            umma_e4m3(tmem + sb * SC + j * NR, kd + 2 * kk, qd + 2 * kk, kIdescS, kk);
+                        umma_commit(&sm.empty_bar[s]);
+                    }
+                    umma_commit(&sm.s_full[sb]);
+                    if (t == tiles_of<S2T>(len) - 1 || pos_eq(nx, end)) umma_commit(&sm.hdr_empty[hs]);
+                }
+                __syncwarp();
+                ring_advance<NK, NBT>(slot, ph, nb);
+            }
+            first = false;
+            ++tcount;
+            x = nx;
+        }
+        // all MMAs complete before the tensor memory is released
+        if (lane == 0) {
+            umma_commit(&sm.done_bar);
+            mbar_wait_drain(&sm.done_bar, 0, p.err, 1024);
+        }
+        __syncwarp();
+        named_bar_sync(2, (kNCW + 1) * 32);
+        tc_fence_after();
+        tmem_dealloc(tmem, TCOLS);
+        return;
+    }
+
     // ================================ consumers ================================
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsRegs));
-    // MM1 / softmax: warp w owns tokens [w TPW, (w+1) TPW) of the tile: block
-    // wblk, tokens tok0 .. tok0 + TPW - 1 of it. In the m16n8 fragments, lane
-    // (g = lane / 4, t4 = lane % 4) holds rows g + 8 h + 16 m and tokens
-    // 8 j + 2 t4 + {0, 1} of n-tile j.
-    // Fold: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (channels) and
-    // O^T columns (query rows) hh * HR .. +HR - 1, hh = w / 4.
-    const int g = lane >> 2, t4 = lane & 3;
-    const int wblk = (warp * TPW) / kBS, tok0 = (warp * TPW) % kBS;
-    const int grp = PAIRS ? (warp >> 1) : warp;           // this warp's MM2 accumulator group
-    const bool issuer = !PAIRS || (warp & 1) == 0;        // the group's MMA-issuing warp
+    // Warp w reads tensor-memory lanes 32 (w % 4) .. +31: tokens of its blocks
+    // (S^T) and channels (O^T). Warps 0-3 take the first half of the tile's
+    // blocks and O^T rows 0 .. NR/2-1, warps 4-7 the rest.
     const int q4 = warp & 3, hh = warp >> 2;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    const int rho = NR == 16 ? (lane >> 1) : lane;   // query row whose reductions this lane holds
+    const bool rep = NR == 32 || (lane & 1) == 0;    // lane that publishes row rho
 
-    int kpos = 0, vpos = 0;     // blocks of this CTA's walk before the current tile (ring positions)
+    int vslot = 0;
+    uint32_t vph = 0;
     int hcount = 0, tcount = 0, hs = 0, nrows = 0;
     bool first = true;
-    uint32_t qa[MT][4][4];      // Q fragments of the unit (m-tile, k-step, register)
-    float Lp[MT][2];            // this thread's share of the row sums (running-max units)
+    float Lp[NR];               // this thread's share of the row sums (running-max units)
     float Oa[HR];               // O^T[32 q4 + lane][hh * HR + k], times 448
-    float Mref = -INFINITY;     // running max of row `lane` (lanes < NR; scaled log2 units)
+    float Mref = -INFINITY;     // running max of row rho (scaled log2 units)
 #pragma unroll
-    for (int m = 0; m < MT; ++m) Lp[m][0] = Lp[m][1] = 0.f;
+    for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
 #pragma unroll
     for (int k = 0; k < HR; ++k) Oa[k] = 0.f;
+    {
+        // O^T starts at zero: every MM2 MMA accumulates
+        const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) qa[m][kk][0] = qa[m][kk][1] = qa[m][kk][2] = qa[m][kk][3] = 0u;
-
-    // Tile k's O^T (buffer k & 1: the accumulators of the groups that had
-    // valid tokens, summed in group order) folded into Oa once its MM2 has
-    // completed, with the weights of tile k.
-    auto fold = [&](int k, int kvalid) {
+        for (int c = 0; c < HR; c += 8) {
+            tmem_st8(tl + OCOL + hh * HR + c, zero8);
+            tmem_st8(tl + OCOL + NR + hh * HR + c, zero8);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+    }
+    // Tile k's O^T (buffer k & 1) folded into Oa once its MM2 has completed,
+    // with the weights of tile k, then zeroed for tile k + 2.
+    auto fold = [&](int k) {
         mbar_wait(&sm.o_full, k & 1, p.err, 512, &sm.abort);
         tc_fence_after();
-        const int nact = min(OCW, (kvalid + GT - 1) / GT);
-        constexpr int FC = HR == 8 ? 4 : 2;   // accumulators read per batch
-        float acc[HR];
-#pragma unroll
-        for (int c = 0; c < HR; ++c) acc[c] = 0.f;
-        const uint32_t cb = tl + static_cast<uint32_t>((k & 1) * OCW * NR + hh * HR);
-#pragma unroll
-        for (int a0 = 0; a0 < OCW; a0 += FC) {
-            if (a0 >= nact) break;
-            float ot[FC][HR];
-#pragma unroll
-            for (int i = 0; i < FC; ++i)
-                if (a0 + i < nact) tmem_ld_cols<HR>(cb + static_cast<uint32_t>((a0 + i) * NR), ot[i]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < FC; ++i)
-                if (a0 + i < nact)
-#pragma unroll
-                    for (int c = 0; c < HR; ++c) acc[c] += ot[i][c];
-        }
+        float ot[HR];
+        tmem_ld_cols<HR>(tl + OCOL + (k & 1) * NR + hh * HR, ot);
+        tmem_wait_ld();
 #pragma unroll
         for (int c4 = 0; c4 < HR / 4; ++c4) {
             const float4 a4 = *reinterpret_cast<const float4*>(&sm.wfold[k & 1][warp][0][hh * HR + 4 * c4]);
             const float4 b4 = *reinterpret_cast<const float4*>(&sm.wfold[k & 1][warp][1][hh * HR + 4 * c4]);
-            Oa[4 * c4 + 0] = Oa[4 * c4 + 0] * a4.x + acc[4 * c4 + 0] * b4.x;
-            Oa[4 * c4 + 1] = Oa[4 * c4 + 1] * a4.y + acc[4 * c4 + 1] * b4.y;
-            Oa[4 * c4 + 2] = Oa[4 * c4 + 2] * a4.z + acc[4 * c4 + 2] * b4.z;
-            Oa[4 * c4 + 3] = Oa[4 * c4 + 3] * a4.w + acc[4 * c4 + 3] * b4.w;
+            Oa[4 * c4 + 0] = Oa[4 * c4 + 0] * a4.x + ot[4 * c4 + 0] * b4.x;
+            Oa[4 * c4 + 1] = Oa[4 * c4 + 1] * a4.y + ot[4 * c4 + 1] * b4.y;
+            Oa[4 * c4 + 2] = Oa[4 * c4 + 2] * a4.z + ot[4 * c4 + 2] * b4.z;
+            Oa[4 * c4 + 3] = Oa[4 * c4 + 3] * a4.w + ot[4 * c4 + 3] * b4.w;
         }
-        // buffer k & 1 is written again by tile k + 2's MMAs, which come
-        // after that tile's row-maximum barrier
+        // zeroed for the MMAs of tile k + 2, which come after that tile's
+        // row-maximum barrier
+        const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < HR; c += 8) tmem_st8(tl + OCOL + (k & 1) * NR + hh * HR + c, zero8);
+        tmem_wait_st();
         tc_fence_before();
     };
-    int pend = -1, pvalid = 0;   // tile whose O^T has not been folded yet, and its valid tokens
-    // Key scales of this warp's tokens, read from global memory through L2
-    // one tile ahead of their use (the block id one tile before that), staged
-    // in shared memory per tile; no copy engine is used.
-    auto tile_id = [&](const Pos& y) {
+    int pend = -1;   // tile whose O^T has not been folded yet
+    // Key scales of this thread's token (lane) in each of its blocks, read
+    // from global memory through L2 one tile ahead of their use (the block
+    // ids one tile before that), so that the loads are in flight while the
+    // current tile is processed and no copy engine or shared memory is used.
+    const int ktok = 32 * q4 + lane;
+    auto tile_ids = [&](const Pos& y, int (&ids)[MBW]) {
         const int nby = min(NBT, (sm.slen[y.b] - y.t * S2T + kBS - 1) / kBS);   // y.b < B here
-        return wblk < nby ? __ldg(p.block_table + static_cast<int64_t>(y.b) * p.max_blocks + y.t * NBT + wblk)
-                          : -1;
-    };
-    auto tile_ks = [&](const Pos& y, int id, float (&dst)[KSL]) {
-        const int n2y = head_of(p, y.i);
-        int blk = id;
-        if (blk < 0 || blk >= p.num_blocks) blk = 0;
+        const int* row = p.block_table + static_cast<int64_t>(y.b) * p.max_blocks + y.t * NBT;
 #pragma unroll
-        for (int q = 0; q < KSL; ++q) {
-            const int tok = tok0 + min(lane + 32 * q, TPW - 1);
-            const int64_t idx = p.layout == PA_LAYOUT_BSND
-                                    ? (static_cast<int64_t>(blk) * kBS + tok) * p.NKV + n2y
-                                    : (static_cast<int64_t>(blk) * p.NKV + n2y) * kBS + tok;
-            dst[q] = __ldcg(p.k_scale + idx);
+        for (int jj = 0; jj < MBW; ++jj) {
+            const int mb = hh * MBW + jj;
+            ids[jj] = mb < nby ? __ldg(row + mb) : -1;
         }
     };
-    float ksn[KSL];   // key scales of the next tile
-    int idn = -1;     // block id of the tile after it
+    auto tile_ks = [&](const Pos& y, const int (&ids)[MBW], float (&dst)[MBW]) {
+        const int n2y = head_of(p, y.i);
 #pragma unroll
-    for (int q = 0; q < KSL; ++q) ksn[q] = 0.f;
+        for (int jj = 0; jj < MBW; ++jj) {
+            int blk = ids[jj];
+            if (blk < 0 || blk >= p.num_blocks) blk = 0;
+            const int64_t idx = p.layout == PA_LAYOUT_BSND
+                                    ? (static_cast<int64_t>(blk) * kBS + ktok) * p.NKV + n2y
+                                    : (static_cast<int64_t>(blk) * p.NKV + n2y) * kBS + ktok;
+            dst[jj] = __ldcg(p.k_scale + idx);
+        }
+    };
+    float ksn[MBW];   // key scales of the next tile
+    int idn[MBW];     // block ids of the tile after it
+#pragma unroll
+    for (int jj = 0; jj < MBW; ++jj) {
+        ksn[jj] = 0.f;
+        idn[jj] = -1;
+    }
     // The walk is carried in registers: the current tile, the next two, and
     // their sequence lengths (a tile's successor needs only its own length).
     auto advance = [&](Pos y, int leny, int& lnext) {
@@ -717,18 +828,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!pos_eq(x1, end)) x2 = advance(x1, len1, len2);
     // block ids (not written by the preceding kernel) before its end; key
     // scales, out and the workspace only after it
-    int id0 = -1;
+    int id0[MBW];
     if (!pos_eq(start, end)) {
-        id0 = tile_id(start);
-        if (!pos_eq(x1, end)) idn = tile_id(x1);
+        tile_ids(start, id0);
+        if (!pos_eq(x1, end)) tile_ids(x1, idn);
     }
     grid_dependency_wait();
     if (!pos_eq(start, end)) tile_ks(start, id0, ksn);
     // sequences of length 0 produce zero rows (no tile ever covers them)
     for (int b = cta; b < p.B; b += p.grid)
         if (sm.slen[b] == 0) zero_rows(p, b, tid, kNCW * 32);
-
-    constexpr uint32_t kIdescO = idesc_e4m3(128, NR, 1, 0);   // MN-major V^T, K-major P8^T
 
     for (Pos x = start; !pos_eq(x, end);) {
         const Pos nx = x1;
@@ -743,24 +852,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 0 && lane < NR) sm.orow[hcount & 1][lane] = q_row(p, b, n2, rc * NR + lane);
             // this warp's copy of q_scale * softmax_scale * log2(e) per row (0
             // past the chunk's rows); the slot holds the row sums at unit end
-            if (lane < NR) sm.wst[warp][1][lane] = lane < nrows ? sm.qs[hs][lane] * p.sscale : 0.f;
-            // Q fragments (rows past the chunk's end are zeros)
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                const int r0 = 16 * m + g, r1 = r0 + 8;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint8_t* a = &sm.qb[hs][r0][32 * kk + 4 * t4];
-                    const uint8_t* c = &sm.qb[hs][r1][32 * kk + 4 * t4];
-                    qa[m][kk][0] = r0 < nrows ? *reinterpret_cast<const uint32_t*>(a) : 0u;
-                    qa[m][kk][1] = r1 < nrows ? *reinterpret_cast<const uint32_t*>(c) : 0u;
-                    qa[m][kk][2] = r0 < nrows ? *reinterpret_cast<const uint32_t*>(a + 16) : 0u;
-                    qa[m][kk][3] = r1 < nrows ? *reinterpret_cast<const uint32_t*>(c + 16) : 0u;
-                }
-            }
+            if (lane < NR) sm.wst[warp][3][lane] = lane < nrows ? sm.qs[hs][lane] * p.sscale : 0.f;
             __syncwarp();
 #pragma unroll
-            for (int m = 0; m < MT; ++m) Lp[m][0] = Lp[m][1] = 0.f;
+            for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
 #pragma unroll
             for (int k = 0; k < HR; ++k) Oa[k] = 0.f;
             Mref = -INFINITY;
@@ -770,17 +865,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const int valid = min(S2T, len - t * S2T);
         const int nb = (valid + kBS - 1) / kBS;
-        const bool hasblk = wblk < nb;
-        const int wvalid = min(max(valid - warp * TPW, 0), TPW);   // this warp's valid tokens
-        const int gvalid = min(max(valid - grp * GT, 0), GT);      // its accumulator group's
-        // this tile's key scales to shared memory; the next tile's requested
+        const int sb = tcount % NSB;
+        float ksv[MBW];
 #pragma unroll
-        for (int q = 0; q < KSL; ++q)
-            if (lane + 32 * q < TPW) sm.ks[warp][lane + 32 * q] = ksn[q];
-        __syncwarp();
+        for (int jj = 0; jj < MBW; ++jj) ksv[jj] = ksn[jj];
         if (!pos_eq(nx, end)) {
             tile_ks(nx, idn, ksn);
-            if (!pos_eq(x2, end)) idn = tile_id(x2);
+            if (!pos_eq(x2, end)) tile_ids(x2, idn);
         }
         // the walk moves on by one tile
         lenx = len1;
@@ -788,200 +879,230 @@ __global__ void __launch_bounds__(kThreads, 1)
         len1 = len2;
         if (!pos_eq(x2, end)) x2 = advance(x2, len2, len2);
 
-        // ---- MM1: S = Q . K^T for this warp's tokens (mma.sync, K via ldmatrix) ----
-        float sc[MT][NT][4];
+        // ---- S^T of this warp's blocks and their key scales ----
+        // With 32 query rows and two blocks per warp, the scores of both blocks
+        // do not fit in registers next to the rest of the state (they spill):
+        // each block is read from tensor memory twice instead, once for the
+        // row maxima and once for P, and the S^T buffer is released after the
+        // second read.
+        constexpr bool kReload = NR == 32 && MBW > 1;
+        constexpr int SVB = kReload ? 1 : MBW;
+        mbar_wait(&sm.s_full[sb], (tcount / NSB) & 1, p.err, 256, &sm.abort);
+        tc_fence_after();
+        float sv[SVB][NR];
+        if constexpr (!kReload) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int j = 0; j < NT; ++j) sc[m][j][0] = sc[m][j][1] = sc[m][j][2] = sc[m][j][3] = 0.f;
-        if (hasblk) {
-            const int ku = (kpos + wblk) / NK, ksl = (kpos + wblk) % NK;
-            mbar_wait(&sm.full_bar[ksl][ku & 1], static_cast<uint32_t>(ku >> 1) & 1u, p.err, 16, &sm.abort);
-            if (wvalid > 0) {
-                // lane L addresses row L % 8 of matrix L / 8; the 16-byte chunk c
-                // of a token row sits at (c ^ row % 8) * 16 (128-byte swizzle)
-                const int r7 = lane & 7, qm = lane >> 3;
-                const uint32_t kb = smem_u32(sm.ring[ksl]) + static_cast<uint32_t>((tok0 + r7) * 128);
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    uint32_t kf[8];
-                    const uint32_t row = kb + static_cast<uint32_t>(j * 8 * 128);
-                    ldsm_x4(row + static_cast<uint32_t>((qm ^ r7) << 4), kf[0], kf[1], kf[2], kf[3]);
-                    ldsm_x4(row + static_cast<uint32_t>(((4 + qm) ^ r7) << 4), kf[4], kf[5], kf[6], kf[7]);
-#pragma unroll
-                    for (int m = 0; m < MT; ++m)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) mma_e4m3(sc[m][j], qa[m][kk], kf[2 * kk], kf[2 * kk + 1]);
-                }
+            for (int jj = 0; jj < MBW; ++jj) {
+                const int mb = hh * MBW + jj;
+                if (mb < nb) tmem_ld_cols<NR>(tl + sb * SC + mb * NR, sv[jj]);
             }
+            tmem_wait_ld();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty_bar[ksl]);
+            if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
         }
 
         // ---- scores x = S * q_scale * scale * log2(e) * k_scale; tile row maxima ----
-        float mx[MT][2];
-        {
-            float qsc[MT][2];
+        float mloc[NR];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                qsc[m][0] = sm.wst[warp][1][16 * m + g];
-                qsc[m][1] = sm.wst[warp][1][16 * m + g + 8];
-                mx[m][0] = mx[m][1] = -INFINITY;
+        for (int r = 0; r < NR; ++r) mloc[r] = -INFINITY;
+        if constexpr (!kReload) {
+            float qsc[NR];
+#pragma unroll
+            for (int r4 = 0; r4 < NR / 4; ++r4) {
+                const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
+                qsc[4 * r4 + 0] = q4v.x;
+                qsc[4 * r4 + 1] = q4v.y;
+                qsc[4 * r4 + 2] = q4v.z;
+                qsc[4 * r4 + 3] = q4v.w;
             }
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const int tk = 8 * j + 2 * t4;
-                const float2 kv = *reinterpret_cast<const float2*>(&sm.ks[warp][tk]);
-                const bool ok0 = tk < wvalid, ok1 = tk + 1 < wvalid;
+            for (int jj = 0; jj < MBW; ++jj) {
+                const int mb = hh * MBW + jj;
+                if (mb < nb) {
+                    const bool ok = mb * kBS + 32 * q4 + lane < valid;
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    sc[m][j][0] = ok0 ? (sc[m][j][0] * qsc[m][0]) * kv.x : -INFINITY;
-                    sc[m][j][1] = ok1 ? (sc[m][j][1] * qsc[m][0]) * kv.y : -INFINITY;
-                    sc[m][j][2] = ok0 ? (sc[m][j][2] * qsc[m][1]) * kv.x : -INFINITY;
-                    sc[m][j][3] = ok1 ? (sc[m][j][3] * qsc[m][1]) * kv.y : -INFINITY;
-                    mx[m][0] = fmaxf(mx[m][0], fmaxf(sc[m][j][0], sc[m][j][1]));
-                    mx[m][1] = fmaxf(mx[m][1], fmaxf(sc[m][j][2], sc[m][j][3]));
+                    for (int r = 0; r < NR; ++r) {
+                        const float xv = ok ? (sv[jj][r] * qsc[r]) * ksv[jj] : -INFINITY;
+                        sv[jj][r] = xv;
+                        mloc[r] = fmaxf(mloc[r], xv);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int jj = 0; jj < MBW; ++jj) {
+                const int mb = hh * MBW + jj;
+                if (mb < nb) {
+                    tmem_ld_cols<NR>(tl + sb * SC + mb * NR, sv[0]);
+                    tmem_wait_ld();
+                    const bool ok = mb * kBS + 32 * q4 + lane < valid;
+#pragma unroll
+                    for (int r4 = 0; r4 < NR / 4; ++r4) {
+                        const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
+                        const float qv[4] = {q4v.x, q4v.y, q4v.z, q4v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r = 4 * r4 + e;
+                            const float xv = ok ? (sv[0][r] * qv[e]) * ksv[jj] : -INFINITY;
+                            mloc[r] = fmaxf(mloc[r], xv);
+                        }
+                    }
                 }
             }
         }
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                mx[m][h] = fmaxf(mx[m][h], __shfl_xor_sync(0xffffffffu, mx[m][h], 1));
-                mx[m][h] = fmaxf(mx[m][h], __shfl_xor_sync(0xffffffffu, mx[m][h], 2));
-            }
+        const float wmax = lane_reduce<NR, true>(mloc, lane);
         const int rb = tcount & 1;
-        if (t4 == 0)
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                sm.red[rb][16 * m + g][warp] = mx[m][0];
-                sm.red[rb][16 * m + g + 8][warp] = mx[m][1];
-            }
+        if (rep) sm.red[rb][rho][warp] = wmax;
         named_bar_sync(1, kNCW * 32);
-        // lane r (< NR) combines row r's maxima over the warps, updates the
-        // running max and publishes this warp's copies of the tile max and the
-        // fold weights c1 = 2^(M_old - M_new), c2 = 2^(m_t - M_new)
-        if (lane < NR) {
-            const float4 a = *reinterpret_cast<const float4*>(&sm.red[rb][lane][0]);
-            const float4 c = *reinterpret_cast<const float4*>(&sm.red[rb][lane][4]);
-            const float mt =
-                fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(c.x, c.y), fmaxf(c.z, c.w)));
+        float mt;
+        {
+            const float4 a = *reinterpret_cast<const float4*>(&sm.red[rb][rho][0]);
+            const float4 c = *reinterpret_cast<const float4*>(&sm.red[rb][rho][4]);
+            mt = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(c.x, c.y), fmaxf(c.z, c.w)));
+        }
+        {
             const float Mn = fmaxf(Mref, mt);
-            sm.wst[warp][0][lane] = mt;
-            sm.wfold[tcount & 1][warp][0][lane] = ex2(Mref - Mn);
-            sm.wfold[tcount & 1][warp][1][lane] = ex2(mt - Mn);
+            const float c1 = ex2(Mref - Mn), c2 = ex2(mt - Mn);
             Mref = Mn;
+            if (rep) {
+                sm.wst[warp][0][rho] = mt;
+                sm.wfold[tcount & 1][warp][0][rho] = c1;
+                sm.wfold[tcount & 1][warp][1][rho] = c2;
+            }
         }
         __syncwarp();
         // the previous tile's MM2 ran while this tile's maxima were found
-        if (pend >= 0) fold(pend, pvalid);
+        if (pend >= 0) fold(pend);
 
         // ---- P = 2^(x - tile max), row sums, P8 = E4M3(448 P) as the MM2 operand ----
-        float ls[MT][2];
+        float ls[NR];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) ls[m][0] = ls[m][1] = 0.f;
-        if (gvalid > 0) {   // the group's MMA reads this warp's codes (zeros past the end)
-            const uint32_t pb = smem_u32(sm.pbuf) + static_cast<uint32_t>(wblk * NR * 128);
+        for (int r = 0; r < NR; ++r) ls[r] = 0.f;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                const float mt0 = sm.wst[warp][0][16 * m + g], mt1 = sm.wst[warp][0][16 * m + g + 8];
-                const uint32_t r0a = pb + static_cast<uint32_t>((16 * m + g) * 128);
+        for (int jj = 0; jj < MBW; ++jj) {
+            const int mb = hh * MBW + jj;
+            if (mb < nb) {
+                const int tok = mb * kBS + 32 * q4 + lane;
+                float* x = sv[kReload ? 0 : jj];
+                if constexpr (kReload) {
+                    // the same scores as in the first pass, bit for bit
+                    tmem_ld_cols<NR>(tl + sb * SC + mb * NR, x);
+                    tmem_wait_ld();
+                    const bool ok = tok < valid;
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const float e0 = ex2(sc[m][j][0] - mt0), e1 = ex2(sc[m][j][1] - mt0);
-                    const float e2 = ex2(sc[m][j][2] - mt1), e3 = ex2(sc[m][j][3] - mt1);
-                    ls[m][0] += e0 + e1;
-                    ls[m][1] += e2 + e3;
-                    const int tb = tok0 + 8 * j + 2 * t4;   // token within the block
-                    const uint32_t off = static_cast<uint32_t>((((tb >> 4) ^ g) << 4) | (tb & 15));
-                    st_shared_u16(r0a + off, e4m3x2(448.f * e0, 448.f * e1));
-                    st_shared_u16(r0a + 8 * 128 + off, e4m3x2(448.f * e2, 448.f * e3));
+                    for (int r4 = 0; r4 < NR / 4; ++r4) {
+                        const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
+                        x[4 * r4 + 0] = ok ? (x[4 * r4 + 0] * q4v.x) * ksv[jj] : -INFINITY;
+                        x[4 * r4 + 1] = ok ? (x[4 * r4 + 1] * q4v.y) * ksv[jj] : -INFINITY;
+                        x[4 * r4 + 2] = ok ? (x[4 * r4 + 2] * q4v.z) * ksv[jj] : -INFINITY;
+                        x[4 * r4 + 3] = ok ? (x[4 * r4 + 3] * q4v.w) * ksv[jj] : -INFINITY;
+                    }
                 }
+                uint32_t pk[NR / 4];
+#pragma unroll
+                for (int r4 = 0; r4 < NR / 4; ++r4) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(&sm.wst[warp][0][4 * r4]);
+                    const float e0 = ex2(x[4 * r4 + 0] - m4.x);
+                    const float e1 = ex2(x[4 * r4 + 1] - m4.y);
+                    const float e2 = ex2(x[4 * r4 + 2] - m4.z);
+                    const float e3 = ex2(x[4 * r4 + 3] - m4.w);
+                    ls[4 * r4 + 0] += e0;
+                    ls[4 * r4 + 1] += e1;
+                    ls[4 * r4 + 2] += e2;
+                    ls[4 * r4 + 3] += e3;
+                    pk[r4] = e4m3x4(448.f * e0, 448.f * e1, 448.f * e2, 448.f * e3);
+                }
+                uint8_t* dst = sm.pbuf + (tok >> 3) * (8 * NR) + (tok & 7) * 16;
+#pragma unroll
+                for (int a = 0; a < NR / 16; ++a)
+                    *reinterpret_cast<uint4*>(dst + a * 128) =
+                        make_uint4(pk[4 * a], pk[4 * a + 1], pk[4 * a + 2], pk[4 * a + 3]);
             }
         }
-        // ---- MM2: O^T[chan][row] = V^T[chan][tok] . P8^T[tok][row] over this
-        // group's tokens, into the group's own accumulator. V rows of tokens
+        if constexpr (kReload) {
+            // both reads of this tile's S^T are done: MM1 may reuse the buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
+        }
+        // ---- this warp's share of MM2: the k-step of its 32 tokens in each of
+        // its blocks, O^T[chan][row] += V^T[chan][tok] . P8^T[tok][row] (O^T
+        // was zeroed when the previous tile was folded). V rows of tokens
         // past the sequence end are zeroed first: P is 0 there, and a stale
         // NaN code times 0 would still be NaN. ----
-        if (hasblk) {
-            const int vu = (vpos + wblk) / NV, vsl = NK + (vpos + wblk) % NV;
-            const uint32_t vpar = static_cast<uint32_t>(vu >> 1) & 1u;
-            if (gvalid > 0 && wvalid < TPW) {
-                mbar_wait(&sm.full_bar[vsl][vu & 1], vpar, p.err, 32, &sm.abort);
-                for (int rr = wvalid + lane; rr < TPW; rr += 32) {
-                    uint4* vr = reinterpret_cast<uint4*>(sm.ring[vsl] + (tok0 + rr) * 128);
+        {
+            constexpr uint32_t kIdescO = idesc_e4m3(128, NR, 1, 1);   // MN-major V^T and P8^T
+            int vsl[MBW];
+            uint32_t vpar[MBW];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
+            for (int jj = 0; jj < MBW; ++jj) {
+                const int mb = hh * MBW + jj;
+                vsl[jj] = NK + ring_slot<NV, NBT>(vslot, vph, mb, &vpar[jj]);
+                if (mb < nb && (mb + 1) * kBS > valid) {
+                    mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort);
+                    const int row = 32 * q4 + lane;
+                    if (mb * kBS + row >= valid) {
+                        uint4* vr = reinterpret_cast<uint4*>(sm.ring[vsl[jj]] + row * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
+                    }
                 }
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if constexpr (PAIRS) named_bar_sync(3 + (warp >> 1), 64);   // both warps' P8 and zeroed rows
-            if (issuer && lane == 0) {
-                mbar_wait(&sm.full_bar[vsl][vu & 1], vpar, p.err, 32, &sm.abort);
-                if (gvalid > 0) {
-                    tc_fence_after();
-                    const uint64_t vd = smem_desc(smem_u32(sm.ring[vsl]), 1024, 1024, kSmem128BSwizzle);
-                    const uint64_t pd = smem_desc(smem_u32(sm.pbuf) + static_cast<uint32_t>(wblk * NR * 128), 16,
-                                                  1024, kSmem128BSwizzle);
-                    const uint32_t d = tmem + static_cast<uint32_t>(((tcount & 1) * OCW + grp) * NR);
-                    const int gt0 = (grp * GT) % kBS;   // the group's first token within the block
+            if (lane == 0) {
+                const uint64_t pd = smem_desc(smem_u32(sm.pbuf), 8 * NR, 128, kSmemNoSwizzle);
+                bool any = false;
 #pragma unroll
-                    for (int s = 0; s < MMS; ++s) {
-                        if (grp * GT + 32 * s >= valid) break;
-                        const int tk = gt0 + 32 * s;
-                        umma_e4m3(d, vd + static_cast<uint64_t>(tk * 8), pd + static_cast<uint64_t>(tk >> 4),
-                                  kIdescO, s > 0 ? 1u : 0u);
+                for (int jj = 0; jj < MBW; ++jj) {
+                    const int mb = hh * MBW + jj;
+                    if (mb < nb) {
+                        mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort);
+                        tc_fence_after();
+                        const uint64_t vd = smem_desc(smem_u32(sm.ring[vsl[jj]]), 1024, 1024, kSmem128BSwizzle);
+                        umma_e4m3(tmem + OCOL + (tcount & 1) * NR, vd + 256 * q4,
+                                  pd + static_cast<uint64_t>(((mb * kBS + 32 * q4) * NR) >> 4), kIdescO, 1);
+                        umma_commit(&sm.empty_bar[vsl[jj]]);
+                        any = true;
                     }
-                    umma_commit(&sm.empty_bar[vsl]);
-                    umma_commit(&sm.o_full);
-                } else {
-                    // nothing valid in this group: release the slot once its copy landed
-                    mbar_arrive(&sm.empty_bar[vsl]);
-                    mbar_arrive(&sm.o_full);
                 }
+                if (any)
+                    umma_commit(&sm.o_full);
+                else
+                    mbar_arrive(&sm.o_full);
             }
             __syncwarp();
-        } else if (issuer && lane == 0) {
-            mbar_arrive(&sm.o_full);
         }
 
         // ---- running sums; this tile's O^T is folded with the next tile ----
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = 16 * m + 8 * h + g;
-                Lp[m][h] = Lp[m][h] * sm.wfold[tcount & 1][warp][0][r] + ls[m][h] * sm.wfold[tcount & 1][warp][1][r];
-            }
+        for (int r4 = 0; r4 < NR / 4; ++r4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&sm.wfold[tcount & 1][warp][0][4 * r4]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&sm.wfold[tcount & 1][warp][1][4 * r4]);
+            Lp[4 * r4 + 0] = Lp[4 * r4 + 0] * a4.x + ls[4 * r4 + 0] * b4.x;
+            Lp[4 * r4 + 1] = Lp[4 * r4 + 1] * a4.y + ls[4 * r4 + 1] * b4.y;
+            Lp[4 * r4 + 2] = Lp[4 * r4 + 2] * a4.z + ls[4 * r4 + 2] * b4.z;
+            Lp[4 * r4 + 3] = Lp[4 * r4 + 3] * a4.w + ls[4 * r4 + 3] * b4.w;
+        }
         pend = tcount;
-        pvalid = valid;
-        kpos += nb;
-        vpos += nb;
+        ring_advance<NV, NBT>(vslot, vph, nb);
         ++tcount;
 
         if (t == T - 1 || pos_eq(nx, end)) {
             // ------------------------------ unit end ------------------------------
-            fold(pend, pvalid);
+            fold(pend);
             pend = -1;
-            // row sums: over the lane quad, then over the warps
+            float lsum[NR];
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float v = Lp[m][h];
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
-                    v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    if (t4 == 0) sm.redl[warp][16 * m + 8 * h + g] = v;
-                }
+            for (int r = 0; r < NR; ++r) lsum[r] = Lp[r];
+            const float wl = lane_reduce<NR, false>(lsum, lane);
+            if (rep) sm.redl[warp][rho] = wl;
             named_bar_sync(1, kNCW * 32);
             float L = 0.f;
-            if (lane < NR) {
 #pragma unroll
-                for (int w = 0; w < kNCW; ++w) L += sm.redl[w][lane];
-                sm.wst[warp][1][lane] = L;
-            }
+            for (int w = 0; w < kNCW; ++w) L += sm.redl[w][rho];
+            if (rep) sm.wst[warp][3][rho] = L;
             __syncwarp();
             const int ch = 32 * q4 + lane;
             const float vs = sm.vsc[hs][ch] * (1.0f / 448.0f);
@@ -996,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < HR; ++k) {
                     const int rr = hh * HR + k;
-                    stage[rr * kD + ch] = __float2bfloat16_rn(Oa[k] * vs * (1.0f / sm.wst[warp][1][rr]));
+                    stage[rr * kD + ch] = __float2bfloat16_rn(Oa[k] * vs * (1.0f / sm.wst[warp][3][rr]));
                 }
                 named_bar_sync(1, kNCW * 32);
                 const int64_t* orow = sm.orow[(hcount - 1) & 1];
@@ -1017,9 +1138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* part = p.part + (u + cta) * kPartFloats;
 #pragma unroll
                 for (int k = 0; k < HR; ++k) part[(hh * HR + k) * kD + ch] = Oa[k] * vs;
-                if (warp == 0 && lane < NR) {
-                    part[32 * kD + lane] = Mref;
-                    part[32 * kD + 32 + lane] = L;
+                if (warp == 0 && rep) {
+                    part[32 * kD + rho] = Mref;
+                    part[32 * kD + 32 + rho] = L;
                 }
             };
             if (cf != cl && !merger) write_part();
@@ -1035,11 +1156,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (orow >= nrows) continue;
                     // one pass over the parts, four at a time with every load
                     // issued first, rescaling to the running maximum
-                    float mxv = -INFINITY, lsm = 0.f;
+                    float mx = -INFINITY, lsm = 0.f;
                     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                     int kfirst = 0;
                     if (own != nullptr) {
-                        mxv = own[32 * kD + orow];
+                        mx = own[32 * kD + orow];
                         lsm = own[32 * kD + 32 + orow];
                         const float4 a = *reinterpret_cast<const float4*>(own + orow * kD + d0);
                         const float4 c = *reinterpret_cast<const float4*>(own + orow * kD + d0 + 4);
@@ -1065,25 +1186,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 ob[q] = oa[q];
                             }
                         }
-                        const float mn = fmaxf(fmaxf(mxv, fmaxf(mk[0], mk[1])), fmaxf(mk[2], mk[3]));
-                        const float c = ex2(mxv - mn);
+                        const float mn = fmaxf(fmaxf(mx, fmaxf(mk[0], mk[1])), fmaxf(mk[2], mk[3]));
+                        const float c = ex2(mx - mn);
                         lsm *= c;
 #pragma unroll
                         for (int e = 0; e < 8; ++e) acc[e] *= c;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const float scq = ex2(mk[q] - mn);
-                            lsm += lk[q] * scq;
-                            acc[0] += oa[q].x * scq;
-                            acc[1] += oa[q].y * scq;
-                            acc[2] += oa[q].z * scq;
-                            acc[3] += oa[q].w * scq;
-                            acc[4] += ob[q].x * scq;
-                            acc[5] += ob[q].y * scq;
-                            acc[6] += ob[q].z * scq;
-                            acc[7] += ob[q].w * scq;
+                            const float sc = ex2(mk[q] - mn);
+                            lsm += lk[q] * sc;
+                            acc[0] += oa[q].x * sc;
+                            acc[1] += oa[q].y * sc;
+                            acc[2] += oa[q].z * sc;
+                            acc[3] += oa[q].w * sc;
+                            acc[4] += ob[q].x * sc;
+                            acc[5] += ob[q].y * sc;
+                            acc[6] += ob[q].z * sc;
+                            acc[7] += ob[q].w * sc;
                         }
-                        mxv = mn;
+                        mx = mn;
                     }
                     uint4 o;
                     o.x = pack_bf16x2(__fdiv_rn(acc[0], lsm), __fdiv_rn(acc[1], lsm));
@@ -1125,9 +1246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float* own = reinterpret_cast<float*>(sm.ring[0]);
 #pragma unroll
                         for (int k = 0; k < HR; ++k) own[(hh * HR + k) * kD + ch] = Oa[k] * vs;
-                        if (warp == 0 && lane < NR) {
-                            own[32 * kD + lane] = Mref;
-                            own[32 * kD + 32 + lane] = L;
+                        if (warp == 0 && rep) {
+                            own[32 * kD + rho] = Mref;
+                            own[32 * kD + 32 + rho] = L;
                         }
                         named_bar_sync(1, kNCW * 32);
                         merge(own);
@@ -1157,19 +1278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         x = nx;
     }
-    // every MMA issued by this warp has completed before the tensor memory is
-    // released (normally already true: each unit end folds its last tile)
-    if (lane == 0) {
-        umma_commit(&sm.done_bar);
-        mbar_wait_drain(&sm.done_bar, 0, p.err, 1024);
-    }
-    __syncwarp();
     tc_fence_before();
-    named_bar_sync(1, kNCW * 32);
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, TCOLS);
+    named_bar_sync(2, (kNCW + 1) * 32);
 }
-
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -1234,8 +1345,8 @@ pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_confi
     pl->G = NQ / NKV;
     pl->R = S1 * pl->G;
     pl->NR = pl->R <= 16 ? 16 : 32;
-    // 1024-token tiles: each consumer warp holds the scores of 128 tokens for
-    // every query row of the unit in registers; 16 rows fit, 32 do not
+    // 1024-token tiles: three S^T buffers of 8 x 16 columns fit the tensor
+    // memory next to O^T, 8 x 32 do not
     PA_REQUIRE(pl->S2T < 1024 || pl->NR == 16, PA_ERR_UNSUPPORTED,
                "pa_fp8_decode: s2_tile 1024 needs at most 16 query rows per kv head (S1 x group = %d)", pl->R);
     pl->NRC = (pl->R + pl->NR - 1) / pl->NR;
@@ -1256,19 +1367,11 @@ pa_status launch(const CUtensorMap& tk, const CUtensorMap& tv,
     const size_t smem = sizeof(DecodeSmem<NR, S2T>) + 1024;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
-    static int nregs = 0;
     std::call_once(once, [&] {
         attr = cudaFuncSetAttribute(decode_kernel<NR, S2T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem));
-        cudaFuncAttributes fa;
-        if (attr == cudaSuccess) attr = cudaFuncGetAttributes(&fa, decode_kernel<NR, S2T>);
-        if (attr == cudaSuccess) nregs = fa.numRegs;
     });
-    PA_REQUIRE(attr == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode: kernel attributes: %s", cudaGetErrorString(attr));
-    // The consumers' setmaxnreg.inc takes registers the producers gave back;
-    // it could only wait forever if the launch held fewer than the split needs.
-    PA_REQUIRE(nregs * (kThreads / 32) >= kNCW * kConsRegs + 4 * kProdRegs, PA_ERR_CUDA,
-               "pa_fp8_decode: kernel built with %d registers per thread, below the register split", nregs);
+    PA_REQUIRE(attr == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode: smem attribute: %s", cudaGetErrorString(attr));
     if (prm.overlap) {
         cudaLaunchConfig_t lc = {};
         lc.gridDim = dim3(static_cast<unsigned>(prm.grid));
@@ -1288,15 +1391,15 @@ pa_status launch(const CUtensorMap& tk, const CUtensorMap& tv,
     return check_launch("pa_fp8_decode");
 }
 
-// Bulk-copy / TMA destinations must be 16-byte aligned; the 128-byte-swizzled
-// K/V tiles and the P8 operand sit on 1024-byte boundaries (the swizzle atom
-// the ldmatrix addressing and the MMA descriptors assume).
+// Bulk-copy / TMA destinations must be 16-byte aligned (128 for the tensor
+// loads of key scales); the 128-byte-swizzled K/V tiles and the Q operand sit
+// on 1024-byte boundaries (the swizzle atom the MMA descriptors assume).
 template <int NR, int S2T>
 struct SmemLayoutChecks {
     using S = DecodeSmem<NR, S2T>;
     static_assert(offsetof(S, ring) % 1024 == 0, "ring alignment");
-    static_assert(offsetof(S, qb) % 16 == 0, "Q rows alignment");
-    static_assert(offsetof(S, pbuf) % 1024 == 0, "P operand alignment");
+    static_assert(offsetof(S, qb) % 1024 == 0, "Q operand alignment");
+    static_assert(offsetof(S, pbuf) % 128 == 0, "P operand alignment");
     static_assert(offsetof(S, vsc) % 16 == 0, "vsc alignment");
     static_assert(offsetof(S, wst) % 16 == 0, "wst alignment");
     static_assert(sizeof(S) + 1024 <= 232448, "decode shared memory over budget");
