@@ -50,7 +50,8 @@ class PaError(RuntimeError):
 
 class pa_decode_config(ctypes.Structure):
     _fields_ = [("s2_tile", ctypes.c_int), ("num_ctas", ctypes.c_int),
-                ("overlap_prologue", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+                ("overlap_prologue", ctypes.c_int), ("merge_wait_ns", ctypes.c_int),
+                ("wait_limit_ns", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 def build(force: bool = False) -> str:
@@ -160,14 +161,16 @@ def _in_dtype(t):
 _configs = {}
 
 
-def _config(s2_tile: int, num_ctas: int, overlap_prologue=0):
-    key = (s2_tile, num_ctas, int(overlap_prologue))
+def _config(s2_tile: int, num_ctas: int, overlap_prologue=0, merge_wait_ns=0, wait_limit_ns=0):
+    key = (s2_tile, num_ctas, int(overlap_prologue), int(merge_wait_ns), int(wait_limit_ns))
     c = _configs.get(key)
     if c is None:
         c = pa_decode_config()
         c.s2_tile = s2_tile
         c.num_ctas = num_ctas
         c.overlap_prologue = int(overlap_prologue)
+        c.merge_wait_ns = int(merge_wait_ns)
+        c.wait_limit_ns = int(wait_limit_ns)
         _configs[key] = c
     return c
 
@@ -194,11 +197,16 @@ class DecodeWorkspace:
         """Non-zero if a kernel wait gave up (bitmask of the wait sites)."""
         return int(self.buf[:4].view(_torch().int32).item())
 
+    def clear_error_flags(self) -> None:
+        """Zero the error word (on the current stream); the kernel only ever
+        sets bits in it."""
+        self.buf[:4].zero_()
+
 
 def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs, out, *,
            S1: int = 1, layout: int = LAYOUT_BSND, s2_tile: int = 512, softmax_scale=None,
            workspace: DecodeWorkspace | None = None, num_ctas: int = 0, stream=None,
-           overlap_prologue: int = 0):
+           overlap_prologue: int = 0, merge_wait_ns: int = 0, wait_limit_ns: int = 0):
     """Paged FP8 decode attention (in place into ``out``).
 
     q [B*S1, NQ, D] E4M3 (uint8 or float8_e4m3fn), q_scale float32 [B*S1, NQ],
@@ -211,6 +219,8 @@ def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_s
     block_table, q, q_scale or v_scale); 2 also lets it load the cache blocks
     below each sequence's S1 newest positions early (that kernel must not
     write the cache there); see pa_decode_config.overlap_prologue.
+    merge_wait_ns, wait_limit_ns: test and diagnostic knobs, see
+    pa_decode_config.
     """
     torch = _torch()
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
@@ -232,7 +242,7 @@ def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_s
     if workspace is None:
         workspace = DecodeWorkspace(B, S1, NQ, NKV, D, s2_tile=s2_tile, num_ctas=num_ctas,
                                     device=q.device)
-    cfg = _config(s2_tile, num_ctas, overlap_prologue)
+    cfg = _config(s2_tile, num_ctas, overlap_prologue, merge_wait_ns, wait_limit_ns)
     st = lib().pa_fp8_decode(_ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
                              _ptr(v_scale), _ptr(block_table), _ptr(kv_act_seqs), _ptr(out),
                              B, S1, NQ, NKV, D, BS, NB, block_table.shape[1], layout,

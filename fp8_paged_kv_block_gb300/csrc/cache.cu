@@ -150,8 +150,13 @@ __global__ void scatter_bytes_kernel(const uint8_t* __restrict__ key, const uint
 // every code is computed before griddepcontrol.wait; only the cache stores
 // follow it. Launched with programmatic stream serialisation the kernel thus
 // runs beside the tail of the preceding kernel and writes once that kernel has
-// completed; launched plainly the wait returns at once. Blocks are two warps
-// (kAppendThreads) so that they fit on an SM beside a resident decode CTA.
+// completed; launched plainly the wait returns at once. Threads that store
+// nothing (a skipped slot, or past the last token) wait too before they exit:
+// the kernel must not complete before its predecessor, or a kernel chained
+// after it (a decode) would start writing while that predecessor still runs
+// -- with every slot skipped, no thread would otherwise wait at all.
+// Blocks are two warps (kAppendThreads) so that they fit on an SM beside a
+// resident decode CTA.
 constexpr int kAppendThreads = 64;
 
 template <typename T, int NC>
@@ -166,7 +171,10 @@ quant_scatter_kernel(const T* __restrict__ key, const T* __restrict__ value,
     grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t th = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (th >= ntok * H) return;
+    if (th >= ntok * H) {
+        grid_dependency_wait();
+        return;
+    }
     const int64_t i = th / H;
     const int j = static_cast<int>(th - i * H);
     const T* krow = key + th * D;
@@ -181,7 +189,10 @@ quant_scatter_kernel(const T* __restrict__ key, const T* __restrict__ value,
         }
     }
     const int64_t s = load_slot(slots, slot_type, i);
-    if (s < 0 || s >= num_blocks * BS) return;
+    if (s < 0 || s >= num_blocks * BS) {
+        grid_dependency_wait();
+        return;
+    }
     int tb = __ldg(token_batch + i);
     tb = tb < 0 ? 0 : (tb >= num_batches ? num_batches - 1 : tb);
     const float* vs = v_scale + (static_cast<int64_t>(tb) * H + j) * D;

@@ -93,7 +93,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait: gives up after ~2 s (or at once when another wait of the
+// Bounded wait: gives up after limit_ns (~2 s by default; or at once when another wait of the
 // same CTA already gave up, signalled through *abort), records error bit
 // `code` in *err and returns false. The caller carries on so that every
 // barrier is still reached and the kernel ends; the output is then garbage
@@ -101,7 +101,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code,
-                                          volatile int* abort)
+                                          volatile int* abort, uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -111,9 +111,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
         // without delaying the wake-up of short ones
         if (it > 64) __nanosleep(32);
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        // the clock is read every 64 polls (every poll under a short limit)
+        if ((it & 63u) == 0 || limit_ns < 1000000u) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 atomicOr(err, code);
                 return false;

@@ -121,6 +121,7 @@ struct __align__(1024) DecodeSmemT {
     uint64_t s_empty[4];
     uint64_t o_full;
     uint64_t done_bar;
+    uint64_t cdrain;            // every consumer warp's MMAs complete (before tensor memory is freed)
     uint32_t tmem;
     Pos range[2];               // this CTA's first tile and the tile after its last
     int owner[2];               // first CTA of the range's first unit, last CTA of its last unit
@@ -159,6 +160,8 @@ struct DecodeParams {
     int B, S1, NQ, NKV, G, R, NRC, max_blocks, layout, grid, maxlen;
     int overlap;   // programmatic stream serialisation: 0 off, 1 prologue, 2 also older cache blocks
     float sscale;  // softmax_scale * log2(e)
+    int64_t merge_wait_ns;   // the merging CTA's wait for the other parts (< 0: none)
+    uint64_t wait_ns;        // limit of the bounded waits
 };
 
 
@@ -383,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&sm.o_full, kNCW);                 // every consumer warp's MM2 share
         mbar_init(&sm.done_bar, 1);
+        mbar_init(&sm.cdrain, kNCW);
         sm.abort = 0;
         sm.k_tiles = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -507,9 +511,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < NBT; ++j) id0[j] = id1[j] = id2[j] = 0;
         // the unit's Q rows (one bulk copy per run of consecutive rows), its
         // q_scale values and its v_scale row
+        // After a wait that gave up nothing more is issued (no copy may land in
+        // a slot whose previous copy or MMA is still running, and no barrier
+        // may see more arrivals than its count); the loop ends.
+        bool stop = false;
         auto issue_header = [&](int b, int n2, int rc) {
             const int hs = hcount & 1;
-            mbar_wait(&sm.hdr_empty[hs], ((hcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort);
+            if (!mbar_wait(&sm.hdr_empty[hs], ((hcount >> 1) & 1) ^ 1, p.err, 2, &sm.abort, p.wait_ns)) {
+                stop = true;
+                return;
+            }
             const int r0 = rc * NR, r1 = min(p.R, r0 + NR);
             mbar_arrive_expect_tx(&sm.hdr_full[hs], static_cast<uint32_t>((r1 - r0) * kD + kD * 4));
             bulk_load_1d(&sm.vsc[hs][0], p.v_scale + (static_cast<int64_t>(b) * p.NKV + n2) * kD,
@@ -533,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             x1 = pos_next<S2T>(sm.slen, sm.bpre, p.B, start, W);
             load_ids(x1, id1);
         }
-        for (Pos x = start; !pos_eq(x, end);) {
+        for (Pos x = start; !pos_eq(x, end) && !stop;) {
             const Pos nx = x1;
             if (!pos_eq(nx, end)) {
                 x1 = pos_next<S2T>(sm.slen, sm.bpre, p.B, nx, W);
@@ -574,12 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     while (*kt <= tcount) {
                         __nanosleep(64);
                         if (*ab) break;
-                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        if (globaltimer_ns() - t0 > p.wait_ns) {
                             *ab = 1;
                             atomicOr(p.err, 2048);
                             break;
                         }
                     }
+                    if (*ab) break;
                 }
             }
 #pragma unroll
@@ -590,7 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     grid_dependency_wait();
                     waited = true;
                 }
-                mbar_wait(&sm.empty_bar[sl], ph ^ 1, p.err, 4, &sm.abort);
+                if (!mbar_wait(&sm.empty_bar[sl], ph ^ 1, p.err, 4, &sm.abort, p.wait_ns)) {
+                    stop = true;
+                    break;
+                }
                 int blk = id0[j];
                 if (blk < 0 || blk >= p.num_blocks) blk = 0;
                 int x0, y0;
@@ -658,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mm1) {
                 if (first || t == 0) {
                     hs = hcount & 1;
-                    mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
+                    mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort, p.wait_ns);
                     // Q rows into the 128-byte-swizzled K-major layout (16-byte
                     // chunk c of row r goes to position c ^ (r % 8)); rows past
                     // the chunk's end become zeros
@@ -676,15 +691,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++hcount;
                 }
                 const int sb = tcount % NSB;
-                if (lane == 0) {
-                    // MM1: S^T[token][row] for each block of the tile
-                    mbar_wait(&sm.s_empty[sb], ((tcount / NSB) & 1) ^ 1, p.err, 64, &sm.abort);
+                if (lane == 0 && !*reinterpret_cast<volatile int*>(&sm.abort)) {
+                    // MM1: S^T[token][row] for each block of the tile (nothing
+                    // is issued after a wait gave up)
+                    bool ok = mbar_wait(&sm.s_empty[sb], ((tcount / NSB) & 1) ^ 1, p.err, 64, &sm.abort, p.wait_ns);
                     tc_fence_after();
                     const uint64_t qd = smem_desc(smem_u32(&sm.qb[hs][0][0]), 16, 1024, kSmem128BSwizzle);
-                    for (int j = 0; j < nb; ++j) {
+                    for (int j = 0; j < nb && ok; ++j) {
                         uint32_t par;
                         const int s = ring_slot<NK, NBT>(slot, ph, j, &par);
-                        mbar_wait(&sm.full_bar[s], par, p.err, 16, &sm.abort);
+                        if (!mbar_wait(&sm.full_bar[s], par, p.err, 16, &sm.abort, p.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
                         tc_fence_after();
                         const uint64_t kd = smem_desc(smem_u32(sm.ring[s]), 16, 1024, kSmem128BSwizzle);
 #pragma unroll
@@ -692,10 +711,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             umma_e4m3(tmem + sb * SC + j * NR, kd + 2 * kk, qd + 2 * kk, kIdescS, kk);
                         umma_commit(&sm.empty_bar[s]);
                     }
-                    umma_commit(&sm.s_full[sb]);
-                    if (t == tiles_of<S2T>(len) - 1 || pos_eq(nx, end)) umma_commit(&sm.hdr_empty[hs]);
+                    if (ok) {
+                        umma_commit(&sm.s_full[sb]);
+                        if (t == tiles_of<S2T>(len) - 1 || pos_eq(nx, end)) umma_commit(&sm.hdr_empty[hs]);
+                    }
                 }
                 __syncwarp();
+                if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&sm.abort), 0)) break;
                 ring_advance<NK, NBT>(slot, ph, nb);
             }
             first = false;
@@ -748,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Tile k's O^T (buffer k & 1) folded into Oa once its MM2 has completed,
     // with the weights of tile k, then zeroed for tile k + 2.
     auto fold = [&](int k) {
-        mbar_wait(&sm.o_full, k & 1, p.err, 512, &sm.abort);
+        mbar_wait(&sm.o_full, k & 1, p.err, 512, &sm.abort, p.wait_ns);
         tc_fence_after();
         float ot[HR];
         tmem_ld_cols<HR>(tl + OCOL + (k & 1) * NR + hh * HR, ot);
@@ -847,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (first || t == 0) {
             hs = hcount & 1;
-            mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort);
+            mbar_wait(&sm.hdr_full[hs], (hcount >> 1) & 1, p.err, 8, &sm.abort, p.wait_ns);
             nrows = min(p.R - rc * NR, NR);
             if (warp == 0 && lane < NR) sm.orow[hcount & 1][lane] = q_row(p, b, n2, rc * NR + lane);
             // this warp's copy of q_scale * softmax_scale * log2(e) per row (0
@@ -887,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // second read.
         constexpr bool kReload = NR == 32 && MBW > 1;
         constexpr int SVB = kReload ? 1 : MBW;
-        mbar_wait(&sm.s_full[sb], (tcount / NSB) & 1, p.err, 256, &sm.abort);
+        mbar_wait(&sm.s_full[sb], (tcount / NSB) & 1, p.err, 256, &sm.abort, p.wait_ns);
         tc_fence_after();
         float sv[SVB][NR];
         if constexpr (!kReload) {
@@ -1040,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int mb = hh * MBW + jj;
                 vsl[jj] = NK + ring_slot<NV, NBT>(vslot, vph, mb, &vpar[jj]);
                 if (mb < nb && (mb + 1) * kBS > valid) {
-                    mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort);
+                    mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort, p.wait_ns);
                     const int row = 32 * q4 + lane;
                     if (mb * kBS + row >= valid) {
                         uint4* vr = reinterpret_cast<uint4*>(sm.ring[vsl[jj]] + row * 128);
@@ -1058,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int jj = 0; jj < MBW; ++jj) {
                     const int mb = hh * MBW + jj;
                     if (mb < nb) {
-                        mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort);
+                        mbar_wait(&sm.full_bar[vsl[jj]], vpar[jj], p.err, 32, &sm.abort, p.wait_ns);
                         tc_fence_after();
                         const uint64_t vd = smem_desc(smem_u32(sm.ring[vsl[jj]]), 1024, 1024, kSmem128BSwizzle);
                         umma_e4m3(tmem + OCOL + (tcount & 1) * NR, vd + 256 * q4,
@@ -1225,14 +1247,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int want = cl - cf;
                         int ok = 0;
                         const uint64_t t0 = globaltimer_ns();
-                        for (;;) {
+                        // (a negative wait hands the merge to the last part at once)
+                        for (; p.merge_wait_ns >= 0;) {
                             int v;
                             asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p.counters + u) : "memory");
                             if (v == want) {
                                 ok = 1;
                                 break;
                             }
-                            if (globaltimer_ns() - t0 > kMergeWaitNs) break;
+                            if (globaltimer_ns() - t0 > static_cast<uint64_t>(p.merge_wait_ns)) break;
                             __nanosleep(64);
                         }
                         if (ok) p.counters[u] = 0;
@@ -1278,6 +1301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         x = nx;
     }
+    // the MM2 MMAs this warp issued have completed (already true unless a wait
+    // gave up) before the tensor memory is released
+    if (lane == 0) {
+        umma_commit(&sm.cdrain);
+        mbar_wait_drain(&sm.cdrain, 0, p.err, 1024);
+    }
+    __syncwarp();
     tc_fence_before();
     named_bar_sync(2, (kNCW + 1) * 32);
 }
@@ -1342,6 +1372,8 @@ pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_confi
                "pa_fp8_decode: s2_tile %d (128, 256, 512 and 1024 are built)", pl->S2T);
     PA_REQUIRE(!cfg || (cfg->overlap_prologue >= 0 && cfg->overlap_prologue <= 2), PA_ERR_INVALID,
                "pa_fp8_decode: overlap_prologue %d (0, 1 or 2)", cfg ? cfg->overlap_prologue : 0);
+    PA_REQUIRE(!cfg || cfg->wait_limit_ns >= 0, PA_ERR_INVALID, "pa_fp8_decode: wait_limit_ns %d < 0",
+               cfg ? cfg->wait_limit_ns : 0);
     pl->G = NQ / NKV;
     pl->R = S1 * pl->G;
     pl->NR = pl->R <= 16 ? 16 : 32;
@@ -1495,6 +1527,9 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     prm.maxlen = static_cast<int>(maxlen);
     prm.sscale = softmax_scale * 1.4426950408889634f;
     prm.overlap = cfg ? cfg->overlap_prologue : 0;
+    prm.merge_wait_ns = (cfg && cfg->merge_wait_ns != 0) ? (cfg->merge_wait_ns < 0 ? -1 : cfg->merge_wait_ns)
+                                                        : static_cast<int64_t>(kMergeWaitNs);
+    prm.wait_ns = (cfg && cfg->wait_limit_ns > 0) ? static_cast<uint64_t>(cfg->wait_limit_ns) : kWaitLimitNs;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pl.NR == 16) {

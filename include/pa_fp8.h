@@ -109,7 +109,21 @@ typedef struct pa_decode_config {
                       append of a decode step does). Key scales, the newest
                       blocks, out and the workspace still wait for it.
                       Other values return PA_ERR_INVALID.                     */
-    int reserved[5];
+    int merge_wait_ns; /* test and diagnostic knob. A sequence whose tiles are
+                      spread over several CTAs is merged by its first CTA,
+                      which waits (bounded) for the other parts' count; when
+                      that wait runs out, the last part to arrive merges
+                      instead. 0: default wait (100 us); negative: no wait, so
+                      the last-arriving part always merges. Same result either
+                      way, up to FP32 rounding order.                         */
+    int wait_limit_ns; /* test and diagnostic knob: time limit of the kernel's
+                      bounded waits (a wait that runs out sets a bit of the
+                      workspace error word and the kernel finishes, its output
+                      undefined; the workspace stays usable). 0: default
+                      (about 2 s). Waits that keep issued copies and MMAs from
+                      outliving the CTA keep the default. Negative values
+                      return PA_ERR_INVALID.                                  */
+    int reserved[3];
 } pa_decode_config;
 
 /* Text of a status code (static storage). */

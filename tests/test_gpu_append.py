@@ -318,3 +318,61 @@ def test_kv_compress_epilog_bitexact(torch_cuda, d, mode, round_scale):
         got = base.cpu().numpy()
         bad = np.nonzero(got != ref)[0]
         assert bad.size == 0, (slot_dtype, bad[:10], got[bad[:10]], ref[bad[:10]])
+
+
+def test_step_chain_all_slots_skipped(torch_cuda):
+    """decode -> append -> decode -> append -> ... with programmatic
+    serialisation on every launch, where every slot of each append is -1 (a
+    legal input: skipped slots): no thread of the append stores anything, yet
+    the append must still complete only after the decode before it, so that
+    the next decode (same workspace, same output buffer) cannot start writing
+    while the previous one runs. Replayed back to back from a CUDA graph;
+    every output matches the oracle and the cache is unchanged."""
+    torch = torch_cuda
+    import fp8_paged_kv_block_gb300 as pa
+    case = workloads.custom("skipchain", 6, 1, 24, 2, [1, 127, 700, 1300, 2049, 3000], max_blocks=25)
+    inp = H.oracle_inputs(case)
+    dev = H.device_inputs(case)
+    ref = H.oracle_decode(case, inp)
+    knew, vnew, slot, _ = workloads.step_tokens(case)
+    c = dev["cache"]
+    snap = [t.clone() for t in (c.k_cache, c.v_cache, c.k_scale)]
+    ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile)
+    shape = (case.B * case.S1, case.NQ, case.D)
+    outs = [torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    kn, vn = knew.cuda(), vnew.cuda()
+    skipped = torch.full((case.B,), -1, dtype=torch.int32, device="cuda")
+    tb = torch.arange(case.B, dtype=torch.int32, device="cuda")
+
+    def chain():
+        for out in outs:
+            pa.decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale,
+                      dev["block_table"], dev["act"], out, S1=case.S1, layout=case.layout,
+                      s2_tile=case.s2_tile, softmax_scale=case.softmax_scale, workspace=ws,
+                      overlap_prologue=2)
+            pa.cache_quant_scatter(kn, vn, c.k_cache, c.v_cache, skipped, c.k_scale, c.v_scale, tb,
+                                   layout=case.layout, overlap_prologue=True)
+
+    def check():
+        torch.cuda.synchronize()
+        assert ws.error_flags() == 0
+        for out in outs:
+            H.compare_bf16(H.to_u16(out), ref)
+        for t, s in zip((c.k_cache, c.v_cache, c.k_scale), snap):
+            assert torch.equal(t, s)
+
+    chain()
+    check()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for out in outs:
+            out.fill_(float("nan"))
+        chain()
+    for _ in range(5):
+        g.replay()
+        check()

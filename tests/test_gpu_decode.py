@@ -308,3 +308,56 @@ def test_decode_long_context_s2_tile_1024_sampled(torch_cuda):
     rows = np.sort(rng.choice(case.B * case.NQ, 24, replace=False))
     batches = np.unique(rows // case.NQ)
     _run_case(case, rows=rows, batches=batches)
+
+
+# ---------------------------------------------------------------------------
+# Failure and fallback paths, forced through the test knobs of pa_decode_config
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("num_ctas", [3, 7, 152])
+def test_decode_last_arriver_merge_forced(torch_cuda, num_ctas):
+    """merge_wait_ns < 0: a split sequence's first CTA does not wait for the
+    other parts' count; it publishes its own part and the last part to arrive
+    merges. Same oracle parity as the designated merger, counters left zero."""
+    import fp8_paged_kv_block_gb300 as pa
+    case = small_case()
+    inp = H.oracle_inputs(case)
+    dev = H.device_inputs(case)
+    ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile, num_ctas=num_ctas)
+    ref = H.oracle_decode(case, inp)
+    for _ in range(2):
+        out = torch_cuda.empty((case.B * case.S1, case.NQ, case.D), dtype=torch_cuda.bfloat16, device="cuda")
+        c = dev["cache"]
+        pa.decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale, dev["block_table"],
+                  dev["act"], out, S1=case.S1, layout=case.layout, s2_tile=case.s2_tile,
+                  softmax_scale=case.softmax_scale, workspace=ws, num_ctas=num_ctas, merge_wait_ns=-1)
+        H.compare_bf16(H.to_u16(out), ref)
+        assert ws.error_flags() == 0
+        counters = ws.buf[256:256 + 4 * case.B * case.NKV].view(torch_cuda.int32).cpu().numpy()
+        assert not counters.any()
+
+
+def test_decode_wait_limit_expires_then_recovers(torch_cuda):
+    """wait_limit_ns = 1: the kernel's first waits for data run out at once
+    (a valid input, nothing broken): the call returns, the kernel finishes and
+    reports it in the workspace error word. After clearing that word, a default
+    call on the same workspace matches the oracle (its counters were left
+    zero by the aborted call)."""
+    import fp8_paged_kv_block_gb300 as pa
+    case = small_case()
+    inp = H.oracle_inputs(case)
+    dev = H.device_inputs(case)
+    ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile, num_ctas=7)
+    c = dev["cache"]
+    out = torch_cuda.empty((case.B * case.S1, case.NQ, case.D), dtype=torch_cuda.bfloat16, device="cuda")
+    pa.decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale, dev["block_table"],
+              dev["act"], out, S1=case.S1, layout=case.layout, s2_tile=case.s2_tile,
+              softmax_scale=case.softmax_scale, workspace=ws, num_ctas=7, wait_limit_ns=1)
+    torch_cuda.cuda.synchronize()
+    assert ws.error_flags() != 0
+    counters = ws.buf[256:256 + 4 * case.B * case.NKV].view(torch_cuda.int32).cpu().numpy()
+    assert not counters.any()
+    ws.clear_error_flags()
+    out = H.gpu_decode(case, dev, num_ctas=7, workspace=ws)
+    H.compare_bf16(H.to_u16(out), H.oracle_decode(case, inp))
+    assert ws.error_flags() == 0
