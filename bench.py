@@ -12,6 +12,10 @@ algorithmic bytes (valid tokens only), plus us/step. The step is timed on the
 device with CUDA events over exactly --steps steps replayed from CUDA graphs;
 the steps rotate over enough cache copies that their KV exceeds 3x the L2.
 
+--gpus N: one rank per GPU, each a whole replica of the step (the path has no
+exchange step); run as a plain script with N > 1 it starts N local ranks of
+itself under torch.distributed.run.
+
 --impl reference times the CPU oracle (the plain C restatement of the
 pages) on a bounded sample of the same workload on the host cores.
 """
@@ -23,6 +27,7 @@ import hashlib
 import json
 import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -44,9 +49,6 @@ WORKLOAD = ("glm45_decode_step: append 1 BF16 token/seq (quantise-on-append scat
             "s2_tile=512 PA_BSND")
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM traffic of one decode launch on this workload, from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
-# sources it was taken with.
 # Programmatic stream serialisation between the step's kernels. The decode's
 # inputs other than the KV cache (lengths, block table, q and its scales,
 # v_scale) are never written by the append kernel before it, and the append
@@ -58,11 +60,14 @@ FALLBACK_HBM_GBS = 6800.0
 OVERLAP_DECODE = 2
 OVERLAP_APPEND = True
 
+# DRAM traffic of one decode launch on this workload, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
+# sources it was taken with.
 DECODE_TRAFFIC = {"sources_sha1": "f2c5a5a43f9dc2eb1c0f2c1fbccdc9e4a25a999c",
                   "bytes_per_launch": 57871104 + 107008}
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -82,7 +87,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
-    return ap.parse_args()
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="--impl reference: wall time of the whole --steps + --warmup run")
+    return ap.parse_args(argv)
 
 
 # --------------------------------------------------------------------------
@@ -101,6 +108,27 @@ def dist_env(env=None):
         raise ValueError("bad rank environment: RANK=%d WORLD_SIZE=%d LOCAL_RANK=%d"
                          % (rank, world, local))
     return rank, world, local
+
+
+def free_port():
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def local_ranks_command(argv, nproc, port):
+    """The command that runs this script as nproc local ranks (one per GPU)
+    with the same arguments: torch.distributed.run on one node, rendezvous on
+    127.0.0.1."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            "--nproc-per-node=%d" % nproc, "--master-addr=127.0.0.1", "--master-port=%d" % port,
+            os.path.abspath(__file__)] + list(argv)
+
+
+def check_world(gpus, world):
+    """--gpus N under a launcher must match the ranks it started."""
+    if gpus != world:
+        raise SystemExit("bench.py --gpus %d but the launcher started %d ranks" % (gpus, world))
 
 
 def init_ranks(world, backend, device=None):
@@ -333,10 +361,10 @@ def reference_arm(args, rank, world):
     from concurrent.futures import ThreadPoolExecutor
     threads = host_threads()
     total_steps = args.steps + args.warmup
-    # about 150 s of wall time over the whole run: whole units in batch order
-    # while the busiest thread's estimated time per step stays within
-    # 150 s / steps (at least one unit)
-    wall = 150.0 / max(total_steps, 1)
+    # about --ref-seconds (150 s by default) of wall time over the whole run:
+    # whole units in batch order while the busiest thread's estimated time per
+    # step stays within that over the steps (at least one unit)
+    wall = args.ref_seconds / max(total_steps, 1)
     G = case.group
     load = [0.0] * threads
     rows, nbytes = [], 0
@@ -366,7 +394,7 @@ def reference_arm(args, rank, world):
     value = nbytes / dt / 1e9
     full = case.algorithmic_bytes()
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": full / (value * 1e9) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f32",
         "data": "synthetic",
@@ -384,9 +412,15 @@ def reference_arm(args, rank, world):
 # GPU arm
 # --------------------------------------------------------------------------
 
-def main():
-    args = parse_args()
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
+    args = parse_args(argv)
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # started without a launcher: start --gpus local ranks of this same
+        # command and pass on their exit status (non-zero if any rank failed)
+        sys.exit(subprocess.call(local_ranks_command(argv, args.gpus, free_port())))
     rank, world, local = dist_env()
+    check_world(args.gpus, world)
     if args.workload == "configs":
         if args.impl == "reference":
             if rank == 0:
@@ -647,22 +681,112 @@ def main():
 # Every decode configuration (--workload configs): one JSON line each
 # --------------------------------------------------------------------------
 
-CONFIGS = [  # (name, workload, description)
-    ("tiny", workloads.tiny, "B=2 S1=1 NQ=4 NKV=1 kv {37,300} s2_tile=512 PA_BSND"),
-    ("glm45", workloads.glm, "B=16 S1=1 NQ=96 NKV=8 kv~U[1,4096] s2_tile=512 PA_BSND"),
-    ("long", workloads.long_ctx, "B=4 S1=1 NQ=96 NKV=8 kv~U[32768,131072], every 64th K row x8 "
-                                 "before quantisation, s2_tile=512 PA_BSND"),
-    ("ragged", workloads.ragged, "B=256 S1=2 NQ=96 NKV=8 kv~lognormal(median 1024, sigma 1) "
-                                 "clipped to [1,16384] s2_tile=512 PA_BSND"),
-    ("append", workloads.append, "64 new BF16 K/V rows (5% of slots -1) into contexts "
-                                 "U[512,8192], NQ=96 NKV=8 BNBD, then decode over the updated cache"),
-]
+def _page_config(i):
+    b, s1, s2, nq, nkv = workloads.PAGE_CASES[i]
+    return ("page%d" % i, lambda: workloads.page_case(i, s2_tile=0),
+            "b=%d s1=%d s2=%d nq=%d nkv=%d, every sequence at its full s2 (a case of the GLM-4.5 "
+            "paged FP8 page's test table) PA_BSND" % (b, s1, s2, nq, nkv))
+
+
+CONFIGS = [  # (name, workload with s2_tile 0 = the library's automatic tile, description)
+    ("tiny", lambda: workloads.tiny(s2_tile=0), "B=2 S1=1 NQ=4 NKV=1 kv {37,300} PA_BSND"),
+    ("glm45", lambda: workloads.glm(s2_tile=0), "B=16 S1=1 NQ=96 NKV=8 kv~U[1,4096] PA_BSND"),
+    ("long", lambda: workloads.long_ctx(s2_tile=0),
+     "B=4 S1=1 NQ=96 NKV=8 kv~U[32768,131072], every 64th K row x8 before quantisation, PA_BSND"),
+    ("ragged", lambda: workloads.ragged(s2_tile=0),
+     "B=256 S1=2 NQ=96 NKV=8 kv~lognormal(median 1024, sigma 1) clipped to [1,16384] PA_BSND"),
+    ("append", lambda: workloads.append(s2_tile=0),
+     "64 new BF16 K/V rows (5% of slots -1) into contexts U[512,8192], NQ=96 NKV=8 BNBD, then "
+     "decode over the updated cache"),
+] + [_page_config(i) for i in range(len(workloads.PAGE_CASES))]
+
+
+def percentiles(samples):
+    """Median, 10th and 90th percentile of per-step samples."""
+    a = np.asarray(samples, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "samples": int(a.size)}
+
+
+def unit_rows(case, b, n2):
+    """Flat output rows (b*S1 + s)*NQ + h of the (batch b, kv head n2) unit."""
+    G = case.group
+    return [(b * case.S1 + s) * case.NQ + n2 * G + g for s in range(case.S1) for g in range(G)]
+
+
+def parity_units(case, act, budget_s, per_row_token_s, seed=0):
+    """Whole (batch, kv head) units in a seeded random order while the
+    oracle's estimated time stays within budget_s (at least one unit)."""
+    units = [(b, n2) for b in range(case.B) for n2 in range(case.NKV)]
+    order = np.random.default_rng(seed).permutation(len(units))
+    pick, est = [], 0.0
+    for k in order:
+        b, n2 = units[int(k)]
+        t = per_row_token_s * max(int(act[b]), 1) * case.S1 * case.group
+        if pick and est + t > budget_s:
+            break
+        pick.append((b, n2))
+        est += t
+    return pick
+
+
+class ConfigOracleLeg:
+    """cpu_baseline leg of one configuration: the oracle's inputs for a
+    sample of whole units (prepared while the case's K/V are in memory), then
+    the oracle on those rows, timed on one host thread, and its outputs
+    against the GPU's for the same rows (max / mean absolute error)."""
+
+    def __init__(self, case, app, act_after, budget_s):
+        from tests import _helpers as H
+        self.case, self.app, self.act = case, app, act_after
+        probe = H.oracle_inputs(case, batches=[int(np.argmin(case.act))])
+        b = int(np.argmin(case.act))
+        t0 = time.perf_counter()
+        H.oracle_decode(case, probe, rows=np.asarray(unit_rows(case, b, 0)[:1]))
+        prt = max((time.perf_counter() - t0) / max(int(case.act[b]), 1), 1e-9)
+        del probe
+        self.units = parity_units(case, act_after, budget_s, prt)
+        batches = sorted({b for b, _ in self.units})
+        self.inp = H.oracle_inputs(case, batches=batches)
+        if app is not None:
+            import oracle
+            kn, vn = app.new_kv_f32()
+            sel = np.asarray(batches)
+            oracle.cache_quant_scatter(kn[sel], vn[sel], self.inp["kc"], self.inp["vc"],
+                                       app.slot_mapping[sel].astype(np.int64), self.inp["ksc"],
+                                       self.inp["vs"], sel.astype(np.int32), layout=case.layout)
+        self.rows = np.asarray(sorted(r for b, n2 in self.units for r in unit_rows(case, b, n2)))
+
+    def run(self, gpu_out_u16):
+        from tests import _helpers as H
+        import oracle
+        dcase = dataclasses.replace(self.case, act=self.act)
+        t0 = time.perf_counter()
+        ref = H.oracle_decode(dcase, self.inp, rows=self.rows)
+        dt = time.perf_counter() - t0
+        g = oracle.bf16_to_float(gpu_out_u16).reshape(-1, self.case.D)[self.rows].astype(np.float64)
+        r = oracle.bf16_to_float(ref).reshape(-1, self.case.D)[self.rows].astype(np.float64)
+        err = np.abs(g - r)
+        nbytes = sum(int(self.act[b]) * (2 * self.case.D + 4) + self.case.S1 * self.case.group
+                     * (self.case.D * 3 + 4) + self.case.D * 4 for b, _ in self.units)
+        cpu = {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "%d whole (batch, kv head) units = %d query rows, seeded random, "
+                         "decode only, one thread, %.2f s" % (len(self.units), self.rows.size, dt)}
+        acc = {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
+               "finite": bool(np.all(np.isfinite(g))), "rows": int(self.rows.size),
+               "tol_max_abs": H.MAX_ABS_TOL, "tol_mean_abs": H.MEAN_ABS_TOL}
+        acc["within_tol"] = bool(acc["finite"] and acc["max_abs"] <= H.MAX_ABS_TOL
+                                 and acc["mean_abs"] <= H.MEAN_ABS_TOL)
+        return cpu, acc
 
 
 def configs_arm(args, rank, world, local):
-    """Decode time per launch for each configuration, inputs built on the
-    device with the library's own kernels (as the parity tests build them);
-    append + decode step for the append configuration."""
+    """Decode time per launch for each configuration at the library's
+    automatic s2_tile (and the other built tiles beside it), inputs built on
+    the device with the library's own kernels (as the parity tests build
+    them); append + decode step for the append configuration; per-replay
+    percentiles; the oracle on a sample of each configuration's rows (the
+    cpu_baseline leg) with the error of the GPU's output on those rows."""
     import torch
     import fp8_paged_kv_block_gb300 as pa
     from fp8_paged_kv_block_gb300 import paged
@@ -678,7 +802,8 @@ def configs_arm(args, rank, world, local):
     peak, peak_src = measured_hbm_peak()
 
     def timed(fn, n, reps):
-        """ms per call of fn(i): a graph of reps calls replayed n // reps times."""
+        """(ms per call of fn(i), per-replay percentiles in us per call): a
+        graph of reps calls replayed n // reps times, an event after each."""
         s = torch.cuda.Stream(device=dev)
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
@@ -691,18 +816,20 @@ def configs_arm(args, rank, world, local):
                 fn(i)
         for _ in range(max(args.warmup, 3)):
             g.replay()
+        nrep = max(3, n // reps)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(nrep + 1)]
         barrier(world)
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
         torch.cuda._sleep(200000)
-        e0.record()
-        for _ in range(max(1, n // reps)):
+        ev[0].record()
+        for k in range(nrep):
             g.replay()
-        e1.record()
+            ev[k + 1].record()
         torch.cuda.synchronize()
         barrier(world)
-        return max_over_ranks(e0.elapsed_time(e1), world, dev) / (max(1, n // reps) * reps)
+        ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world, dev) / (nrep * reps)
+        dist = percentiles([ev[k].elapsed_time(ev[k + 1]) * 1e3 / reps for k in range(nrep)])
+        return ms, dist
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -712,6 +839,11 @@ def configs_arm(args, rank, world, local):
         app = made if name == "append" else None
         case = app.ctx if app is not None else made
         act_after = app.act_after if app is not None else case.act
+        tile = case.s2_tile or pa.auto_s2_tile(case.S1, case.NQ, case.NKV,
+                                               case.max_blocks * case.BS)
+        case = dataclasses.replace(case, s2_tile=tile)
+        if app is not None:
+            app = dataclasses.replace(app, ctx=case)
         dcase = dataclasses.replace(case, act=act_after)
         dec_bytes = dcase.algorithmic_bytes()
         q8, qs = paged.quantize_queries(torch.from_numpy(case.q()).to(dev))
@@ -722,6 +854,8 @@ def configs_arm(args, rank, world, local):
                                  torch.from_numpy(case.token_batch).to(dev), case.num_blocks,
                                  case.layout)
         del k32, v32
+        leg = (ConfigOracleLeg(case, app, act_after, args.cpu_seconds / len(CONFIGS))
+               if rank == 0 and not args.no_cpu_baseline else None)
         case.drop()
         cache_bytes = 2 * base.k_cache.numel() + 4 * base.k_scale.numel()
         copies = max(1, math.ceil(3 * l2 / cache_bytes))
@@ -731,20 +865,17 @@ def configs_arm(args, rank, world, local):
         bt = torch.from_numpy(case.block_table).to(dev)
         act_d = torch.from_numpy(act_after).to(dev)
         out = torch.empty((case.B * case.S1, case.NQ, case.D), dtype=torch.bfloat16, device=dev)
-        ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, s2_tile=case.s2_tile,
-                                device=dev)
+        ws = pa.DecodeWorkspace(case.B, case.S1, case.NQ, case.NKV, device=dev)
 
-        def attend(i, overlap=OVERLAP_DECODE):
+        def attend(i, overlap=OVERLAP_DECODE, s2_tile=tile):
             c = caches[i % copies]
             pa.decode(q8, qs, c.k_cache, c.k_scale, c.v_cache, c.v_scale, bt, act_d, out,
-                      S1=case.S1, layout=case.layout, s2_tile=case.s2_tile,
+                      S1=case.S1, layout=case.layout, s2_tile=s2_tile,
                       softmax_scale=case.softmax_scale, workspace=ws, overlap_prologue=overlap)
 
         est_us = max(5.0, dec_bytes / (peak * 1e3) * 2.0)
         n = max(50, min(args.steps, int(100000 / est_us)))
         reps = copies * max(1, math.ceil(16 / copies))
-        ms_dec = timed(attend, n, reps)
-        ms_dec0 = timed(lambda i: attend(i, 0), n, reps)
         extra = {}
         if app is not None:
             kb, vb = app.new_kv_bf16()
@@ -763,34 +894,55 @@ def configs_arm(args, rank, world, local):
                 append(i)
                 attend(i)
 
-            ms_app = timed(append, n, reps)
-            ms_step = timed(step, n, reps)
-            extra = {"append_us_per_launch": ms_app * 1e3, "append_bytes": app_bytes,
-                     "step_us": ms_step * 1e3,
+            # the append first: every cache copy then holds the new token
+            ms_app, dist_app = timed(append, n, reps)
+            ms_step, dist_step = timed(step, n, reps)
+            extra = {"append_us_per_launch": ms_app * 1e3, "append_us_dist": dist_app,
+                     "append_bytes": app_bytes, "step_us": ms_step * 1e3,
+                     "step_us_dist": dist_step,
                      "step_gbs": world * (dec_bytes + app_bytes) / (ms_step * 1e-3) / 1e9}
+        ms_dec, dist_dec = timed(attend, n, reps)
+        torch.cuda.synchronize()
+        out_sel = host_u16(out)
+        ms_dec0, _ = timed(lambda i: attend(i, 0), n, reps)
+        alt = {}
+        for t in ((256, 512, 1024) if case.S1 * case.group <= 16 else (256, 512)):
+            if t != tile:
+                alt[str(t)] = timed(lambda i, t=t: attend(i, s2_tile=t), n, reps)[0] * 1e3
+        alt[str(tile)] = ms_dec * 1e3
         assert ws.error_flags() == 0, "decode kernel reported a wait timeout"
+        cpu, acc = leg.run(out_sel) if leg is not None else (None, None)
         gbs = dec_bytes / (ms_dec * 1e-3) / 1e9
         lines.append({
             "metric": METRIC, "value": world * gbs, "unit": UNIT, "n_gpus": world,
             "steps": n, "warmup": args.warmup, "ms_per_step": ms_dec,
-            "us_per_step": ms_dec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "us_per_step": ms_dec * 1e3, "us_per_step_dist": dist_dec,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3+f32", "data": "synthetic",
             "config": {"workload": name + ": " + desc, "B": case.B, "S1": case.S1,
+                       "NQ": case.NQ, "NKV": case.NKV, "s2_tile": tile,
+                       "s2_tile_rule": "automatic (s2 = block table capacity %d)"
+                                       % (case.max_blocks * case.BS),
                        "kv_tokens": int(act_after.sum()), "decode_bytes": dec_bytes,
                        "l2": ("inputs larger than L2: %d cache copies rotated (%.0f MB, L2 %.0f MB)"
                               % (copies, copies * cache_bytes / 1e6, l2 / 1e6)),
-                       "timing": "CUDA graph of back-to-back decode launches "
-                                 "(overlap_prologue=%d), CUDA events" % OVERLAP_DECODE},
+                       "timing": "CUDA graph of %d back-to-back decode launches "
+                                 "(overlap_prologue=%d) replayed, CUDA events around each "
+                                 "replay; dist = per-replay us per launch (rank 0)"
+                                 % (reps, OVERLAP_DECODE)},
             "gpu_launches": n,
             "roofline": {"bound": "hbm", "kernel": "pa_fp8_decode", "achieved": gbs, "peak": peak,
                          "unit": "GB/s", "frac": gbs / peak, "traffic": None,
                          "peak_source": peak_src, "frac_of_8tbs_nominal": gbs / 8000.0,
                          "us_per_launch": ms_dec * 1e3,
-                         "us_per_launch_stream_order": ms_dec0 * 1e3},
+                         "us_per_launch_stream_order": ms_dec0 * 1e3,
+                         "us_per_launch_by_s2_tile": alt},
+            "accuracy": acc,
+            "cpu_baseline": cpu,
             "tokens_per_s": world * case.B * case.S1 / (ms_dec * 1e-3),
             **extra,
         })
-        del caches, base, out, ws
+        del caches, base, out, ws, leg
         torch.cuda.empty_cache()
     clk = clocks.stop()
     if rank == 0:
@@ -798,6 +950,12 @@ def configs_arm(args, rank, world, local):
             line["clocks"] = clk
             print(json.dumps(line), flush=True)
     finish_ranks(world)
+
+
+def host_u16(t):
+    """A BF16 device tensor's bits as a host uint16 array."""
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
 # --------------------------------------------------------------------------
@@ -910,7 +1068,7 @@ def mla_reference_arm(args, rank, world):
     value = statistics.median(vals) if vals else 0.0
     line = {
         "impl": "reference", "metric": MLA_METRIC, "value": value, "unit": MLA_UNIT,
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": case.flops() / (value * 1e12) * 1e3 if value else None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
         "data": "synthetic", "config": {"workload": mla_workload_name(args, case.B),

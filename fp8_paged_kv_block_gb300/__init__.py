@@ -80,6 +80,8 @@ def lib():
         L.pa_fp8_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, P,
                                                    ctypes.POINTER(sz)]
         L.pa_fp8_decode_workspace_size.restype = i32
+        L.pa_fp8_decode_auto_s2_tile.argtypes = [i32, i32, i32, i64]
+        L.pa_fp8_decode_auto_s2_tile.restype = i32
         L.pa_fp8_decode.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
                                     i32, i32, f32, P, P, sz, P]
         L.pa_fp8_decode.restype = i32
@@ -175,8 +177,18 @@ def _config(s2_tile: int, num_ctas: int, overlap_prologue=0, merge_wait_ns=0, wa
     return c
 
 
+def auto_s2_tile(S1: int, NQ: int, NKV: int, s2: int) -> int:
+    """The s2_tile that s2_tile=0 selects for sequences of capacity s2 (the
+    block table's width x block_size): 1024 from 8192 tokens on where at most
+    16 query rows share a kv head, else 512 (pa_fp8_decode_auto_s2_tile)."""
+    t = lib().pa_fp8_decode_auto_s2_tile(S1, NQ, NKV, s2)
+    if t == 0:
+        raise ValueError("auto_s2_tile: invalid shape S1=%d NQ=%d NKV=%d s2=%d" % (S1, NQ, NKV, s2))
+    return t
+
+
 def decode_workspace_size(B: int, S1: int, NQ: int, NKV: int, D: int = 128, *,
-                          s2_tile: int = 512, num_ctas: int = 0) -> int:
+                          s2_tile: int = 0, num_ctas: int = 0) -> int:
     n = ctypes.c_size_t(0)
     cfg = _config(s2_tile, num_ctas)
     _check(lib().pa_fp8_decode_workspace_size(B, S1, NQ, NKV, D, ctypes.byref(cfg),
@@ -188,7 +200,7 @@ class DecodeWorkspace:
     """Zero-initialised device scratch for pa_fp8_decode (reusable: every call
     leaves its counters at zero)."""
 
-    def __init__(self, B, S1, NQ, NKV, D=128, *, s2_tile=512, num_ctas=0, device=None):
+    def __init__(self, B, S1, NQ, NKV, D=128, *, s2_tile=0, num_ctas=0, device=None):
         torch = _torch()
         self.nbytes = decode_workspace_size(B, S1, NQ, NKV, D, s2_tile=s2_tile, num_ctas=num_ctas)
         self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device or "cuda")
@@ -204,7 +216,7 @@ class DecodeWorkspace:
 
 
 def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs, out, *,
-           S1: int = 1, layout: int = LAYOUT_BSND, s2_tile: int = 512, softmax_scale=None,
+           S1: int = 1, layout: int = LAYOUT_BSND, s2_tile: int = 0, softmax_scale=None,
            workspace: DecodeWorkspace | None = None, num_ctas: int = 0, stream=None,
            overlap_prologue: int = 0, merge_wait_ns: int = 0, wait_limit_ns: int = 0):
     """Paged FP8 decode attention (in place into ``out``).
@@ -214,6 +226,7 @@ def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_s
     [NB, NKV, BS, D] for BNBD), k_scale float32 (cache shape without D),
     v_scale float32 [B, NKV, D], block_table int32 [B, max_blocks],
     kv_act_seqs int32 [B], out bfloat16 [B*S1, NQ, D].
+    s2_tile: 0 (automatic, see auto_s2_tile), 128, 256, 512 or 1024.
     overlap_prologue: 1 (or True) lets the kernel's prologue overlap the
     preceding kernel in the stream (that kernel must not write kv_act_seqs,
     block_table, q, q_scale or v_scale); 2 also lets it load the cache blocks
@@ -378,6 +391,7 @@ def value_channel_scale(v, cu_seqlens, v_scale, *, stream=None):
 
 __all__ = [
     "LAYOUT_BSND", "LAYOUT_BNBD", "PaError", "build", "lib", "decode", "decode_workspace_size",
+    "auto_s2_tile",
     "DecodeWorkspace", "cache_scatter", "cache_quant_scatter", "quantize_rows",
     "value_channel_scale",
 ]

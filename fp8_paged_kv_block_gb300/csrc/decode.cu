@@ -1303,7 +1303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the MM2 MMAs this warp issued have completed (already true unless a wait
     // gave up) before the tensor memory is released
-    if (lane == 0) {
+    if (lane == 0 && *(volatile int*)&sm.abort) {
         umma_commit(&sm.cdrain);
         mbar_wait_drain(&sm.cdrain, 0, p.err, 1024);
     }
@@ -1358,14 +1358,28 @@ struct Plan {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_config* cfg, Plan* pl)
+// s2_tile 0 picks the tile from the sequences' capacity s2 (the block table's
+// width x block_size, the longest a sequence can be): the GLM-4.5 paged FP8
+// page's configuration notes give 1024-token tiles to sequences of 8192 and
+// more; that tile is built for up to 16 query rows per kv head. Everything
+// else gets 512, this kernel's measured best at short lengths (the page's
+// short tile of 128 follows its own hardware's tiling).
+constexpr int64_t kLongS2 = 8192;
+
+int auto_s2_tile(int S1, int G, int64_t s2)
+{
+    return (s2 >= kLongS2 && static_cast<int64_t>(S1) * G <= 16) ? 1024 : 512;
+}
+
+pa_status make_plan(int B, int S1, int NQ, int NKV, int D, const pa_decode_config* cfg, Plan* pl,
+                    int64_t s2 = 0)
 {
     PA_REQUIRE(B > 0 && S1 > 0 && NQ > 0 && NKV > 0 && D > 0, PA_ERR_INVALID,
                "pa_fp8_decode: empty or negative shape (B=%d S1=%d NQ=%d NKV=%d D=%d)", B, S1, NQ, NKV, D);
     PA_REQUIRE(NQ % NKV == 0, PA_ERR_INVALID, "pa_fp8_decode: NQ %d is not a multiple of NKV %d", NQ, NKV);
     PA_REQUIRE(D == kD, PA_ERR_UNSUPPORTED, "pa_fp8_decode: head size %d (only 128 is built)", D);
     PA_REQUIRE(B <= kMaxB, PA_ERR_UNSUPPORTED, "pa_fp8_decode: batch %d > %d", B, kMaxB);
-    pl->S2T = (cfg && cfg->s2_tile) ? cfg->s2_tile : 512;
+    pl->S2T = (cfg && cfg->s2_tile) ? cfg->s2_tile : auto_s2_tile(S1, NQ / NKV, s2);
     PA_REQUIRE(pl->S2T > 0 && pl->S2T % kBS == 0, PA_ERR_INVALID,
                "pa_fp8_decode: s2_tile %d is not a multiple of block_size 128", pl->S2T);
     PA_REQUIRE(pl->S2T == 128 || pl->S2T == 256 || pl->S2T == 512 || pl->S2T == 1024, PA_ERR_UNSUPPORTED,
@@ -1460,6 +1474,12 @@ extern "C" pa_status pa_fp8_decode_workspace_size(int B, int S1, int NQ, int NKV
     return PA_OK;
 }
 
+extern "C" int pa_fp8_decode_auto_s2_tile(int S1, int NQ, int NKV, int64_t s2)
+{
+    if (S1 <= 0 || NQ <= 0 || NKV <= 0 || NQ % NKV != 0 || s2 < 0) return 0;
+    return auto_s2_tile(S1, NQ / NKV, s2);
+}
+
 extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const void* k_cache,
                                    const float* k_scale, const void* v_cache, const float* v_scale,
                                    const int32_t* block_table, const int32_t* kv_act_seqs, void* out,
@@ -1472,7 +1492,7 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
                    kv_act_seqs && out,
                PA_ERR_NULLPTR, "pa_fp8_decode: NULL tensor pointer");
     Plan pl;
-    pa_status st = make_plan(B, S1, NQ, NKV, D, cfg, &pl);
+    pa_status st = make_plan(B, S1, NQ, NKV, D, cfg, &pl, static_cast<int64_t>(max_blocks_per_seq) * block_size);
     if (st != PA_OK) return st;
     PA_REQUIRE(block_size == kBS, PA_ERR_UNSUPPORTED, "pa_fp8_decode: block_size %d (only 128 is built)", block_size);
     PA_REQUIRE(num_blocks > 0 && max_blocks_per_seq > 0, PA_ERR_INVALID,
@@ -1545,7 +1565,7 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of pa_fp8_decode: the same kernel, with its scratch
-// (split partials, per-sequence counters, error flag) in a fixed array that
+// (split partials, per-sequence counters, error word) in a fixed array that
 // is part of the library's device image instead of a caller workspace.
 // ---------------------------------------------------------------------------
 namespace pa {
@@ -1556,25 +1576,60 @@ constexpr size_t kStaticScratchBytes = static_cast<size_t>(PA_FP8_DECODE_NOALLOC
 // One array per device that loads the library, alive until process exit.
 __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    });
+    return fn;
+}
+
 // Device address of g_decode_scratch on the current device. The host-side
-// name is only a stand-in for the symbol, so the address is looked up once
-// per device (with that device current) and cached.
-pa_status decode_scratch_address(void** out)
+// name is only a stand-in for the symbol, so the address is looked up with
+// that device current and cached per device together with the context it
+// was found in: after a device reset the library's image is loaded again
+// (possibly elsewhere), the context differs, and the address is looked up
+// anew. The first lookup in a context also clears the whole array on
+// `stream` (every call leaves the counters zero after that; the error word
+// keeps its bits until the caller clears it).
+pa_status decode_scratch_address(void** out, cudaStream_t stream)
 {
     static std::mutex mu;
     static void* cache[64] = {nullptr};
+    static CUcontext ctx_of[64] = {nullptr};
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode_noalloc: cudaGetDevice: %s",
                cudaGetErrorString(e));
     PA_REQUIRE(dev >= 0 && dev < 64, PA_ERR_UNSUPPORTED, "pa_fp8_decode_noalloc: device %d", dev);
+    auto get = ctx_get_current();
+    PA_REQUIRE(get != nullptr, PA_ERR_CUDA, "pa_fp8_decode_noalloc: cuCtxGetCurrent is not available");
+    CUcontext ctx = nullptr;   // none yet before the runtime's first call on this thread
+    PA_REQUIRE(get(&ctx) == CUDA_SUCCESS, PA_ERR_CUDA, "pa_fp8_decode_noalloc: cannot read the current context");
     std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev] == nullptr) {
+    if (ctx == nullptr || cache[dev] == nullptr || ctx_of[dev] != ctx) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);   // makes the device's context current
         PA_REQUIRE(e == cudaSuccess && p != nullptr, PA_ERR_CUDA,
                    "pa_fp8_decode_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        cache[dev] = p;
+        PA_REQUIRE(get(&ctx) == CUDA_SUCCESS && ctx != nullptr, PA_ERR_CUDA,
+                   "pa_fp8_decode_noalloc: no current context");
+        if (p != cache[dev] || ctx != ctx_of[dev]) {
+            e = cudaMemsetAsync(p, 0, kStaticScratchBytes, stream);
+            PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode_noalloc: clearing scratch: %s",
+                       cudaGetErrorString(e));
+            cache[dev] = p;
+            ctx_of[dev] = ctx;
+        }
     }
     *out = cache[dev];
     return PA_OK;
@@ -1603,15 +1658,29 @@ extern "C" pa_status pa_fp8_decode_noalloc(const void* q, const float* q_scale, 
                "built-in %zu; use pa_fp8_decode with a caller workspace",
                pl.total, kStaticScratchBytes);
     void* ws = nullptr;
-    st = decode_scratch_address(&ws);
+    st = decode_scratch_address(&ws, static_cast<cudaStream_t>(stream));
     if (st != PA_OK) return st;
-    // The array keeps the previous call's contents: the error flag and the
-    // per-sequence counters must start at zero.
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeader + pl.counters_bytes, s);
-    PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode_noalloc: clearing scratch: %s",
-               cudaGetErrorString(e));
+    // Every call leaves the counters zero (also one whose waits gave up), so
+    // nothing is cleared here and the decode is the only work enqueued: with
+    // overlap_prologue it overlaps the preceding kernel as pa_fp8_decode does.
     return pa_fp8_decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs,
                          out, B, S1, NQ, NKV, D, block_size, num_blocks, max_blocks_per_seq, layout,
                          softmax_scale, cfg, ws, kStaticScratchBytes, stream);
+}
+
+extern "C" pa_status pa_fp8_decode_noalloc_error(int32_t* flags, int clear, void* stream)
+{
+    PA_REQUIRE(flags != nullptr, PA_ERR_NULLPTR, "pa_fp8_decode_noalloc_error: flags is NULL");
+    void* ws = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    pa_status st = decode_scratch_address(&ws, s);
+    if (st != PA_OK) return st;
+    cudaError_t e = cudaMemcpyAsync(flags, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode_noalloc_error: copy: %s", cudaGetErrorString(e));
+    if (clear) {
+        e = cudaMemsetAsync(ws, 0, sizeof(int32_t), s);
+        PA_REQUIRE(e == cudaSuccess, PA_ERR_CUDA, "pa_fp8_decode_noalloc_error: clear: %s",
+                   cudaGetErrorString(e));
+    }
+    return PA_OK;
 }

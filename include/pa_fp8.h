@@ -87,7 +87,9 @@ typedef struct pa_decode_config {
     int s2_tile;   /* KV tile of the online softmax and the P-quantisation
                       group ([PA] 配置说明: s2_tile). Multiple of block_size;
                       128, 256 and 512 are built, and 1024 (the pages' tile
-                      for long sequences) when S1 x NQ/NKV <= 16. Default 512. */
+                      for long sequences) when S1 x NQ/NKV <= 16. 0 (default):
+                      pa_fp8_decode_auto_s2_tile() of the block table's
+                      capacity max_blocks_per_seq x block_size.              */
     int num_ctas;  /* persistent grid size. Default: SM count x resident
                       CTAs per SM.                                            */
     int overlap_prologue; /* 1: launch with programmatic stream serialisation
@@ -176,9 +178,9 @@ PA_API const char* pa_last_error(void);
  *                this workspace (e.g. cudaMemset once after allocation);
  *                every call leaves them zero again. Calls that share a
  *                workspace must not overlap in time (same stream is fine).
- * Limits: B <= 1024; s2_tile (cfg) 128, 256, 512 (default) or 1024 (1024
- * needs S1 x NQ/NKV <= 16). Other values return PA_ERR_UNSUPPORTED before
- * anything is enqueued.
+ * Limits: B <= 1024; s2_tile (cfg) 0 (automatic), 128, 256, 512 or 1024
+ * (1024 needs S1 x NQ/NKV <= 16). Other values return PA_ERR_UNSUPPORTED
+ * before anything is enqueued.
  * Alignment: q, k_cache, v_cache, v_scale and out 16-byte aligned, k_scale
  * 4-byte aligned (PA_ERR_INVALID otherwise).
  * Errors on the device: every wait inside the kernel is bounded (about 2 s);
@@ -188,6 +190,18 @@ PA_API const char* pa_last_error(void);
  * ------------------------------------------------------------------------ */
 PA_API pa_status pa_fp8_decode_workspace_size(int B, int S1, int NQ, int NKV, int D,
                                        const pa_decode_config* cfg, size_t* bytes);
+
+/* ------------------------------------------------------------------------
+ * pa_fp8_decode_auto_s2_tile -- the s2_tile that s2_tile 0 selects.
+ * [PA] 配置说明 (s2_tile): a 1024-token tile for long sequences (its
+ * threshold 8192; the comparator is lost in the page, read here as s2 >=
+ * 8192), a short tile otherwise. Returns 1024 when s2 >= 8192 and
+ * S1 x NQ/NKV <= 16 (the query rows a 1024-token tile is built for), else
+ * 512; 0 for an invalid shape (S1, NQ or NKV < 1, NQ not a multiple of NKV,
+ * s2 < 0). s2 is the longest a sequence can be: pa_fp8_decode passes
+ * max_blocks_per_seq x block_size. Host-only; touches no device.
+ * ------------------------------------------------------------------------ */
+PA_API int pa_fp8_decode_auto_s2_tile(int S1, int NQ, int NKV, int64_t s2);
 
 PA_API pa_status pa_fp8_decode(const void* q, const float* q_scale,
                         const void* k_cache, const float* k_scale,
@@ -214,14 +228,19 @@ PA_API pa_status pa_fp8_decode(const void* q, const float* q_scale,
  * process exits. Shapes whose pa_fp8_decode_workspace_size() exceeds it are
  * rejected with PA_ERR_WORKSPACE (nothing is enqueued).
  *  - No cudaMalloc, cudaFree or allocating library routine is called.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
- *  - Each call clears the scratch's flag and counter words with
- *    cudaMemsetAsync on `stream`, then launches the decode kernel.
+ *  - The first call on each device (and the first after a device reset)
+ *    looks up the array's device address (cudaGetSymbolAddress, with that
+ *    device current) and clears the array with cudaMemsetAsync on `stream`;
+ *    make that first call before any stream capture. Later calls enqueue the
+ *    decode kernel only (so overlap_prologue works as for pa_fp8_decode):
+ *    every call leaves the array's counters zero again.
  *  - All calls on a device share the one array: calls whose execution
  *    overlaps on the GPU (different streams without ordering) race and give
  *    wrong results. Calls ordered on one stream are safe.
+ *  - Errors on the device: the array's first word is the error word of
+ *    pa_fp8_decode (a bit set when a kernel wait gave up, output undefined);
+ *    it keeps its bits across calls until cleared. Read it with
+ *    pa_fp8_decode_noalloc_error.
  * ------------------------------------------------------------------------ */
 #define PA_FP8_DECODE_NOALLOC_MAX_SCRATCH (16u << 20)
 
@@ -235,6 +254,14 @@ PA_API pa_status pa_fp8_decode_noalloc(const void* q, const float* q_scale,
                                        int max_blocks_per_seq, int layout,
                                        float softmax_scale, const pa_decode_config* cfg,
                                        void* stream);
+
+/* pa_fp8_decode_noalloc_error: enqueues on `stream` a copy of the allocation-
+ * free decode's error word (of the current device) into *flags (host memory;
+ * the value is valid once the stream has completed the copy: after a stream
+ * or event synchronisation), and, if `clear` is non-zero, then zeroes the
+ * word. Like the decode itself it allocates nothing; the pages have no
+ * counterpart to it. */
+PA_API pa_status pa_fp8_decode_noalloc_error(int32_t* flags, int clear, void* stream);
 
 /* ------------------------------------------------------------------------
  * FP8 cache append scatter ([SC] 功能说明与计算公式, 参数说明, 约束说明).

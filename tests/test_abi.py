@@ -2,14 +2,39 @@
 exports every function declared in include/pa_fp8.h, and rejects bad
 arguments before touching the device."""
 import ctypes
+
+import numpy as np
 import os
 import re
 import subprocess
 
 import pytest
 
+import workloads
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pa_fp8.h")
+
+
+_KEEP = []
+
+
+def _buf():
+    """A small real buffer (64 KiB) for an argument that validation must reject
+    before any use: device memory when a GPU is present, so that a regression
+    that launched anyway would still touch valid memory; host memory otherwise
+    (no kernel can run without a device)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            t = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+            _KEEP.append(t)
+            return ctypes.c_void_p(t.data_ptr())
+    except ImportError:
+        pass
+    a = np.zeros(1 << 16, dtype=np.uint8)
+    _KEEP.append(a)
+    return ctypes.c_void_p(a.ctypes.data)
 
 
 @pytest.fixture(scope="module")
@@ -60,7 +85,7 @@ def test_status_strings(L):
 
 def test_scatter_rejects_bad_arguments_without_launching(L):
     P = ctypes.c_void_p
-    fake = P(256)  # never dereferenced: validation fails first
+    fake = _buf()  # never dereferenced: validation fails first
     st = L.pa_fp8_cache_scatter(None, fake, fake, fake, fake, 0, fake, 1, 1, fake, 4, 8, 128, 128,
                                 2, 16, 1, None)
     assert st == 1 and b"NULL" in L.pa_last_error()
@@ -103,7 +128,7 @@ def test_decode_rejects_bad_arguments_without_launching(L):
                                           ctypes.byref(n)) == 2
     assert b"overlap_prologue" in L.pa_last_error()
     P = ctypes.c_void_p
-    fake = P(256)
+    fake = _buf()
     st = L.pa_fp8_decode(fake, fake, None, fake, fake, fake, fake, fake, fake, 16, 1, 96, 8, 128,
                          128, 10, 4, 0, ctypes.c_float(0.088), None, fake, 1 << 20, None)
     assert st == 1
@@ -111,7 +136,7 @@ def test_decode_rejects_bad_arguments_without_launching(L):
 
 def test_quantizers_reject_bad_arguments(L):
     P = ctypes.c_void_p
-    fake = P(256)
+    fake = _buf()
     assert L.pa_fp8_quantize_rows(fake, 0, 10, 6, fake, fake, None) == 5
     assert L.pa_fp8_quantize_rows(fake, 9, 10, 128, fake, fake, None) == 2
     assert L.pa_fp8_quantize_rows(None, 0, 10, 128, fake, fake, None) == 1
@@ -133,7 +158,7 @@ def test_product_path_has_no_oracle_dependency():
 
 def test_kv_compress_epilog_rejects_bad_arguments(L):
     P = ctypes.c_void_p
-    fake = P(256)
+    fake = _buf()
     f = L.pa_fp8_kv_compress_epilog
     f.restype = ctypes.c_int
     f.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int, P, ctypes.c_int64,
@@ -154,7 +179,7 @@ def test_mla_sparse_decode_rejects_bad_arguments(L):
     """Host validation of the MLA decode: every rejection happens before a
     launch (no GPU is needed to reach these answers)."""
     P = ctypes.c_void_p
-    fake = P(256)
+    fake = _buf()
     f = L.pa_mla_sparse_decode
     scale = ctypes.c_float(1.0 / 24.0)
 
@@ -184,7 +209,7 @@ def test_mla_sparse_decode_kvc_rejects_bad_arguments(L):
     """Host validation of the MLA decode over KV compress epilog rows: the
     shared checks, plus the quant mode (0 and 1 are built, 2 is HiFloat8)."""
     P = ctypes.c_void_p
-    fake = P(256)
+    fake = _buf()
     f = L.pa_mla_sparse_decode_kvc
     scale = ctypes.c_float(1.0 / 24.0)
 
@@ -255,3 +280,32 @@ def test_binding_argtypes_match_the_header(L):
         assert got == want, (name, got, want)
         checked += 1
     assert checked >= 11
+
+
+def test_auto_s2_tile_rule(L):
+    """s2_tile 0: [PA] 配置说明's long-sequence tile of 1024 from s2 = 8192
+    on (s2 = the block table's capacity), where at most 16 query rows share a
+    kv head (the rows a 1024-token tile is built for); 512 otherwise."""
+    import fp8_paged_kv_block_gb300 as pa
+    f = L.pa_fp8_decode_auto_s2_tile
+    assert f(1, 96, 8, 33 * 128) == 512          # GLM-4.5 bench shape: U[1, 4096]
+    assert f(1, 96, 8, 8191) == 512
+    assert f(1, 96, 8, 8192) == 1024             # the page's threshold
+    assert f(1, 96, 8, 1025 * 128) == 1024       # 32K-131K contexts
+    assert f(2, 96, 8, 129 * 128) == 512         # 24 rows per kv head: 1024 not built
+    assert f(1, 128, 4, 1 << 20) == 512          # 32 rows per kv head
+    assert f(1, 16, 1, 8192) == 1024             # 16 rows: still built
+    for i, (b, s1, s2, nq, nkv) in enumerate(workloads.PAGE_CASES):
+        cap = -(-s2 // 128) * 128
+        want = 1024 if cap >= 8192 and s1 * nq // nkv <= 16 else 512
+        assert pa.auto_s2_tile(s1, nq, nkv, cap) == want, i
+    assert [pa.auto_s2_tile(s1, nq, nkv, -(-s2 // 128) * 128)
+            for b, s1, s2, nq, nkv in workloads.PAGE_CASES] == [512, 1024, 1024, 1024, 512, 512]
+    for bad in ((0, 8, 1, 100), (1, 0, 1, 100), (1, 8, 0, 100), (1, 12, 5, 100), (1, 8, 1, -1)):
+        assert f(*bad) == 0
+    with pytest.raises(ValueError):
+        pa.auto_s2_tile(1, 12, 5, 100)
+    # the workspace size does not depend on the tile, so s2_tile 0 sizes it
+    assert (pa.decode_workspace_size(16, 1, 96, 8, num_ctas=152)
+            == pa.decode_workspace_size(16, 1, 96, 8, s2_tile=512, num_ctas=152)
+            == pa.decode_workspace_size(16, 1, 96, 8, s2_tile=128, num_ctas=152))

@@ -3,7 +3,8 @@
 Each GPU runs a whole replica of the decode step (the path has no exchange
 step); the ranks meet only on the host: a barrier on both sides of the timed
 region, the slowest rank's time, and the whole-job throughput over all ranks.
-These tests run that logic as two processes over gloo on 127.0.0.1.
+These tests run that logic as two processes over gloo on 127.0.0.1, and the
+launcher that bench.py --gpus N uses when it is started as a plain script.
 """
 import contextlib
 import io
@@ -108,3 +109,33 @@ def test_two_gloo_ranks(tmp_path):
         assert value == pytest.approx(WORLD * 1_000_000 * 10 / 7.25e-3 / 1e9)
         assert printed == ""
     assert rows[0][2] > 0.2                    # rank 0 waited at the barrier for rank 1
+
+
+def test_launcher_command_and_world_check():
+    cmd = bench.local_ranks_command(["--gpus", "4", "--steps", "3"], 4, 29123)
+    assert cmd[:3] == [sys.executable, "-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--master-addr=127.0.0.1" in cmd
+    assert "--master-port=29123" in cmd
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "3"]
+    assert os.path.samefile(cmd[-5], os.path.join(ROOT, "bench.py"))
+    bench.check_world(2, 2)
+    with pytest.raises(SystemExit):
+        bench.check_world(2, 1)
+
+
+def test_gpus_2_without_a_launcher_starts_two_ranks():
+    """bench.py --gpus 2 run as a plain script starts two local ranks of
+    itself under torch.distributed.run; with --impl reference rank 0 alone
+    prints its line, which carries n_gpus 2, and both ranks exit 0."""
+    import subprocess
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "0", "--ref-seconds", "0.2"],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]

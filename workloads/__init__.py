@@ -284,7 +284,8 @@ class AppendCase:
         return (self.ctx.act + (self.slot_mapping >= 0)).astype(np.int32)
 
 
-def append(frac_skip: float = 0.05, B: int = 64, lo: int = 512, hi: int = 8192) -> AppendCase:
+def append(frac_skip: float = 0.05, B: int = 64, lo: int = 512, hi: int = 8192,
+           s2_tile: int = 512) -> AppendCase:
     """64 new BF16 K/V rows into contexts ~ U{512..8192}, NQ=96, NKV=8, BNBD."""
     seed = BASE_SEED + 4
     r = _rng(seed, 9)
@@ -301,7 +302,8 @@ def append(frac_skip: float = 0.05, B: int = 64, lo: int = 512, hi: int = 8192) 
         bt[b, :need[b]] = perm[pos:pos + need[b]]
         pos += need[b]
     ctx = DecodeCase(name="append", B=B, S1=1, NQ=96, NKV=8, act=act, max_blocks=max_blocks,
-                     num_blocks=num_blocks, block_table=bt, seed=seed, layout=LAYOUT_BNBD)
+                     num_blocks=num_blocks, block_table=bt, seed=seed, layout=LAYOUT_BNBD,
+                     s2_tile=s2_tile)
     slot = (bt[np.arange(B), act // BS].astype(np.int64) * BS + act % BS).astype(np.int32)
     nskip = int(round(frac_skip * B))
     skip = r.choice(B, size=nskip, replace=False)
