@@ -110,6 +110,9 @@ typedef struct pa_decode_config {
                       write each sequence's S1 newest positions, as the
                       append of a decode step does). Key scales, the newest
                       blocks, out and the workspace still wait for it.
+                      Units of more than 16 query rows per kv head
+                      (S1 x NQ/NKV > 16) are always launched in plain
+                      stream order: 1 and 2 act as 0 there.
                       Other values return PA_ERR_INVALID.                     */
     int merge_wait_ns; /* test and diagnostic knob. A sequence whose tiles are
                       spread over several CTAs is merged by its first CTA,

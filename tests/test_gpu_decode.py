@@ -122,6 +122,33 @@ def test_decode_s1_two_rows_per_head(torch_cuda):
     _run_case(case, num_ctas=4)
 
 
+def test_decode_32_row_units_run_in_stream_order(torch_cuda):
+    """More than 16 query rows per kv head: overlap_prologue 1 and 2 act as 0
+    (plain stream order); the output matches the oracle."""
+    import fp8_paged_kv_block_gb300 as pa
+    case = workloads.custom("s1two", 3, 2, 24, 2, [100, 700, 1500], s2_tile=512)
+    inp = H.oracle_inputs(case)
+    dev = H.device_inputs(case)
+    c = dev["cache"]
+    ref = H.oracle_decode(case, inp)
+    for overlap in (1, 2):
+        out = torch_cuda.full((case.B * case.S1, case.NQ, case.D), float("nan"),
+                              dtype=torch_cuda.bfloat16, device="cuda")
+        pa.decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale,
+                  dev["block_table"], dev["act"], out, S1=case.S1, layout=case.layout,
+                  s2_tile=512, softmax_scale=case.softmax_scale, overlap_prologue=overlap)
+        torch_cuda.cuda.synchronize()
+        H.compare_bf16(H.to_u16(out), ref)
+
+
+@pytest.mark.parametrize("num_ctas", [0, 5])
+def test_decode_24_rows_at_one_position(torch_cuda, num_ctas):
+    """24 query heads per kv head at S1=1: 24 rows in one 32-row chunk, whose
+    8 padding rows' softmax work is skipped; split across CTAs (5) or not."""
+    case = workloads.custom("g24", 4, 1, 48, 2, [1, 600, 1537, 3000], s2_tile=512)
+    _run_case(case, num_ctas=num_ctas)
+
+
 @pytest.mark.parametrize("layout", [workloads.LAYOUT_BSND, workloads.LAYOUT_BNBD])
 @pytest.mark.parametrize("nkv", [3, 5, 6, 7])
 def test_decode_kv_head_counts(torch_cuda, nkv, layout):
