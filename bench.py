@@ -63,8 +63,8 @@ OVERLAP_APPEND = True
 # DRAM traffic of one decode launch on this workload, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources it was taken with.
-DECODE_TRAFFIC = {"sources_sha1": "f2c5a5a43f9dc2eb1c0f2c1fbccdc9e4a25a999c",
-                  "bytes_per_launch": 57871104 + 107008}
+DECODE_TRAFFIC = {"sources_sha1": "dd6e60f3cdfe5b009974fbe8dad986e998ae3eb8",
+                  "bytes_per_launch": 57872384 + 106752}
 
 
 def parse_args(argv=None):
