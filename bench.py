@@ -587,6 +587,11 @@ def main(argv=None):
     # ---- end to end through the public API with host buffers ----
     # The step's inputs travel in one pinned host buffer (one host-to-device
     # copy per step); the output comes back with one device-to-host copy.
+    # As a serving loop runs it: two device input buffers and two output
+    # buffers alternate, the input copy of step i (its own stream) overlaps
+    # the kernels of step i-1 and the output copy of step i (another stream)
+    # those of step i+1; every step still copies its own inputs in and its
+    # output back, and the timed region ends after the last output copy.
     host_parts = [q8.cpu(), qs.cpu(), knew, vnew, torch.from_numpy(slot), torch.from_numpy(act_after),
                   torch.from_numpy(case.block_table)]
     offs, total = [], 0
@@ -597,27 +602,62 @@ def main(argv=None):
     for t, o in zip(host_parts, offs):
         n = t.numel() * t.element_size()
         h_pack[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
-    d_pack = torch.empty(total, dtype=torch.uint8, device=dev)
-    d_q8, d_qs, d_kn, d_vn, d_slot, d_act, d_bt = [
-        d_pack[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-        for t, o in zip(host_parts, offs)]
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    NBUF = 2
+    d_packs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(NBUF)]
+    d_views = [[dp[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                for t, o in zip(host_parts, offs)] for dp in d_packs]
+    outs = [torch.empty_like(out) for _ in range(NBUF)]
+    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(NBUF)]
     h2d = total
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
 
-    def e2e_step(i):
-        c = caches[i % copies]
-        d_pack.copy_(h_pack, non_blocking=True)
-        pa.cache_quant_scatter(d_kn, d_vn, c.k_cache, c.v_cache, d_slot, c.k_scale, c.v_scale,
-                               tb_d, layout=case.layout)
-        pa.decode(d_q8, d_qs, c.k_cache, c.k_scale, c.v_cache, c.v_scale, d_bt, d_act, out,
-                  S1=case.S1, layout=case.layout, s2_tile=case.s2_tile,
-                  softmax_scale=case.softmax_scale, workspace=ws, overlap_prologue=OVERLAP_DECODE)
-        h_out.copy_(out, non_blocking=True)
+    def e2e_steps(i0, n):
+        main = torch.cuda.current_stream()
+        ev_in = [torch.cuda.Event() for _ in range(NBUF)]    # inputs of buffer k landed
+        ev_used = [torch.cuda.Event() for _ in range(NBUF)]  # kernels done with buffer k
+        ev_out = [torch.cuda.Event() for _ in range(NBUF)]   # output k copied to the host
+        for k in range(NBUF):
+            ev_used[k].record(main)
+            ev_out[k].record(main)
+        for i in range(i0, i0 + n):
+            k = i % NBUF
+            c = caches[i % copies]
+            d_q8, d_qs, d_kn, d_vn, d_slot, d_act, d_bt = d_views[k]
+            s_in.wait_event(ev_used[k])
+            with torch.cuda.stream(s_in):
+                d_packs[k].copy_(h_pack, non_blocking=True)
+            ev_in[k].record(s_in)
+            main.wait_event(ev_in[k])
+            main.wait_event(ev_out[k])
+            pa.cache_quant_scatter(d_kn, d_vn, c.k_cache, c.v_cache, d_slot, c.k_scale, c.v_scale,
+                                   tb_d, layout=case.layout, overlap_prologue=OVERLAP_APPEND)
+            pa.decode(d_q8, d_qs, c.k_cache, c.k_scale, c.v_cache, c.v_scale, d_bt, d_act,
+                      outs[k], S1=case.S1, layout=case.layout, s2_tile=case.s2_tile,
+                      softmax_scale=case.softmax_scale, workspace=ws,
+                      overlap_prologue=OVERLAP_DECODE)
+            ev_used[k].record(main)
+            s_out.wait_event(ev_used[k])
+            with torch.cuda.stream(s_out):
+                h_outs[k].copy_(outs[k], non_blocking=True)
+            ev_out[k].record(s_out)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+
+    def e2e_graph(n):
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            e2e_steps(0, min(n, NBUF * copies))
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            e2e_steps(0, n)
+        return g
 
     # eager calls (one Python round trip per API call) ...
-    for i in range(3):
-        e2e_step(i)
+    e2e_steps(0, 3)
     torch.cuda.synchronize()
     n_e2e = args.steps
     barrier(world)
@@ -625,15 +665,14 @@ def main(argv=None):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(n_e2e):
-        e2e_step(i)
+    e2e_steps(0, n_e2e)
     e1.record()
     torch.cuda.synchronize()
     ms_e2e_eager = e0.elapsed_time(e1)
     # ... and the same calls captured once in a CUDA graph (how a serving loop
-    # issues a decode step): every replayed step still copies its inputs in
+    # issues its decode steps): every replayed step still copies its inputs in
     # from pinned host memory and its output back
-    g_e2e = with_tail(e2e_step, capture(e2e_step, cyc), counts)
+    g_e2e = (e2e_graph(cyc), {n % cyc: e2e_graph(n % cyc) for n in counts if n % cyc})
     run_steps(g_e2e, max(args.warmup, 3))
     ms_e2e = timed(g_e2e, n_e2e)
     clk = clocks.stop()
@@ -689,8 +728,11 @@ def main(argv=None):
             "e2e": {"value": whole_job_gbs(world, bytes_per_step, n_e2e, ms_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_step": ms_e2e / n_e2e * 1e3,
-                    "issue": "the public-API calls of a step (pinned H2D copy, append, decode, "
-                             "D2H copy of the output) captured in a CUDA graph, replayed per step",
+                    "issue": "the public-API calls of each step (pinned H2D copy of its "
+                             "inputs, append, decode, D2H copy of its output) captured in a CUDA "
+                             "graph; two input and two output buffers alternate so that a "
+                             "step's copies overlap its neighbours' kernels (copies on their "
+                             "own streams, ordered by events)",
                     "eager_us_per_step": ms_e2e_eager / n_e2e * 1e3},
             "clocks": clk,
             "cpu_baseline": cpu,
