@@ -1253,23 +1253,60 @@ def mla_arm(args, rank, world, local):
         torch.cuda.synchronize()
 
     # ---- end to end: queries and selections in from pinned host memory, the
-    # output back, around every launch (one CUDA graph per step) ----
+    # output back, every step; two device input sets and two outputs alternate
+    # so that a step's copies (on their own streams, ordered by events)
+    # overlap its neighbours' decode; captured in CUDA graphs ----
     h_q = [qn_h.pin_memory(), qr_h.pin_memory()]
     h_tk = [torch.from_numpy(case.topk_indices(v)).pin_memory() for v in range(V)]
-    d_q = [torch.empty_like(qn), torch.empty_like(qr)]
-    d_tk = torch.empty_like(tks[0])
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    NBUF = 2
+    d_qs = [[torch.empty_like(qn), torch.empty_like(qr)] for _ in range(NBUF)]
+    d_tks = [torch.empty_like(tks[0]) for _ in range(NBUF)]
+    d_outs = [torch.empty_like(out) for _ in range(NBUF)]
+    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(NBUF)]
     h2d = sum(t.numel() * t.element_size() for t in h_q) + h_tk[0].numel() * 4
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
 
-    def e2e_step(i):
-        d_q[0].copy_(h_q[0], non_blocking=True)
-        d_q[1].copy_(h_q[1], non_blocking=True)
-        d_tk.copy_(h_tk[i % V], non_blocking=True)
-        launch(i, q=d_q, tk=d_tk)
-        h_out.copy_(out, non_blocking=True)
+    def e2e_steps(n):
+        main = torch.cuda.current_stream()
+        ev_in = [torch.cuda.Event() for _ in range(NBUF)]
+        ev_used = [torch.cuda.Event() for _ in range(NBUF)]
+        ev_out = [torch.cuda.Event() for _ in range(NBUF)]
+        for k in range(NBUF):
+            ev_used[k].record(main)
+            ev_out[k].record(main)
+        for i in range(n):
+            k = i % NBUF
+            s_in.wait_event(ev_used[k])
+            with torch.cuda.stream(s_in):
+                d_qs[k][0].copy_(h_q[0], non_blocking=True)
+                d_qs[k][1].copy_(h_q[1], non_blocking=True)
+                d_tks[k].copy_(h_tk[i % V], non_blocking=True)
+            ev_in[k].record(s_in)
+            main.wait_event(ev_in[k])
+            main.wait_event(ev_out[k])
+            launch(i, q=d_qs[k], tk=d_tks[k], o=d_outs[k])
+            ev_used[k].record(main)
+            s_out.wait_event(ev_used[k])
+            with torch.cuda.stream(s_out):
+                h_outs[k].copy_(d_outs[k], non_blocking=True)
+            ev_out[k].record(s_out)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
 
-    g_e2e = (capture(e2e_step, cyc), {n % cyc: capture(e2e_step, n % cyc) for n in counts if n % cyc})
+    def e2e_graph(n):
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            e2e_steps(min(n, NBUF * V))
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            e2e_steps(n)
+        return g
+
+    g_e2e = (e2e_graph(cyc), {n % cyc: e2e_graph(n % cyc) for n in counts if n % cyc})
     run_steps(g_e2e, max(args.warmup, 3))
     n_e2e = args.steps
     ms_e2e = timed(g_e2e, n_e2e)
@@ -1326,7 +1363,9 @@ def mla_arm(args, rank, world, local):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_step": ms_e2e / n_e2e * 1e3,
                     "issue": "pinned H2D copies of the queries and the step's top-k selection, "
-                             "the decode, the D2H copy of the output: one CUDA graph per step"},
+                             "the decode, the D2H copy of the output, every step; two buffer "
+                             "sets alternate so that a step's copies (own streams, ordered by "
+                             "events) overlap its neighbours' decode; CUDA graphs"},
             "clocks": clk,
             "cpu_baseline": cpu,
         }
