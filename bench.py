@@ -288,6 +288,22 @@ def run_oracle_rows(case, inp, rows):
                             softmax_scale=case.softmax_scale, rows=np.asarray(rows))
 
 
+def host_cpu() -> dict:
+    """The host's CPU model (lscpu's model name, else the machine type) and its
+    core count, recorded beside every oracle timing."""
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":", 1)[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return {"cpu_model": model or platform.machine(), "nproc": os.cpu_count() or 0}
+
+
 def host_threads() -> int:
     """Cores this process may run on."""
     try:
@@ -401,7 +417,8 @@ def reference_arm(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f32",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample_rows": len(rows)},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(chunks), "kind": "oracle",
+        "cpu_baseline": {**host_cpu(), "value": value, "unit": UNIT, "cores": len(chunks),
+                         "kind": "oracle",
                          "sample": "%d query rows (whole units, dealt round-robin to %d threads) "
                                    "per step, decode only; ms_per_step extrapolated to the full "
                                    "step by bytes" % (len(rows), len(chunks))},
@@ -692,6 +709,7 @@ def main(argv=None):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(workload(), args.cpu_seconds)
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu.update(host_cpu())
 
     if rank == 0:
         line = {
@@ -834,7 +852,7 @@ class ConfigOracleLeg:
         err = np.abs(g - r)
         nbytes = sum(int(self.act[b]) * (2 * self.case.D + 4) + self.case.S1 * self.case.group
                      * (self.case.D * 3 + 4) + self.case.D * 4 for b, _ in self.units)
-        cpu = {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+        cpu = {**host_cpu(), "value": nbytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "%d whole (batch, kv head) units = %d query rows, seeded random, "
                          "decode only, one thread, %.2f s" % (len(self.units), self.rows.size, dt)}
         acc = {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
@@ -1153,7 +1171,8 @@ def mla_reference_arm(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
         "data": "synthetic", "config": {"workload": mla_workload_name(args, case.B),
                                         "sample_tokens": tok},
-        "cpu_baseline": {"value": value, "unit": MLA_UNIT, "cores": threads, "kind": "oracle",
+        "cpu_baseline": {**host_cpu(), "value": value, "unit": MLA_UNIT, "cores": threads,
+                         "kind": "oracle",
                          "sample": "%d query tokens (all 128 heads) per step, %d at a time on "
                                    "%d threads; ms_per_step extrapolated to the 128-token decode "
                                    "by flops" % (tok, threads, threads)},
@@ -1331,7 +1350,7 @@ def mla_arm(args, rank, world, local):
         host = mla_host_cache(case, used, rb)
         threads = host_threads()
         v, tok, dt, _ = mla_oracle_sample(case, host, args.cpu_seconds, fmt, threads)
-        cpu = {"value": v, "unit": MLA_UNIT, "cores": threads, "kind": "oracle",
+        cpu = {**host_cpu(), "value": v, "unit": MLA_UNIT, "cores": threads, "kind": "oracle",
                "sample": "%d query tokens x 128 heads of the same workload (top-k selection 0), "
                          "C oracle, %d tokens at a time on %d threads, %.1f s"
                          % (tok, threads, threads, dt)}

@@ -94,3 +94,9 @@ def test_config_oracle_leg_reports_the_error_of_the_gpu_rows():
     _, acc = leg.run(bad.reshape(full.shape))
     assert acc["max_abs"] == abs(x - y) > 0
     assert acc["mean_abs"] == abs(x - y) / (3 * 8 * case.D)
+
+
+def test_host_cpu_record():
+    rec = bench.host_cpu()
+    assert isinstance(rec["cpu_model"], str) and rec["cpu_model"]
+    assert rec["nproc"] >= 1
