@@ -235,6 +235,19 @@ def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_s
     merge_wait_ns, wait_limit_ns: test and diagnostic knobs, see
     pa_decode_config.
     """
+    args, keep = _decode_args(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table,
+                              kv_act_seqs, out, S1, layout, s2_tile, softmax_scale, workspace,
+                              num_ctas, overlap_prologue, merge_wait_ns, wait_limit_ns)
+    _check(lib().pa_fp8_decode(*args, _stream(stream)), "pa_fp8_decode")
+    del keep   # (a workspace made here lives until the launch is enqueued)
+    return out
+
+
+def _decode_args(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs, out,
+                 S1, layout, s2_tile, softmax_scale, workspace, num_ctas, overlap_prologue,
+                 merge_wait_ns, wait_limit_ns):
+    """pa_fp8_decode's arguments but the stream, validated, and the objects
+    they point into."""
     torch = _torch()
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, _fp8_types())
@@ -256,13 +269,42 @@ def decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_s
         workspace = DecodeWorkspace(B, S1, NQ, NKV, D, s2_tile=s2_tile, num_ctas=num_ctas,
                                     device=q.device)
     cfg = _config(s2_tile, num_ctas, overlap_prologue, merge_wait_ns, wait_limit_ns)
-    st = lib().pa_fp8_decode(_ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
-                             _ptr(v_scale), _ptr(block_table), _ptr(kv_act_seqs), _ptr(out),
-                             B, S1, NQ, NKV, D, BS, NB, block_table.shape[1], layout,
-                             float(softmax_scale), ctypes.byref(cfg), _ptr(workspace.buf),
-                             workspace.nbytes, _stream(stream))
-    _check(st, "pa_fp8_decode")
-    return out
+    args = (_ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
+            _ptr(block_table), _ptr(kv_act_seqs), _ptr(out), B, S1, NQ, NKV, D, BS, NB,
+            block_table.shape[1], layout, float(softmax_scale), ctypes.byref(cfg),
+            _ptr(workspace.buf), workspace.nbytes)
+    keep = (q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs, out,
+            workspace, cfg)
+    return args, keep
+
+
+class _Prepared:
+    """A library call whose arguments were validated and marshalled once, for
+    a loop that makes the same call every step (the buffers' contents may
+    change between calls, not their addresses, shapes or dtypes). Runs on the
+    stream given when it was made (default: the current stream then), or on
+    the stream passed to the call."""
+
+    def __init__(self, fn, where, args, keep, stream):
+        self._fn, self._where, self._args, self._keep = fn, where, args, keep
+        self._stream = _stream(stream)
+
+    def __call__(self, stream=None):
+        st = self._fn(*self._args, self._stream if stream is None else _stream(stream))
+        if st != PA_OK:
+            _check(st, self._where)
+
+
+def prepare_decode(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table, kv_act_seqs, out,
+                   *, S1: int = 1, layout: int = LAYOUT_BSND, s2_tile: int = 0,
+                   softmax_scale=None, workspace: DecodeWorkspace | None = None,
+                   num_ctas: int = 0, overlap_prologue: int = 0, stream=None):
+    """decode() prepared once: returns a callable that launches the same
+    decode on the same buffers (arguments as for decode())."""
+    args, keep = _decode_args(q, q_scale, k_cache, k_scale, v_cache, v_scale, block_table,
+                              kv_act_seqs, out, S1, layout, s2_tile, softmax_scale, workspace,
+                              num_ctas, overlap_prologue, 0, 0)
+    return _Prepared(lib().pa_fp8_decode, "pa_fp8_decode", args, keep, stream)
 
 
 # --------------------------------------------------------------------------
@@ -317,6 +359,15 @@ def cache_quant_scatter(key, value, key_cache, value_cache, slot_mapping, key_sc
     programmatic stream serialisation: the inputs are read while the preceding
     kernel may still run (it must not write them), the caches are written after
     it has completed."""
+    args, keep = _quant_scatter_args(key, value, key_cache, value_cache, slot_mapping,
+                                     key_scale_cache, v_scale, token_batch, layout,
+                                     overlap_prologue)
+    _check(lib().pa_fp8_cache_quant_scatter(*args, _stream(stream)), "pa_fp8_cache_quant_scatter")
+    del keep
+
+
+def _quant_scatter_args(key, value, key_cache, value_cache, slot_mapping, key_scale_cache,
+                        v_scale, token_batch, layout, overlap_prologue):
     torch = _torch()
     _need(key, "key", (torch.float32, torch.bfloat16))
     _need(value, "value", (key.dtype,))
@@ -328,13 +379,26 @@ def cache_quant_scatter(key, value, key_cache, value_cache, slot_mapping, key_sc
     _need(token_batch, "token_batch", torch.int32)
     T, H, D = key.shape
     NB, _, BS = _cache_dims(key_cache, layout)
-    st = lib().pa_fp8_cache_quant_scatter(_ptr(key), _ptr(value), _in_dtype(key), _ptr(key_cache),
-                                          _ptr(value_cache), _ptr(slot_mapping),
-                                          _slot_type(slot_mapping), _ptr(key_scale_cache),
-                                          _ptr(v_scale), _ptr(token_batch), v_scale.shape[0], T, H,
-                                          D, NB, BS, layout, int(bool(overlap_prologue)),
-                                          _stream(stream))
-    _check(st, "pa_fp8_cache_quant_scatter")
+    args = (_ptr(key), _ptr(value), _in_dtype(key), _ptr(key_cache), _ptr(value_cache),
+            _ptr(slot_mapping), _slot_type(slot_mapping), _ptr(key_scale_cache), _ptr(v_scale),
+            _ptr(token_batch), v_scale.shape[0], T, H, D, NB, BS, layout,
+            int(bool(overlap_prologue)))
+    keep = (key, value, key_cache, value_cache, slot_mapping, key_scale_cache, v_scale,
+            token_batch)
+    return args, keep
+
+
+def prepare_cache_quant_scatter(key, value, key_cache, value_cache, slot_mapping,
+                                key_scale_cache, v_scale, token_batch, *,
+                                layout: int = LAYOUT_BNBD, overlap_prologue: bool = False,
+                                stream=None):
+    """cache_quant_scatter() prepared once: returns a callable that launches the
+    same append on the same buffers."""
+    args, keep = _quant_scatter_args(key, value, key_cache, value_cache, slot_mapping,
+                                     key_scale_cache, v_scale, token_batch, layout,
+                                     overlap_prologue)
+    return _Prepared(lib().pa_fp8_cache_quant_scatter, "pa_fp8_cache_quant_scatter", args, keep,
+                     stream)
 
 
 def kv_compress_epilog(cache, x, slot_mapping, *, quant_group_size: int = 64, quant_mode: int = 1,
@@ -391,7 +455,7 @@ def value_channel_scale(v, cu_seqlens, v_scale, *, stream=None):
 
 __all__ = [
     "LAYOUT_BSND", "LAYOUT_BNBD", "PaError", "build", "lib", "decode", "decode_workspace_size",
-    "auto_s2_tile",
+    "auto_s2_tile", "prepare_decode", "prepare_cache_quant_scatter",
     "DecodeWorkspace", "cache_scatter", "cache_quant_scatter", "quantize_rows",
     "value_channel_scale",
 ]

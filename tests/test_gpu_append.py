@@ -284,6 +284,70 @@ def test_step_chain_overlap_in_graph(torch_cuda, mode):
         check()
 
 
+def test_prepared_step_calls(torch_cuda):
+    """prepare_cache_quant_scatter and prepare_decode: the step's two calls
+    validated and marshalled once, then launched (programmatic serialisation,
+    decode mode 2) eagerly on the prepared stream, on another stream, and
+    captured in a CUDA graph; output against the oracle, cache bit-exact."""
+    torch = torch_cuda
+    import dataclasses
+    import fp8_paged_kv_block_gb300 as pa
+    case = workloads.custom("prep", 6, 1, 24, 2, [1, 127, 700, 1300, 2049, 3000], max_blocks=25)
+    inp = H.oracle_inputs(case)
+    dev = H.device_inputs(case)
+    knew, vnew, slot, act_after = workloads.step_tokens(case)
+    oracle.cache_quant_scatter(knew.float().numpy(), vnew.float().numpy(), inp["kc"], inp["vc"],
+                               slot.astype(np.int64), inp["ksc"], inp["vs"],
+                               np.arange(case.B, dtype=np.int32), layout=case.layout)
+    ref = H.oracle_decode(dataclasses.replace(case, act=act_after), inp)
+    c = dev["cache"]
+    snap = [t.clone() for t in (c.k_cache, c.v_cache, c.k_scale)]
+    out = torch.empty((case.B * case.S1, case.NQ, case.D), dtype=torch.bfloat16, device="cuda")
+    kn, vn = knew.cuda(), vnew.cuda()
+    sl = torch.from_numpy(slot).cuda()
+    tb = torch.arange(case.B, dtype=torch.int32, device="cuda")
+    act1 = torch.from_numpy(act_after).cuda()
+    append = pa.prepare_cache_quant_scatter(kn, vn, c.k_cache, c.v_cache, sl, c.k_scale,
+                                            c.v_scale, tb, layout=case.layout,
+                                            overlap_prologue=True)
+    attend = pa.prepare_decode(dev["q8"], dev["qs"], c.k_cache, c.k_scale, c.v_cache, c.v_scale,
+                               dev["block_table"], act1, out, S1=case.S1, layout=case.layout,
+                               s2_tile=case.s2_tile, softmax_scale=case.softmax_scale,
+                               overlap_prologue=2)
+
+    def restore():
+        for t, sn in zip((c.k_cache, c.v_cache, c.k_scale), snap):
+            t.copy_(sn)
+        out.fill_(float("nan"))
+
+    def check():
+        torch.cuda.synchronize()
+        H.compare_bf16(H.to_u16(out), ref)
+        assert np.array_equal(c.k_cache.cpu().numpy(), inp["kc"])
+        assert np.array_equal(c.v_scale.cpu().numpy(), inp["vs"])
+        assert np.array_equal(c.k_scale.cpu().numpy(), inp["ksc"])
+
+    append()
+    attend()
+    check()
+    restore()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    append(s)
+    attend(s)
+    torch.cuda.current_stream().wait_stream(s)
+    check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        restore()
+        cur = torch.cuda.current_stream()
+        append(cur)
+        attend(cur)
+    for _ in range(2):
+        g.replay()
+        check()
+
+
 @pytest.mark.parametrize("round_scale", [True, False])
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("d", [128, 256, 576, 1024])
