@@ -63,8 +63,8 @@ OVERLAP_APPEND = True
 # DRAM traffic of one decode launch on this workload, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources it was taken with.
-DECODE_TRAFFIC = {"sources_sha1": "dd6e60f3cdfe5b009974fbe8dad986e998ae3eb8",
-                  "bytes_per_launch": 57872384 + 106752}
+DECODE_TRAFFIC = {"sources_sha1": "5bd24b40229e25f453dc4324eaa82276b9949e65",
+                  "bytes_per_launch": 57872640 + 110080}
 
 
 def parse_args(argv=None):

@@ -298,7 +298,8 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v)
         tmem_ld8(taddr, v);
     } else {
 #pragma unroll
-        for (int c = 0; c < N; c += 16) tmem_ld16(taddr + c, v + c);
+        for (int c = 0; c + 16 <= N; c += 16) tmem_ld16(taddr + c, v + c);
+        if constexpr (N % 16 == 8) tmem_ld8(taddr + N - 8, v + N - 8);
     }
 }
 
@@ -753,11 +754,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t vph = 0;
     int hcount = 0, tcount = 0, hs = 0, nrows = 0;
     bool first = true;
-    float Lp[NR];               // this thread's share of the row sums (running-max units)
+    // Row sums (running-max units). 16 rows: this thread's share of every row,
+    // reduced over the lanes at unit end. 32 rows: reduced over the lanes
+    // every tile into one value per lane (row rho), which frees the registers
+    // that let a 24-row unit keep its scores across the row-maximum barrier.
+    constexpr bool kRowSumPerTile = NR == 32;
+    float Lp[kRowSumPerTile ? 1 : NR];
+    float Lr = 0.f;
     float Oa[HR];               // O^T[32 q4 + lane][hh * HR + k], times 448
     float Mref = -INFINITY;     // running max of row rho (scaled log2 units)
 #pragma unroll
-    for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
+    for (int r = 0; r < (kRowSumPerTile ? 1 : NR); ++r) Lp[r] = 0.f;
 #pragma unroll
     for (int k = 0; k < HR; ++k) Oa[k] = 0.f;
     {
@@ -881,7 +888,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < NR) sm.wst[warp][3][lane] = lane < nrows ? sm.qs[hs][lane] * p.sscale : 0.f;
             __syncwarp();
 #pragma unroll
-            for (int r = 0; r < NR; ++r) Lp[r] = 0.f;
+            for (int r = 0; r < (kRowSumPerTile ? 1 : NR); ++r) Lp[r] = 0.f;
+            Lr = 0.f;
 #pragma unroll
             for (int k = 0; k < HR; ++k) Oa[k] = 0.f;
             Mref = -INFINITY;
@@ -910,8 +918,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // do not fit in registers next to the rest of the state (they spill):
         // each block is read from tensor memory twice instead, once for the
         // row maxima and once for P, and the S^T buffer is released after the
-        // second read.
-        constexpr bool kReload = NR == 32 && MBW > 1;
+        // second read. With 24 computed rows they fit and are read once.
+        constexpr bool kReload = NR == 32 && MBW > 1 && NRV == NR;
         constexpr int SVB = kReload ? 1 : MBW;
         mbar_wait(&sm.s_full[sb], (tcount / NSB) & 1, p.err, 256, &sm.abort, p.wait_ns);
         tc_fence_after();
@@ -920,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < MBW; ++jj) {
                 const int mb = hh * MBW + jj;
-                if (mb < nb) tmem_ld_cols<NR>(tl + sb * SC + mb * NR, sv[jj]);
+                if (mb < nb) tmem_ld_cols<NRV>(tl + sb * SC + mb * NR, sv[jj]);
             }
             tmem_wait_ld();
             tc_fence_before();
@@ -935,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (!kReload) {
             float qsc[NR];
 #pragma unroll
-            for (int r4 = 0; r4 < NR / 4; ++r4) {
+            for (int r4 = 0; r4 < NRV / 4; ++r4) {
                 const float4 q4v = *reinterpret_cast<const float4*>(&sm.wst[warp][3][4 * r4]);
                 qsc[4 * r4 + 0] = q4v.x;
                 qsc[4 * r4 + 1] = q4v.y;
@@ -948,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (mb < nb) {
                     const bool ok = mb * kBS + 32 * q4 + lane < valid;
 #pragma unroll
-                    for (int r = 0; r < NR; ++r) {
+                    for (int r = 0; r < NRV; ++r) {
                         const float xv = ok ? (sv[jj][r] * qsc[r]) * ksv[jj] : -INFINITY;
                         sv[jj][r] = xv;
                         mloc[r] = fmaxf(mloc[r], xv);
@@ -1104,14 +1112,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- running sums; this tile's O^T is folded with the next tile ----
+        if constexpr (kRowSumPerTile) {
+            const float wls = lane_reduce<NR, false>(ls, lane);
+            Lr = Lr * sm.wfold[tcount & 1][warp][0][rho] + wls * sm.wfold[tcount & 1][warp][1][rho];
+        } else {
 #pragma unroll
-        for (int r4 = 0; r4 < NR / 4; ++r4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(&sm.wfold[tcount & 1][warp][0][4 * r4]);
-            const float4 b4 = *reinterpret_cast<const float4*>(&sm.wfold[tcount & 1][warp][1][4 * r4]);
-            Lp[4 * r4 + 0] = Lp[4 * r4 + 0] * a4.x + ls[4 * r4 + 0] * b4.x;
-            Lp[4 * r4 + 1] = Lp[4 * r4 + 1] * a4.y + ls[4 * r4 + 1] * b4.y;
-            Lp[4 * r4 + 2] = Lp[4 * r4 + 2] * a4.z + ls[4 * r4 + 2] * b4.z;
-            Lp[4 * r4 + 3] = Lp[4 * r4 + 3] * a4.w + ls[4 * r4 + 3] * b4.w;
+            for (int r4 = 0; r4 < NR / 4; ++r4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(&sm.wfold[tcount & 1][warp][0][4 * r4]);
+                const float4 b4 = *reinterpret_cast<const float4*>(&sm.wfold[tcount & 1][warp][1][4 * r4]);
+                Lp[4 * r4 + 0] = Lp[4 * r4 + 0] * a4.x + ls[4 * r4 + 0] * b4.x;
+                Lp[4 * r4 + 1] = Lp[4 * r4 + 1] * a4.y + ls[4 * r4 + 1] * b4.y;
+                Lp[4 * r4 + 2] = Lp[4 * r4 + 2] * a4.z + ls[4 * r4 + 2] * b4.z;
+                Lp[4 * r4 + 3] = Lp[4 * r4 + 3] * a4.w + ls[4 * r4 + 3] * b4.w;
+            }
         }
         pend = tcount;
         ring_advance<NV, NBT>(vslot, vph, nb);
@@ -1121,10 +1134,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------ unit end ------------------------------
             fold(pend);
             pend = -1;
-            float lsum[NR];
+            float wl = Lr;
+            if constexpr (!kRowSumPerTile) {
+                float lsum[NR];
 #pragma unroll
-            for (int r = 0; r < NR; ++r) lsum[r] = Lp[r];
-            const float wl = lane_reduce<NR, false>(lsum, lane);
+                for (int r = 0; r < NR; ++r) lsum[r] = Lp[r];
+                wl = lane_reduce<NR, false>(lsum, lane);
+            }
             if (rep) sm.redl[warp][rho] = wl;
             named_bar_sync(1, kNCW * 32);
             float L = 0.f;
