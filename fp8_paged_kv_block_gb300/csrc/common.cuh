@@ -140,6 +140,15 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
     }
 }
 
+// Maximum of v over the 32 lanes of the warp, returned to every lane (one
+// warp-wide reduction instruction; every lane must execute it).
+__device__ __forceinline__ float warp_max_f32(float v)
+{
+    float m;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+    return m;
+}
+
 // Generic-proxy writes to shared memory made visible to the async proxy
 // (TMA, tensor core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem()

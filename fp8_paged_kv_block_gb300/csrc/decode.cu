@@ -263,11 +263,11 @@ __device__ __forceinline__ void zero_rows(const DecodeParams& p, int b, int tid,
     for (int64_t k = tid; k < n16; k += nthreads) dst[k] = make_uint4(0, 0, 0, 0);
 }
 
-// Butterfly reduction over the 32 lanes of a warp of N per-lane values (one
-// per query row): on return lane L holds the reduction of row
-// (N == 16 ? L / 2 : L) over all lanes. `a` is clobbered.
-template <int N, bool kMax>
-__device__ __forceinline__ float lane_reduce(float (&a)[N], int lane)
+// Butterfly sum over the 32 lanes of a warp of N per-lane values (one per
+// query row): on return lane L holds the sum of row (N == 16 ? L / 2 : L)
+// over all lanes. `a` is clobbered.
+template <int N>
+__device__ __forceinline__ float lane_sum(float (&a)[N], int lane)
 {
 #pragma unroll
     for (int s = 0; s < 5; ++s) {
@@ -279,15 +279,11 @@ __device__ __forceinline__ float lane_reduce(float (&a)[N], int lane)
         for (int i = 0; i < h; ++i) {
             const float keep = up ? a[i + h] : a[i];
             const float send = up ? a[i] : a[i + h];
-            const float got = __shfl_xor_sync(0xffffffffu, send, o);
-            a[i] = kMax ? fmaxf(keep, got) : keep + got;
+            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
     }
     float v = a[0];
-    if (N == 16) {
-        const float got = __shfl_xor_sync(0xffffffffu, v, 1);
-        v = kMax ? fmaxf(v, got) : v + got;
-    }
+    if (N == 16) v += __shfl_xor_sync(0xffffffffu, v, 1);
     return v;
 }
 
@@ -985,7 +981,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        const float wmax = lane_reduce<NR, true>(mloc, lane);
+        // each row's maximum over the warp's tokens (one warp reduction per
+        // computed row), kept by the lanes that hold row rho
+        float wmax = 0.f;
+#pragma unroll
+        for (int r = 0; r < NRV; ++r) {
+            const float m = warp_max_f32(mloc[r]);
+            wmax = rho == r ? m : wmax;
+        }
         const int rb = tcount & 1;
         if (rep) sm.red[rb][rho][warp] = wmax;
         named_bar_sync(1, kNCW * 32);
@@ -1113,7 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- running sums; this tile's O^T is folded with the next tile ----
         if constexpr (kRowSumPerTile) {
-            const float wls = lane_reduce<NR, false>(ls, lane);
+            const float wls = lane_sum<NR>(ls, lane);
             Lr = Lr * sm.wfold[tcount & 1][warp][0][rho] + wls * sm.wfold[tcount & 1][warp][1][rho];
         } else {
 #pragma unroll
@@ -1139,7 +1142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float lsum[NR];
 #pragma unroll
                 for (int r = 0; r < NR; ++r) lsum[r] = Lp[r];
-                wl = lane_reduce<NR, false>(lsum, lane);
+                wl = lane_sum<NR>(lsum, lane);
             }
             if (rep) sm.redl[warp][rho] = wl;
             named_bar_sync(1, kNCW * 32);
