@@ -656,13 +656,16 @@ def main(argv=None):
         for i in range(i0, i0 + n):
             k = i % NBUF
             append, attend = step_calls(k, i % copies)
+            # the append follows its input copy on the input stream: it writes
+            # only each sequence's newest position, which the previous step's
+            # decode does not read, so it may run beside that decode
             s_in.wait_event(ev_used[k])
             with torch.cuda.stream(s_in):
                 d_packs[k].copy_(h_pack, non_blocking=True)
+            append(s_in)
             ev_in[k].record(s_in)
             main.wait_event(ev_in[k])
             main.wait_event(ev_out[k])
-            append(main)
             attend(main)
             ev_used[k].record(main)
             s_out.wait_event(ev_used[k])
@@ -759,9 +762,11 @@ def main(argv=None):
                     "issue": "the public-API calls of each step (pinned H2D copy of its "
                              "inputs, append, decode, D2H copy of its output; the two library "
                              "calls prepared once per buffer set) captured in a CUDA graph; two "
-                             "input and two output buffers alternate so that a step's copies "
-                             "overlap its neighbours' kernels (copies on their own streams, "
-                             "ordered by events)",
+                             "input and two output buffers alternate; the copy and the append "
+                             "run on an input stream beside the previous step's decode (the "
+                             "append writes only the newest positions, which that decode does "
+                             "not read), the output copy on an output stream, all ordered by "
+                             "events",
                     "eager_us_per_step": ms_e2e_eager / n_e2e * 1e3},
             "clocks": clk,
             "cpu_baseline": cpu,
