@@ -337,13 +337,13 @@ __device__ __forceinline__ void ring_advance(int& slot, uint32_t& ph, int n)
 
 // NRV: the query rows of a chunk that are computed (a multiple of 4, at most
 // NR); rows NRV..NR-1 are MMA padding whose scores, exponentials and P codes
-// are skipped (only used where every chunk has exactly NRV rows).
+// are skipped (only used where every chunk has exactly NRV rows: 12 or 24).
 template <int NR, int S2T, int NRV = NR>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
 {
-    static_assert(NRV % 4 == 0 && NRV <= NR && (NRV == NR || NR == 32), "computed rows");
+    static_assert(NRV % 4 == 0 && NRV <= NR, "computed rows");
     constexpr int NBT = S2T / kBS;               // 128-token blocks (MMA M-blocks) per tile
     constexpr int MBW = NBT >= 2 ? NBT / 2 : 1;  // blocks per consumer warp
     constexpr int SC = NBT * NR;                 // tensor-memory columns of one S^T buffer
@@ -924,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < MBW; ++jj) {
                 const int mb = hh * MBW + jj;
-                if (mb < nb) tmem_ld_cols<NRV>(tl + sb * SC + mb * NR, sv[jj]);
+                if (mb < nb) tmem_ld_cols<(NRV % 8 == 0 ? NRV : NR)>(tl + sb * SC + mb * NR, sv[jj]);
             }
             tmem_wait_ld();
             tc_fence_before();
@@ -1583,8 +1583,10 @@ extern "C" pa_status pa_fp8_decode(const void* q, const float* q_scale, const vo
     if (pl.NR == 16) {
         if (pl.S2T == 128) return launch<16, 128>(tk, tv, prm, s);
         if (pl.S2T == 256) return launch<16, 256>(tk, tv, prm, s);
-        if (pl.S2T == 512) return launch<16, 512>(tk, tv, prm, s);
-        return launch<16, 1024>(tk, tv, prm, s);
+        // 12 rows per kv head (the GLM-4.5 group at S1 = 1): the 4 padding
+        // rows' softmax work is skipped
+        if (pl.S2T == 512) return pl.R == 12 ? launch<16, 512, 12>(tk, tv, prm, s) : launch<16, 512>(tk, tv, prm, s);
+        return pl.R == 12 ? launch<16, 1024, 12>(tk, tv, prm, s) : launch<16, 1024>(tk, tv, prm, s);
     }
     if (pl.S2T == 128) return launch<32, 128>(tk, tv, prm, s);
     if (pl.S2T == 256) return launch<32, 256>(tk, tv, prm, s);
