@@ -63,8 +63,8 @@ OVERLAP_APPEND = True
 # DRAM traffic of one decode launch on this workload, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources it was taken with.
-DECODE_TRAFFIC = {"sources_sha1": "d055a74cfe47a7dd7a437b320b962a7db6a2ceed",
-                  "bytes_per_launch": 57872896 + 103424}
+DECODE_TRAFFIC = {"sources_sha1": "913e24342602e851b8cd2947e066b3eae93f7761",
+                  "bytes_per_launch": 57871104 + 116736}
 
 
 def parse_args(argv=None):
