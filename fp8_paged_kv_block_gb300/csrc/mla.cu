@@ -201,11 +201,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// Warp transpose-reduce of a 32 x 32 block (lane = row, v[c] = column c):
-// returns, in lane l, the reduction of column l over the 32 lanes. v is
-// destroyed.
-template <bool kMax>
-__device__ __forceinline__ float col_reduce(float (&v)[32], int lane)
+// Warp transpose-sum of a 32 x 32 block (lane = row, v[c] = column c):
+// returns, in lane l, the sum of column l over the 32 lanes. v is destroyed.
+__device__ __forceinline__ float col_sum(float (&v)[32], int lane)
 {
 #pragma unroll
     for (int s = 16; s >= 1; s >>= 1) {
@@ -214,8 +212,7 @@ __device__ __forceinline__ float col_reduce(float (&v)[32], int lane)
         for (int i = 0; i < s; ++i) {
             const float send = up ? v[i] : v[i + s];
             const float keep = up ? v[i + s] : v[i];
-            const float got = __shfl_xor_sync(0xffffffffu, send, s);
-            v[i] = kMax ? fmaxf(keep, got) : keep + got;
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
         }
     }
     return v[0];
@@ -519,7 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
             float w[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) w[c] = v[c];
-            sm.red[0][q4][hf * 32 + lane] = col_reduce<true>(w, lane);
+            {
+                // column c's maximum over the warp's 32 keys (one warp reduction
+                // per head column), kept by lane c
+                float cm = 0.f;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float m = warp_max_f32(w[c]);
+                    cm = lane == c ? m : cm;
+                }
+                sm.red[0][q4][hf * 32 + lane] = cm;
+            }
             named_bar_sync(1, kConsWarps * 32);
             const int hc = hf * 32 + lane;
             const float m_t = fmaxf(fmaxf(sm.red[0][0][hc], sm.red[0][1][hc]),
@@ -545,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const MlaParams
 #pragma unroll
             for (int c2 = 0; c2 < 16; ++c2) pk[c2] = pack_bf16(w[2 * c2], w[2 * c2 + 1]);
             __syncwarp();
-            sm.red[1][q4][hc] = col_reduce<false>(w, lane);
+            sm.red[1][q4][hc] = col_sum(w, lane);
             named_bar_sync(1, kConsWarps * 32);
             const float l_t = (sm.red[1][0][hc] + sm.red[1][1][hc]) + (sm.red[1][2][hc] + sm.red[1][3][hc]);
             // ---- running state of head hc and the factor for O^T ----
