@@ -1099,8 +1099,8 @@ MLA_VARIANTS = 2          # top-k selections rotated between steps (each ~172 MB
 # valid only for the kernel source it was taken with.
 # Captured on the 16-sequence case and scaled by the selected rows (x4): each
 # row is read from DRAM once, so the traffic grows in proportion.
-MLA_TRAFFIC = {"sources_sha1": "f10072f4bc2b9234db2c028594393e1055ae42f1", "format": "page",
-               "bytes_per_launch": 4 * (54290176 + 382720)}
+MLA_TRAFFIC = {"sources_sha1": "0d68231f9ece537b28bc832b8f9d4feb72772394", "format": "page",
+               "bytes_per_launch": 4 * (54289152 + 336640)}
 
 
 def mla_sources_sha1() -> str:
