@@ -309,3 +309,24 @@ def test_auto_s2_tile_rule(L):
     assert (pa.decode_workspace_size(16, 1, 96, 8, num_ctas=152)
             == pa.decode_workspace_size(16, 1, 96, 8, s2_tile=512, num_ctas=152)
             == pa.decode_workspace_size(16, 1, 96, 8, s2_tile=128, num_ctas=152))
+
+
+def test_prepared_calls_validate_before_touching_a_device(L):
+    """prepare_decode / prepare_cache_quant_scatter check their tensors as
+    decode() and cache_quant_scatter() do, before anything reaches the
+    library: host tensors are refused."""
+    torch = pytest.importorskip("torch")
+    import fp8_paged_kv_block_gb300 as pa
+    u8 = torch.zeros((2, 4, 128), dtype=torch.uint8)
+    f32 = torch.zeros((2, 4), dtype=torch.float32)
+    kc = torch.zeros((4, 128, 1, 128), dtype=torch.uint8)
+    ks = torch.zeros((4, 128, 1), dtype=torch.float32)
+    vs = torch.zeros((2, 1, 128), dtype=torch.float32)
+    bt = torch.zeros((2, 1), dtype=torch.int32)
+    act = torch.ones(2, dtype=torch.int32)
+    out = torch.zeros((2, 4, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pa.prepare_decode(u8, f32, kc, ks, kc, ks, bt, act, out)
+    kn = torch.zeros((2, 1, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pa.prepare_cache_quant_scatter(kn, kn, kc, kc, act, ks, vs, act)
